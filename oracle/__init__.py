@@ -1,0 +1,12 @@
+"""Float64 CPU oracle of the headwise-chunked causal GQA attention layer.
+
+TEST INFRASTRUCTURE: only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline of ``bench.py`` use it.  It shares no code with the CUDA path and is
+never called by it.  Every function cites the passage it follows; see
+``attention_layer`` for the readings taken where the pages are silent.
+"""
+from .attention_layer import (  # noqa: F401
+    apply_rope, apply_rope_transpose, bf16_round, causal_attention,
+    layer_backward, layer_forward, layer_loss, project_kv, rms_norm,
+    rms_norm_backward, rope_cos_sin,
+)
