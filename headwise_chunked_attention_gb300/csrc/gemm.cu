@@ -1,0 +1,446 @@
+// Persistent tcgen05 GEMM with fused epilogues.
+//
+//   C[M, N] = sum_k A[m, k] * B[n, k]       (bf16 operands, fp32 in TMEM)
+//
+// One CTA per SM walks the output tiles (BM = 128 rows x BN columns) with a
+// static stride.  Warp roles:
+//   warp 0      TMA producer: 128-byte-swizzled 64-wide K slabs of A and B
+//               into a ring of shared-memory stages;
+//   warp 1      TMEM owner and MMA issuer: tcgen05.mma M=128, N=BN, K=16,
+//               accumulating into one of two TMEM accumulators, so that the
+//               epilogue of tile i overlaps the main loop of tile i+1;
+//   warps 2..5  epilogue: tcgen05.ld of one accumulator row per thread,
+//               then the fused operation and the global store.
+// Operands may be K-major (row-major [M,K] / [N,K]) or MN-major ([K,M] /
+// [K,N]); the layout is chosen by the instruction descriptor's transpose bits
+// and the shared-memory descriptors, the data is never transposed.
+//
+// Epilogues (what the attention layer needs around the attention kernel):
+//   EPI_PROJ        Q/K/V projection of one head chunk: optional per-head
+//                   RMSNorm (Qwen3 geometry), RoPE, bf16 store to workspace;
+//   EPI_F32         Wo-slice partial result: out (+)= O_c Wo_c^T in fp32;
+//   EPI_DO          dO_c = dOut Wo_c with D = rowsum(dO * O) per head;
+//   EPI_F32_ATOMIC  split-K weight gradients, reduced with red.global.add.
+#include <algorithm>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace upipe {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;                      // one 128-byte swizzle atom of bf16
+constexpr int kThreads = 192;
+constexpr uint32_t A_STAGE_BYTES = BM * BK * 2;  // 16 KB
+
+template <int BN>
+struct GemmCfg {
+  static constexpr uint32_t B_STAGE_BYTES = BN * BK * 2;
+  static constexpr uint32_t STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  static constexpr uint32_t TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
+  static constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*bars*/;
+};
+
+struct TileCoord {
+  int m0, n0, kb0, kb1;
+};
+
+__device__ __forceinline__ TileCoord tile_coord(int t, int num_m, int num_n, int kb_total,
+                                                int ksplit) {
+  const int per_split = num_m * num_n;
+  const int ks = t / per_split;
+  const int r = t - ks * per_split;
+  TileCoord c;
+  c.m0 = (r / num_n) * BM;
+  c.n0 = (r % num_n);
+  const int kb_per = (kb_total + ksplit - 1) / ksplit;
+  c.kb0 = ks * kb_per;
+  c.kb1 = min(kb_total, c.kb0 + kb_per);
+  return c;
+}
+
+// ---- epilogue helpers -------------------------------------------------
+
+// cos/sin of pos * w_i from the two-level table: angle = hi part + lo part.
+__device__ __forceinline__ void rope_cs(const float2* __restrict__ hi,
+                                        const float2* __restrict__ lo, long long pos, int half,
+                                        int i, float& c, float& s) {
+  const float2 a = __ldg(hi + (pos >> 10) * half + i);
+  const float2 b = __ldg(lo + (pos & 1023) * half + i);
+  c = a.x * b.x - a.y * b.y;
+  s = a.y * b.x + a.x * b.y;
+}
+
+template <int D>
+__device__ __forceinline__ void epi_proj_row(const EpiParams& ep, const ProjSeg& sg, long long m,
+                                             int n_local, float (&v)[D]) {
+  constexpr int H = D / 2;
+  if (sg.mode == PROJ_NORM_ROPE) {
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < D; ++i) ss = fmaf(v[i], v[i], ss);
+    const float rs = rsqrtf(ss * (1.0f / D) + ep.eps);
+    if (sg.yhat) {
+      bf16* yp = sg.yhat + m * sg.ld_yhat + n_local;
+#pragma unroll
+      for (int i = 0; i < D; i += 8) {
+        uint4 w;
+        w.x = pack_bf16(v[i + 0] * rs, v[i + 1] * rs);
+        w.y = pack_bf16(v[i + 2] * rs, v[i + 3] * rs);
+        w.z = pack_bf16(v[i + 4] * rs, v[i + 5] * rs);
+        w.w = pack_bf16(v[i + 6] * rs, v[i + 7] * rs);
+        *reinterpret_cast<uint4*>(yp + i) = w;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < D; ++i) {
+      const float gmul = sg.gamma ? __ldg(sg.gamma + i) : 1.f;
+      v[i] = v[i] * rs * gmul;
+    }
+  }
+  if (sg.mode != PROJ_PLAIN) {
+#pragma unroll
+    for (int i = 0; i < H; ++i) {
+      float c, s;
+      rope_cs(ep.rope_hi, ep.rope_lo, m, H, i, c, s);
+      const float a = v[i], b = v[i + H];
+      v[i] = a * c - b * s;
+      v[i + H] = b * c + a * s;
+    }
+  }
+  bf16* op = sg.out + m * sg.ld + sg.col0 + n_local;
+#pragma unroll
+  for (int i = 0; i < D; i += 8) {
+    uint4 w;
+    w.x = pack_bf16(v[i + 0], v[i + 1]);
+    w.y = pack_bf16(v[i + 2], v[i + 3]);
+    w.z = pack_bf16(v[i + 4], v[i + 5]);
+    w.w = pack_bf16(v[i + 6], v[i + 7]);
+    *reinterpret_cast<uint4*>(op + i) = w;
+  }
+}
+
+}  // namespace
+
+template <int BN, bool A_MN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap0,
+                const __grid_constant__ CUtensorMap bmap1,
+                const __grid_constant__ CUtensorMap bmap2, const GemmArgs g, const EpiParams ep,
+                int* __restrict__ err) {
+  using Cfg = GemmCfg<BN>;
+  constexpr int STAGES = Cfg::STAGES;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * Cfg::STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* acc_full = empty + STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain_bar = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const int num_m = (g.M + BM - 1) / BM;
+  const int num_n = g.N / BN;
+  const int kb_total = (g.K + BK - 1) / BK;
+  const int ksplit = g.ksplit > 0 ? g.ksplit : 1;
+  const int num_tiles = num_m * num_n * ksplit;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&amap);
+    prefetch_tmap(&bmap0);
+    if (EPI == EPI_PROJ) {
+      prefetch_tmap(&bmap1);
+      prefetch_tmap(&bmap2);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_phase = 0;  // per-stage bit masks
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        const TileCoord tc = tile_coord(t, num_m, num_n, kb_total, ksplit);
+        const int n0 = tc.n0 * BN;
+        const CUtensorMap* bm = &bmap0;
+        int brow = n0;
+        if (EPI == EPI_PROJ) {
+          int s = 0;
+          while (s + 1 < ep.nseg && n0 >= ep.seg[s].n_end) ++s;
+          bm = ep.seg[s].bmap == 0 ? &bmap0 : (ep.seg[s].bmap == 1 ? &bmap1 : &bmap2);
+          brow = ep.seg[s].b_row0 + (n0 - ep.seg[s].n_begin);
+        }
+        for (int kb = tc.kb0; kb < tc.kb1; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, err, abort_flag)) { ok = false; break; }
+          uint8_t* sa = smem + stage * Cfg::STAGE_BYTES;
+          uint8_t* sb = sa + A_STAGE_BYTES;
+          mbar_expect_tx(&full[stage], Cfg::STAGE_BYTES);
+          const int k0 = kb * BK;
+          if (!A_MN) {
+            tma_load_2d(sa, &amap, &full[stage], k0, tc.m0);
+          } else {
+            tma_load_2d(sa, &amap, &full[stage], tc.m0, k0);
+            tma_load_2d(sa + 8192, &amap, &full[stage], tc.m0 + 64, k0);
+          }
+          if (!B_MN) {
+            tma_load_2d(sb, bm, &full[stage], k0, brow);
+          } else {
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i)
+              tma_load_2d(sb + i * 8192, bm, &full[stage], brow + 64 * i, k0);
+          }
+          issued |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (*abort_flag) {
+        // leave no bulk copy in flight into this CTA's shared memory
+        for (int s = 0; s < STAGES; ++s)
+          if (issued & (1u << s)) mbar_wait_drain(&full[s], (issued_phase >> s) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      constexpr uint32_t IDESC = idesc_bf16(BM, BN, A_MN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++it) {
+        const TileCoord tc = tile_coord(t, num_m, num_n, kb_total, ksplit);
+        const int acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, err, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = tc.kb0; kb < tc.kb1; ++kb) {
+          if (!mbar_wait(&full[stage], phase, err, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * Cfg::STAGE_BYTES);
+          const uint32_t sb = sa + A_STAGE_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            uint64_t ad, bd;
+            if (!A_MN) ad = sdesc_sw128(sa + k * 32, 16, 1024);
+            else ad = sdesc_sw128(sa + k * 2048, 8192, 1024);
+            if (!B_MN) bd = sdesc_sw128(sb + k * 32, 16, 1024);
+            else bd = sdesc_sw128(sb + k * 2048, 8192, 1024);
+            mma_ss(d_tmem, ad, bd, IDESC, (kb > tc.kb0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit(&empty[stage]);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        // an empty K range (split-K remainder) commits without MMAs; the
+        // epilogue skips such tiles by the same test
+        mma_commit(&acc_full[acc]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    int it = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
+      const TileCoord tc = tile_coord(t, num_m, num_n, kb_total, ksplit);
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      // warp-uniform: the tcgen05.ld below is warp-collective
+      if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[acc], acc_phase, err, abort_flag))) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(quarter * 32) << 16);
+      const long long m = (long long)tc.m0 + row;
+      const int n0 = tc.n0 * BN;
+      const bool live = (m < g.M) && (tc.kb1 > tc.kb0);
+
+      if constexpr (EPI == EPI_PROJ) {
+        constexpr int D = BN;  // one head per tile
+        float v[D];
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tbase + c * 32, r);
+          tmem_ld_wait(r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[c * 32 + i] = __uint_as_float(r[i]);
+        }
+        if (live) {
+          int s = 0;
+          while (s + 1 < ep.nseg && n0 >= ep.seg[s].n_end) ++s;
+          const ProjSeg& sg = ep.seg[s];
+          const int n_local = n0 - sg.n_begin;
+          if (sg.mode == PROJ_NORM_ROPE && sg.rstd) {
+            float ss = 0.f;
+#pragma unroll
+            for (int i = 0; i < D; ++i) ss = fmaf(v[i], v[i], ss);
+            sg.rstd[(long long)(n_local / D) * g.M + m] = rsqrtf(ss * (1.0f / D) + ep.eps);
+          }
+          epi_proj_row<D>(ep, sg, m, n_local, v);
+        }
+      } else if constexpr (EPI == EPI_DO) {
+        constexpr int D = BN;
+        float dot = 0.f;
+        const int head = n0 / D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tbase + c * 32, r);
+          tmem_ld_wait(r);
+          if (live) {
+            const bf16* op = ep.O + m * ep.ld_o + n0 + c * 32;
+            bf16* dp = ep.dO + m * ep.ld_do + n0 + c * 32;
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+              const uint4 ov = *reinterpret_cast<const uint4*>(op + i);
+              const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+              uint4 w;
+              uint32_t* wp = &w.x;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const float a = __uint_as_float(r[i + 2 * j]);
+                const float b = __uint_as_float(r[i + 2 * j + 1]);
+                const float2 of = __bfloat1622float2(o2[j]);
+                dot = fmaf(a, of.x, dot);
+                dot = fmaf(b, of.y, dot);
+                wp[j] = pack_bf16(a, b);
+              }
+              *reinterpret_cast<uint4*>(dp + i) = w;
+            }
+          }
+        }
+        if (live) ep.D[(long long)head * g.M + m] = dot;
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tbase + c * 32, r);
+          tmem_ld_wait(r);
+          if (live) {
+            float* cp = ep.C + m * ep.ldc + n0 + c * 32;
+            if constexpr (EPI == EPI_F32) {
+#pragma unroll
+              for (int i = 0; i < 32; i += 4) {
+                float4 w = make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
+                                       __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+                if (ep.beta) {
+                  const float4 o = *reinterpret_cast<const float4*>(cp + i);
+                  w.x += o.x; w.y += o.y; w.z += o.z; w.w += o.w;
+                }
+                *reinterpret_cast<float4*>(cp + i) = w;
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; i += 4)
+                red_add_v4_f32(cp + i, __uint_as_float(r[i]), __uint_as_float(r[i + 1]),
+                               __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+    }
+  }
+
+  // --------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    if (*abort_flag) {
+      // make sure no MMA issued by this CTA still writes TMEM
+      if (lane == 0) {
+        mma_commit(drain_bar);
+        mbar_wait_drain(drain_bar, 0);
+      }
+      __syncwarp();
+    }
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host --
+
+template <int BN, bool A_MN, bool B_MN, int EPI>
+static cudaError_t launch_t(const CUtensorMap& amap, const CUtensorMap* bmaps, int nb,
+                            const GemmArgs& g, const EpiParams& ep, int* err, int num_sms,
+                            cudaStream_t stream) {
+  using Cfg = GemmCfg<BN>;
+  auto kfn = gemm_kernel<BN, A_MN, B_MN, EPI>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int num_m = (g.M + BM - 1) / BM;
+  const long long tiles = (long long)num_m * (g.N / BN) * std::max(1, g.ksplit);
+  const int grid = (int)std::max(1LL, std::min<long long>(tiles, num_sms));
+  const CUtensorMap& b1 = nb > 1 ? bmaps[1] : bmaps[0];
+  const CUtensorMap& b2 = nb > 2 ? bmaps[2] : bmaps[0];
+  kfn<<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(amap, bmaps[0], b1, b2, g, ep, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm(int bn, bool a_mn, bool b_mn, EpiKind epi, const CUtensorMap& amap,
+                        const CUtensorMap* bmaps, int nb, const GemmArgs& g, const EpiParams& ep,
+                        int* err, int num_sms, cudaStream_t stream) {
+  if (g.M <= 0 || g.N <= 0) return cudaSuccess;
+  if (g.N % bn != 0) return cudaErrorInvalidValue;
+#define UPIPE_GEMM_CASE(BN_, AMN, BMN, E)                                              \
+  if (bn == BN_ && a_mn == AMN && b_mn == BMN && epi == E)                             \
+    return launch_t<BN_, AMN, BMN, E>(amap, bmaps, nb, g, ep, err, num_sms, stream);
+  // projections (one head per tile: BN = d)
+  UPIPE_GEMM_CASE(64, false, false, EPI_PROJ)
+  UPIPE_GEMM_CASE(128, false, false, EPI_PROJ)
+  // Wo-slice accumulate
+  UPIPE_GEMM_CASE(128, false, false, EPI_F32)
+  UPIPE_GEMM_CASE(256, false, false, EPI_F32)
+  // dO = dOut Wo_c (+ D)
+  UPIPE_GEMM_CASE(64, false, true, EPI_DO)
+  UPIPE_GEMM_CASE(128, false, true, EPI_DO)
+  // dX += dQKV W
+  UPIPE_GEMM_CASE(128, false, true, EPI_F32)
+  UPIPE_GEMM_CASE(256, false, true, EPI_F32)
+  // weight gradients (K = S, split)
+  UPIPE_GEMM_CASE(128, true, true, EPI_F32_ATOMIC)
+  UPIPE_GEMM_CASE(64, true, true, EPI_F32_ATOMIC)
+#undef UPIPE_GEMM_CASE
+  return cudaErrorNotSupported;
+}
+
+}  // namespace upipe

@@ -1,0 +1,141 @@
+// Internal (not exported) interfaces between the translation units of
+// libupipe: kernel launchers and their parameter blocks.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace upipe {
+
+using bf16 = __nv_bfloat16;
+
+// ----------------------------------------------------------- tensor maps --
+
+// Encode a 2-D bf16 tensor map over a row-major matrix [rows, cols] with
+// leading dimension ``ld`` elements, box [box_rows, box_cols] (box_cols * 2
+// must be 128: 128-byte swizzle).  Returns false when the driver refuses.
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                    uint64_t ld, uint32_t box_rows, uint32_t box_cols);
+
+// ------------------------------------------------------------------ GEMM --
+
+enum EpiKind : int {
+  EPI_PROJ = 0,        // bf16 store with optional per-head RMSNorm and RoPE
+  EPI_F32 = 1,         // fp32 store (beta = 0) or read-modify-write add (beta = 1)
+  EPI_DO = 2,          // bf16 store of dO plus D = rowsum(dO * O) per head
+  EPI_F32_ATOMIC = 3,  // fp32 reduction-add (split-K partial sums)
+};
+
+enum ProjMode : int { PROJ_PLAIN = 0, PROJ_ROPE = 1, PROJ_NORM_ROPE = 2 };
+
+// One contiguous run of output columns of the fused projection GEMM.  The
+// GEMM's N range [n_begin, n_end) comes from B map ``bmap`` starting at
+// weight row ``b_row0`` and lands in ``out`` (row stride ``ld``) starting at
+// column ``col0``.
+struct ProjSeg {
+  int n_begin, n_end;
+  int bmap;
+  int b_row0;
+  bf16* out;
+  int ld;
+  int col0;
+  int mode;
+  const float* gamma;  // RMSNorm gain [d], nullptr means ones
+  bf16* yhat;          // optional: normalised, pre-gain, pre-RoPE values (bf16)
+  int ld_yhat;
+  float* rstd;         // optional: 1/sqrt(mean(a^2)+eps) per (head, row): [heads][rows]
+};
+
+struct EpiParams {
+  // EPI_PROJ
+  ProjSeg seg[3];
+  int nseg;
+  const float2* rope_hi;  // [(S >> 10) + 1][d/2] (cos, sin) of (pos & ~1023) * w_i
+  const float2* rope_lo;  // [1024][d/2]          (cos, sin) of (pos & 1023) * w_i
+  float eps;
+  // EPI_F32 / EPI_F32_ATOMIC
+  float* C;
+  long long ldc;
+  int beta;
+  // EPI_DO
+  bf16* dO;
+  int ld_do;
+  const bf16* O;
+  int ld_o;
+  float* D;  // [heads][M]
+};
+
+struct GemmArgs {
+  int M, N, K;      // C[M, N] = sum_k A[m, k] * B[n, k]
+  int ksplit;       // number of K partitions (EPI_F32_ATOMIC only)
+  int head_dim;     // d (EPI_PROJ / EPI_DO)
+};
+
+// a_mn / b_mn: operand stored MN-major (A as [K, M] row-major, B as [K, N]).
+// bmaps: 1..3 maps for B (EPI_PROJ may use one per segment).
+cudaError_t launch_gemm(int bn, bool a_mn, bool b_mn, EpiKind epi, const CUtensorMap& amap,
+                        const CUtensorMap* bmaps, int nbmaps, const GemmArgs& g,
+                        const EpiParams& ep, int* err, int num_sms, cudaStream_t stream);
+
+// ------------------------------------------------------------- attention --
+
+struct AttnFwdArgs {
+  int S;
+  int heads;        // query heads in this launch
+  int group;        // query heads per kv head (GQA)
+  int h0;           // global index of the first query head (kv map)
+  int kv0;          // global index of the first kv head held in K/V buffers
+  bf16* O;          // [S, ldo] bf16, head i at column i*d
+  int ldo;
+  float* lse;       // [heads][S] natural-log LSE (nullptr: not written)
+  long long lse_stride;
+  float scale_log2; // log2(e) / sqrt(d)
+};
+
+cudaError_t launch_attn_fwd(const CUtensorMap& qmap, const CUtensorMap& kmap,
+                            const CUtensorMap& vmap, const AttnFwdArgs& a, int d, int* err,
+                            cudaStream_t stream);
+
+struct AttnBwdArgs {
+  int S, heads, group, h0, kv0, d;
+  const bf16* Q; int ldq;       // [S, ldq]
+  const bf16* K; const bf16* V; int ldkv;
+  const bf16* dO; int ld_do;
+  const float* lse; long long lse_stride;   // caller's LSE, rows of this chunk
+  const float* D;               // [heads][S]
+  float* dQ; int ld_dq;         // fp32 [S, ld_dq], accumulated
+  float* dK; float* dV; int ld_dkv;  // fp32, accumulated across the group's chunks
+  float scale;                  // 1/sqrt(d)
+};
+
+cudaError_t launch_attn_bwd(const AttnBwdArgs& a, cudaStream_t stream);
+
+// ---------------------------------------------------------- elementwise --
+
+cudaError_t launch_rope_table(float2* hi, float2* lo, long long S, int d, double theta,
+                              cudaStream_t stream);
+
+// Backward of (RMSNorm ->) RoPE for one block of heads: g (fp32, gradient of
+// the rotated values) -> bf16 gradient of the projection output; optionally
+// accumulates the gain gradient.
+struct QkBwdArgs {
+  long long S;
+  int heads, d;
+  const float* g; int ld_g;          // [S, ld_g] fp32
+  bf16* out; int ld_out;             // [S, ld_out] bf16
+  int mode;                          // PROJ_ROPE or PROJ_NORM_ROPE
+  const bf16* yhat; int ld_yhat;     // saved normalised values (norm mode)
+  const float* rstd;                 // [heads][S]
+  const float* gamma;                // [d] or nullptr
+  float* dgamma;                     // [d] accumulated (norm mode)
+  const float2* rope_hi; const float2* rope_lo;
+};
+cudaError_t launch_qk_bwd(const QkBwdArgs& a, cudaStream_t stream);
+
+// fp32 [S, ld_in] -> bf16 [S, ld_out] for ``cols`` columns.
+cudaError_t launch_f32_to_bf16(const float* in, int ld_in, bf16* out, int ld_out, long long S,
+                               int cols, cudaStream_t stream);
+
+}  // namespace upipe

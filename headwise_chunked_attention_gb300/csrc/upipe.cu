@@ -1,0 +1,561 @@
+// libupipe host side: argument validation, the workspace planner and the
+// head-chunk scheduler behind the C ABI of include/upipe.h.
+//
+// The chunk loop is the UPipe loop (memeeeeeex.com article, "Untied Ulysses
+// (UPipe)"; liquidgold.cc talk transcript: divide the heads into chunks and
+// reuse all the buffers): for chunk c of ``chunk_heads`` query heads, project
+// the chunk's Q (and its KV group's K/V when the chunk starts a new group)
+// into the workspace, run causal attention for those heads over the whole
+// sequence, and add the chunk's Wo-slice partial result into ``out``.  Every
+// chunk reuses the same workspace views; stream order alone makes the reuse
+// safe, there is no host synchronisation inside the loop.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/upipe.h"
+#include "internal.h"
+
+namespace upipe {
+
+__device__ int g_device_error = 0;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+// --------------------------------------------------------- device state --
+
+struct DeviceState {
+  bool ready = false;
+  int num_sms = 0;
+  int* err = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return UPIPE_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& s = g_dev[dev];
+  if (!s.ready) {
+    if (cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return UPIPE_ERR_CUDA;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return UPIPE_ERR_CUDA;
+    s.err = static_cast<int*>(p);
+    s.ready = true;
+  }
+  *out = &s;
+  return UPIPE_OK;
+}
+
+// ---------------------------------------------------------- tensor maps --
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                    uint32_t box_rows, uint32_t box_cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+
+// ------------------------------------------------------------ validation --
+
+struct Geo {
+  long long S;
+  int hidden, Hq, Hkv, d, ch, g, kvc, nchunks;
+  bool norm;
+};
+
+int check_shape(const upipe_shape_t* sh, Geo* geo) {
+  if (!sh) return UPIPE_ERR_INVALID_ARG;
+  if (sh->S < 1 || sh->S > (int64_t)INT32_MAX - 256) return UPIPE_ERR_INVALID_ARG;
+  if (sh->hidden <= 0 || sh->Hq <= 0 || sh->Hkv <= 0 || sh->d <= 0 || sh->chunk_heads <= 0)
+    return UPIPE_ERR_INVALID_ARG;
+  if (sh->Hq % sh->Hkv != 0 || sh->Hq % sh->chunk_heads != 0) return UPIPE_ERR_INVALID_ARG;
+  const int g = sh->Hq / sh->Hkv;
+  if (!(sh->chunk_heads % g == 0 || g % sh->chunk_heads == 0)) return UPIPE_ERR_INVALID_ARG;
+  if (!(sh->rope_theta > 0.0) || !std::isfinite(sh->rope_theta)) return UPIPE_ERR_INVALID_ARG;
+  if (sh->qk_norm != 0 && sh->qk_norm != 1) return UPIPE_ERR_INVALID_ARG;
+  if (sh->qk_norm && !(sh->norm_eps >= 0.f)) return UPIPE_ERR_INVALID_ARG;
+  if (sh->d != 64 && sh->d != 128) return UPIPE_ERR_UNSUPPORTED;
+  if (sh->hidden % 128 != 0) return UPIPE_ERR_UNSUPPORTED;
+  if ((long long)sh->Hq * sh->d > 65536) return UPIPE_ERR_UNSUPPORTED;
+  geo->S = sh->S;
+  geo->hidden = sh->hidden;
+  geo->Hq = sh->Hq;
+  geo->Hkv = sh->Hkv;
+  geo->d = sh->d;
+  geo->ch = sh->chunk_heads;
+  geo->g = g;
+  geo->kvc = sh->chunk_heads >= g ? sh->chunk_heads / g : 1;
+  geo->nchunks = sh->Hq / sh->chunk_heads;
+  geo->norm = sh->qk_norm != 0;
+  return UPIPE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ----------------------------------------------------------- workspace --
+
+struct Layout {
+  size_t rope_hi, rope_lo, q, k, v, o;            // forward
+  size_t dO, D, dq, dk, dv, yq, rq, yk, rk;       // backward
+  size_t total;
+};
+
+Layout plan(const Geo& g, int mode) {
+  Layout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = off;
+    off += align_up(bytes);
+    return at;
+  };
+  const size_t S = (size_t)g.S, d = (size_t)g.d, ch = (size_t)g.ch, kvc = (size_t)g.kvc;
+  L.rope_hi = take((((size_t)g.S >> 10) + 1) * (d / 2) * sizeof(float2));
+  L.rope_lo = take(1024 * (d / 2) * sizeof(float2));
+  L.q = take(S * ch * d * 2);
+  L.k = take(S * kvc * d * 2);
+  L.v = take(S * kvc * d * 2);
+  L.o = take(S * ch * d * 2);
+  if (mode == 1) {
+    L.dO = take(S * ch * d * 2);
+    L.D = take(ch * S * 4);
+    L.dq = take(S * ch * d * 4);
+    L.dk = take(S * kvc * d * 4);
+    L.dv = take(S * kvc * d * 4);
+    if (g.norm) {
+      L.yq = take(S * ch * d * 2);
+      L.rq = take(ch * S * 4);
+      L.yk = take(S * kvc * d * 2);
+      L.rk = take(kvc * S * 4);
+    }
+  }
+  L.total = off;
+  return L;
+}
+
+int cuda_fail(cudaError_t e) { return e == cudaSuccess ? UPIPE_OK : UPIPE_ERR_CUDA; }
+
+#define UPIPE_TRY(expr)                 \
+  do {                                  \
+    int _rc = (expr);                   \
+    if (_rc != UPIPE_OK) return _rc;    \
+  } while (0)
+#define UPIPE_CUDA(expr) UPIPE_TRY(cuda_fail(expr))
+#define UPIPE_MAP(...) \
+  do { if (!make_tmap_bf16(__VA_ARGS__)) return UPIPE_ERR_CUDA; } while (0)
+
+template <class T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+// Fused projection of one chunk: Q heads [h0, h0+ch) and, when the chunk
+// starts a new KV group, K and V heads [kv0, kv0+kvc).  Each 128-row x d
+// output tile is one head, so a head's values never depend on chunk_heads.
+int project_chunk(const Geo& g, const DeviceState* ds, cudaStream_t st, const CUtensorMap& xmap,
+                  const bf16* Wq, const bf16* Wk, const bf16* Wv, const float* qgw,
+                  const float* kgw, float eps, int h0, int kv0, bool new_group, bf16* Q, bf16* K,
+                  bf16* V, const float2* rhi, const float2* rlo, bf16* yq, float* rq, bf16* yk,
+                  float* rk) {
+  const int d = g.d;
+  CUtensorMap bm[3];
+  EpiParams ep{};
+  ep.rope_hi = rhi;
+  ep.rope_lo = rlo;
+  ep.eps = eps;
+  const int qk_mode = g.norm ? PROJ_NORM_ROPE : PROJ_ROPE;
+  int n = 0, ns = 0;
+  UPIPE_MAP(&bm[0], Wq, (uint64_t)g.Hq * d, g.hidden, g.hidden, d, 64);
+  ep.seg[ns++] = ProjSeg{n, n + g.ch * d, 0, h0 * d, Q, g.ch * d, 0, qk_mode, qgw, yq, g.ch * d, rq};
+  n += g.ch * d;
+  if (new_group) {
+    UPIPE_MAP(&bm[1], Wk, (uint64_t)g.Hkv * d, g.hidden, g.hidden, d, 64);
+    UPIPE_MAP(&bm[2], Wv, (uint64_t)g.Hkv * d, g.hidden, g.hidden, d, 64);
+    ep.seg[ns++] = ProjSeg{n, n + g.kvc * d, 1, kv0 * d, K, g.kvc * d, 0, qk_mode, kgw, yk,
+                           g.kvc * d, rk};
+    n += g.kvc * d;
+    ep.seg[ns++] = ProjSeg{n, n + g.kvc * d, 2, kv0 * d, V, g.kvc * d, 0, PROJ_PLAIN, nullptr,
+                           nullptr, 0, nullptr};
+    n += g.kvc * d;
+  }
+  ep.nseg = ns;
+  GemmArgs ga{(int)g.S, n, g.hidden, 1, d};
+  UPIPE_CUDA(launch_gemm(d, false, false, EPI_PROJ, xmap, bm, new_group ? 3 : 1, ga, ep, ds->err,
+                         ds->num_sms, st));
+  return UPIPE_OK;
+}
+
+int attention_chunk(const Geo& g, const DeviceState* ds, cudaStream_t st, const bf16* Q,
+                    const bf16* K, const bf16* V, int h0, int kv0, bf16* O, int ldo,
+                    float* lse) {
+  const int d = g.d;
+  CUtensorMap qm, km, vm;
+  UPIPE_MAP(&qm, Q, g.S, (uint64_t)g.ch * d, (uint64_t)g.ch * d, 128, 64);
+  UPIPE_MAP(&km, K, g.S, (uint64_t)g.kvc * d, (uint64_t)g.kvc * d, 128, 64);
+  UPIPE_MAP(&vm, V, g.S, (uint64_t)g.kvc * d, (uint64_t)g.kvc * d, 128, 64);
+  AttnFwdArgs a{};
+  a.S = (int)g.S;
+  a.heads = g.ch;
+  a.group = g.g;
+  a.h0 = h0;
+  a.kv0 = kv0;
+  a.O = O;
+  a.ldo = ldo;
+  a.lse = lse;
+  a.lse_stride = g.S;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
+  UPIPE_CUDA(launch_attn_fwd(qm, km, vm, a, d, ds->err, st));
+  return UPIPE_OK;
+}
+
+}  // namespace
+}  // namespace upipe
+
+using namespace upipe;
+
+extern "C" size_t upipe_workspace_bytes(const upipe_shape_t* shape, int mode) {
+  Geo g;
+  if (mode != 0 && mode != 1) return 0;
+  if (check_shape(shape, &g) != UPIPE_OK) return 0;
+  return plan(g, mode).total;
+}
+
+extern "C" int upipe_attn_fwd(const upipe_shape_t* shape, const upipe_bf16* x_,
+                              const upipe_bf16* Wq_, const upipe_bf16* Wk_, const upipe_bf16* Wv_,
+                              const upipe_bf16* Wo_, const float* q_norm_w, const float* k_norm_w,
+                              float* out, float* lse, void* workspace, size_t ws_bytes,
+                              upipe_bf16* attn_o_debug, void* stream) {
+  Geo g;
+  UPIPE_TRY(check_shape(shape, &g));
+  const bf16* x = reinterpret_cast<const bf16*>(x_);
+  const bf16* Wq = reinterpret_cast<const bf16*>(Wq_);
+  const bf16* Wk = reinterpret_cast<const bf16*>(Wk_);
+  const bf16* Wv = reinterpret_cast<const bf16*>(Wv_);
+  const bf16* Wo = reinterpret_cast<const bf16*>(Wo_);
+  bf16* dbg = reinterpret_cast<bf16*>(attn_o_debug);
+  if (!x || !Wq || !Wk || !Wv || !Wo || !out || !lse || !workspace) return UPIPE_ERR_INVALID_ARG;
+  for (const void* p : {(const void*)x, (const void*)Wq, (const void*)Wk, (const void*)Wv,
+                        (const void*)Wo, (const void*)out, (const void*)lse, (const void*)dbg,
+                        (const void*)q_norm_w, (const void*)k_norm_w})
+    if (p && !aligned16(p)) return UPIPE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return UPIPE_ERR_INVALID_ARG;
+  const Layout L = plan(g, 0);
+  if (ws_bytes < L.total) return UPIPE_ERR_WORKSPACE_TOO_SMALL;
+  DeviceState* ds = nullptr;
+  UPIPE_TRY(device_state(&ds));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  float2* rhi = at<float2>(workspace, L.rope_hi);
+  float2* rlo = at<float2>(workspace, L.rope_lo);
+  bf16* Q = at<bf16>(workspace, L.q);
+  bf16* K = at<bf16>(workspace, L.k);
+  bf16* V = at<bf16>(workspace, L.v);
+  bf16* Ows = at<bf16>(workspace, L.o);
+  UPIPE_CUDA(launch_rope_table(rhi, rlo, g.S, g.d, shape->rope_theta, st));
+
+  CUtensorMap xmap;
+  UPIPE_MAP(&xmap, x, g.S, g.hidden, g.hidden, 128, 64);
+  const int out_bn = (g.hidden % 256 == 0) ? 256 : 128;
+  for (int c = 0; c < g.nchunks; ++c) {
+    const int h0 = c * g.ch;
+    const int kv0 = h0 / g.g;
+    const bool new_group = (g.ch >= g.g) || (h0 % g.g == 0);
+    UPIPE_TRY(project_chunk(g, ds, st, xmap, Wq, Wk, Wv, q_norm_w, k_norm_w, shape->norm_eps, h0,
+                            kv0, new_group, Q, K, V, rhi, rlo, nullptr, nullptr, nullptr,
+                            nullptr));
+    bf16* O = dbg ? dbg + (size_t)h0 * g.d : Ows;
+    const int ldo = dbg ? g.Hq * g.d : g.ch * g.d;
+    UPIPE_TRY(attention_chunk(g, ds, st, Q, K, V, h0, kv0, O, ldo, lse + (size_t)h0 * g.S));
+    // out (+)= O_c Wo[:, h0*d : (h0+ch)*d]^T  (the chunk's partial result)
+    CUtensorMap om, wom;
+    UPIPE_MAP(&om, O, g.S, (uint64_t)g.ch * g.d, ldo, 128, 64);
+    UPIPE_MAP(&wom, Wo + (size_t)h0 * g.d, g.hidden, (uint64_t)g.ch * g.d,
+              (uint64_t)g.Hq * g.d, out_bn, 64);
+    EpiParams ep{};
+    ep.C = out;
+    ep.ldc = g.hidden;
+    ep.beta = c > 0;
+    GemmArgs ga{(int)g.S, g.hidden, g.ch * g.d, 1, g.d};
+    UPIPE_CUDA(launch_gemm(out_bn, false, false, EPI_F32, om, &wom, 1, ga, ep, ds->err,
+                           ds->num_sms, st));
+  }
+  return UPIPE_OK;
+}
+
+extern "C" int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x_,
+                              const upipe_bf16* Wq_, const upipe_bf16* Wk_, const upipe_bf16* Wv_,
+                              const upipe_bf16* Wo_, const float* q_norm_w, const float* k_norm_w,
+                              const upipe_bf16* dout_, const float* lse, float* dx, float* dWq,
+                              float* dWk, float* dWv, float* dWo, float* dq_norm_w,
+                              float* dk_norm_w, void* workspace, size_t ws_bytes, void* stream) {
+  Geo g;
+  UPIPE_TRY(check_shape(shape, &g));
+  const bf16* x = reinterpret_cast<const bf16*>(x_);
+  const bf16* Wq = reinterpret_cast<const bf16*>(Wq_);
+  const bf16* Wk = reinterpret_cast<const bf16*>(Wk_);
+  const bf16* Wv = reinterpret_cast<const bf16*>(Wv_);
+  const bf16* Wo = reinterpret_cast<const bf16*>(Wo_);
+  const bf16* dout = reinterpret_cast<const bf16*>(dout_);
+  if (!x || !Wq || !Wk || !Wv || !Wo || !dout || !lse || !dx || !dWq || !dWk || !dWv || !dWo ||
+      !workspace)
+    return UPIPE_ERR_INVALID_ARG;
+  if (g.norm && (!dq_norm_w || !dk_norm_w)) return UPIPE_ERR_INVALID_ARG;
+  for (const void* p : {(const void*)x, (const void*)Wq, (const void*)Wk, (const void*)Wv,
+                        (const void*)Wo, (const void*)dout, (const void*)lse, (const void*)dx,
+                        (const void*)dWq, (const void*)dWk, (const void*)dWv, (const void*)dWo,
+                        (const void*)q_norm_w, (const void*)k_norm_w, (const void*)dq_norm_w,
+                        (const void*)dk_norm_w})
+    if (p && !aligned16(p)) return UPIPE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return UPIPE_ERR_INVALID_ARG;
+  const Layout L = plan(g, 1);
+  if (ws_bytes < L.total) return UPIPE_ERR_WORKSPACE_TOO_SMALL;
+  DeviceState* ds = nullptr;
+  UPIPE_TRY(device_state(&ds));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int d = g.d;
+  const size_t S = (size_t)g.S;
+
+  float2* rhi = at<float2>(workspace, L.rope_hi);
+  float2* rlo = at<float2>(workspace, L.rope_lo);
+  bf16* Q = at<bf16>(workspace, L.q);
+  bf16* K = at<bf16>(workspace, L.k);
+  bf16* V = at<bf16>(workspace, L.v);
+  bf16* Ows = at<bf16>(workspace, L.o);
+  bf16* dO = at<bf16>(workspace, L.dO);
+  float* Dv = at<float>(workspace, L.D);
+  float* dQ = at<float>(workspace, L.dq);
+  float* dK = at<float>(workspace, L.dk);
+  float* dV = at<float>(workspace, L.dv);
+  bf16* yq = g.norm ? at<bf16>(workspace, L.yq) : nullptr;
+  float* rq = g.norm ? at<float>(workspace, L.rq) : nullptr;
+  bf16* yk = g.norm ? at<bf16>(workspace, L.yk) : nullptr;
+  float* rk = g.norm ? at<float>(workspace, L.rk) : nullptr;
+
+  UPIPE_CUDA(launch_rope_table(rhi, rlo, g.S, d, shape->rope_theta, st));
+  // split-K weight gradients accumulate with reductions: start from zero
+  UPIPE_CUDA(cudaMemsetAsync(dWq, 0, sizeof(float) * (size_t)g.Hq * d * g.hidden, st));
+  UPIPE_CUDA(cudaMemsetAsync(dWk, 0, sizeof(float) * (size_t)g.Hkv * d * g.hidden, st));
+  UPIPE_CUDA(cudaMemsetAsync(dWv, 0, sizeof(float) * (size_t)g.Hkv * d * g.hidden, st));
+  UPIPE_CUDA(cudaMemsetAsync(dWo, 0, sizeof(float) * (size_t)g.Hq * d * g.hidden, st));
+  if (g.norm) {
+    UPIPE_CUDA(cudaMemsetAsync(dq_norm_w, 0, sizeof(float) * d, st));
+    UPIPE_CUDA(cudaMemsetAsync(dk_norm_w, 0, sizeof(float) * d, st));
+  }
+
+  CUtensorMap xmap, x_mn, dout_k, dout_mn;
+  UPIPE_MAP(&xmap, x, g.S, g.hidden, g.hidden, 128, 64);       // A, K-major
+  UPIPE_MAP(&x_mn, x, g.S, g.hidden, g.hidden, 64, 64);        // B of dW = dA^T x (MN-major)
+  UPIPE_MAP(&dout_k, dout, g.S, g.hidden, g.hidden, 128, 64);  // A of dO = dout Wo_c
+  UPIPE_MAP(&dout_mn, dout, g.S, g.hidden, g.hidden, 64, 64);  // A of dWo = dout^T O
+  const int dx_bn = (g.hidden % 256 == 0) ? 256 : 128;
+  const int ksplit_w = std::max(1, std::min(64, (int)((S + 8191) / 8192)));
+  bool dx_started = false;
+
+  auto dx_gemm = [&](const bf16* dA, int ncols, int ld_a, const bf16* W) -> int {
+    // dx (+)= dA[S, ncols] W[ncols rows, hidden]
+    CUtensorMap am, bm;
+    UPIPE_MAP(&am, dA, g.S, (uint64_t)ncols, (uint64_t)ld_a, 128, 64);
+    UPIPE_MAP(&bm, W, (uint64_t)ncols, g.hidden, g.hidden, 64, 64);
+    EpiParams ep{};
+    ep.C = dx;
+    ep.ldc = g.hidden;
+    ep.beta = dx_started ? 1 : 0;
+    GemmArgs ga{(int)g.S, g.hidden, ncols, 1, d};
+    UPIPE_CUDA(launch_gemm(dx_bn, false, true, EPI_F32, am, &bm, 1, ga, ep, ds->err,
+                           ds->num_sms, st));
+    dx_started = true;
+    return UPIPE_OK;
+  };
+  auto dw_gemm = [&](const bf16* dA, int ncols, int ld_a, float* dW) -> int {
+    // dW[ncols, hidden] += dA^T x  (K = S, split and reduced)
+    CUtensorMap am;
+    UPIPE_MAP(&am, dA, g.S, (uint64_t)ncols, (uint64_t)ld_a, 64, 64);
+    EpiParams ep{};
+    ep.C = dW;
+    ep.ldc = g.hidden;
+    GemmArgs ga{ncols, g.hidden, (int)g.S, ksplit_w, d};
+    UPIPE_CUDA(launch_gemm(128, true, true, EPI_F32_ATOMIC, am, &x_mn, 1, ga, ep, ds->err,
+                           ds->num_sms, st));
+    return UPIPE_OK;
+  };
+
+  for (int c = 0; c < g.nchunks; ++c) {
+    const int h0 = c * g.ch;
+    const int kv0 = h0 / g.g;
+    const bool new_group = (g.ch >= g.g) || (h0 % g.g == 0);
+    const bool last_of_group = (g.ch >= g.g) || ((h0 + g.ch) % g.g == 0);
+    // 1. recompute Q (and K, V) and the attention output of the chunk
+    UPIPE_TRY(project_chunk(g, ds, st, xmap, Wq, Wk, Wv, q_norm_w, k_norm_w, shape->norm_eps, h0,
+                            kv0, new_group, Q, K, V, rhi, rlo, yq, rq, yk, rk));
+    if (new_group) {
+      UPIPE_CUDA(cudaMemsetAsync(dK, 0, sizeof(float) * S * g.kvc * d, st));
+      UPIPE_CUDA(cudaMemsetAsync(dV, 0, sizeof(float) * S * g.kvc * d, st));
+    }
+    UPIPE_TRY(attention_chunk(g, ds, st, Q, K, V, h0, kv0, Ows, g.ch * d, nullptr));
+    // 2. dO_c = dout Wo_c, D = rowsum(dO * O); dWo_c = dout^T O_c
+    {
+      CUtensorMap wom;
+      UPIPE_MAP(&wom, Wo + (size_t)h0 * d, g.hidden, (uint64_t)g.ch * d, (uint64_t)g.Hq * d, 64,
+                64);
+      EpiParams ep{};
+      ep.dO = dO;
+      ep.ld_do = g.ch * d;
+      ep.O = Ows;
+      ep.ld_o = g.ch * d;
+      ep.D = Dv;
+      GemmArgs ga{(int)g.S, g.ch * d, g.hidden, 1, d};
+      UPIPE_CUDA(launch_gemm(d, false, true, EPI_DO, dout_k, &wom, 1, ga, ep, ds->err,
+                             ds->num_sms, st));
+      CUtensorMap om;
+      UPIPE_MAP(&om, Ows, g.S, (uint64_t)g.ch * d, (uint64_t)g.ch * d, 64, 64);
+      EpiParams ep2{};
+      ep2.C = dWo + (size_t)h0 * d;
+      ep2.ldc = (long long)g.Hq * d;
+      GemmArgs gb{g.hidden, g.ch * d, (int)g.S, ksplit_w, d};
+      const int bn = (g.ch * d) % 128 == 0 ? 128 : 64;
+      UPIPE_CUDA(launch_gemm(bn, true, true, EPI_F32_ATOMIC, dout_mn, &om, 1, gb, ep2, ds->err,
+                             ds->num_sms, st));
+    }
+    // 3. attention backward: dQ_c (fresh), dK/dV (accumulated over the group)
+    UPIPE_CUDA(cudaMemsetAsync(dQ, 0, sizeof(float) * S * g.ch * d, st));
+    {
+      AttnBwdArgs a{};
+      a.S = (int)g.S;
+      a.heads = g.ch;
+      a.group = g.g;
+      a.h0 = h0;
+      a.kv0 = kv0;
+      a.d = d;
+      a.Q = Q;
+      a.ldq = g.ch * d;
+      a.K = K;
+      a.V = V;
+      a.ldkv = g.kvc * d;
+      a.dO = dO;
+      a.ld_do = g.ch * d;
+      a.lse = lse + (size_t)h0 * S;
+      a.lse_stride = g.S;
+      a.D = Dv;
+      a.dQ = dQ;
+      a.ld_dq = g.ch * d;
+      a.dK = dK;
+      a.dV = dV;
+      a.ld_dkv = g.kvc * d;
+      a.scale = (float)(1.0 / std::sqrt((double)d));
+      UPIPE_CUDA(launch_attn_bwd(a, st));
+    }
+    // 4. dQ -> gradient of the Q projection output (RoPE^T, RMSNorm backward),
+    //    bf16 into the dO buffer (dO is dead now); dx += dA_q Wq_c;
+    //    dWq_c = dA_q^T x
+    {
+      QkBwdArgs q{};
+      q.S = g.S;
+      q.heads = g.ch;
+      q.d = d;
+      q.g = dQ;
+      q.ld_g = g.ch * d;
+      q.out = dO;
+      q.ld_out = g.ch * d;
+      q.mode = g.norm ? PROJ_NORM_ROPE : PROJ_ROPE;
+      q.yhat = yq;
+      q.ld_yhat = g.ch * d;
+      q.rstd = rq;
+      q.gamma = q_norm_w;
+      q.dgamma = dq_norm_w;
+      q.rope_hi = rhi;
+      q.rope_lo = rlo;
+      UPIPE_CUDA(launch_qk_bwd(q, st));
+      UPIPE_TRY(dx_gemm(dO, g.ch * d, g.ch * d, Wq + (size_t)h0 * d * g.hidden));
+      UPIPE_TRY(dw_gemm(dO, g.ch * d, g.ch * d, dWq + (size_t)h0 * d * g.hidden));
+    }
+    // 5. at the group's last chunk: dK -> dA_k (bf16 over K), dV -> bf16 over V
+    if (last_of_group) {
+      QkBwdArgs q{};
+      q.S = g.S;
+      q.heads = g.kvc;
+      q.d = d;
+      q.g = dK;
+      q.ld_g = g.kvc * d;
+      q.out = K;
+      q.ld_out = g.kvc * d;
+      q.mode = g.norm ? PROJ_NORM_ROPE : PROJ_ROPE;
+      q.yhat = yk;
+      q.ld_yhat = g.kvc * d;
+      q.rstd = rk;
+      q.gamma = k_norm_w;
+      q.dgamma = dk_norm_w;
+      q.rope_hi = rhi;
+      q.rope_lo = rlo;
+      UPIPE_CUDA(launch_qk_bwd(q, st));
+      UPIPE_CUDA(launch_f32_to_bf16(dV, g.kvc * d, V, g.kvc * d, g.S, g.kvc * d, st));
+      UPIPE_TRY(dx_gemm(K, g.kvc * d, g.kvc * d, Wk + (size_t)kv0 * d * g.hidden));
+      UPIPE_TRY(dx_gemm(V, g.kvc * d, g.kvc * d, Wv + (size_t)kv0 * d * g.hidden));
+      UPIPE_TRY(dw_gemm(K, g.kvc * d, g.kvc * d, dWk + (size_t)kv0 * d * g.hidden));
+      UPIPE_TRY(dw_gemm(V, g.kvc * d, g.kvc * d, dWv + (size_t)kv0 * d * g.hidden));
+    }
+  }
+  return UPIPE_OK;
+}
+
+extern "C" int upipe_last_error(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return UPIPE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return UPIPE_ERR_CUDA;
+  const int zero = 0;
+  if (v != 0 && cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess)
+    return UPIPE_ERR_CUDA;
+  return v;
+}
+
+extern "C" const char* upipe_strerror(int code) {
+  switch (code) {
+    case UPIPE_OK: return "ok";
+    case UPIPE_ERR_INVALID_ARG: return "invalid argument";
+    case UPIPE_ERR_UNSUPPORTED: return "unsupported shape";
+    case UPIPE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case UPIPE_ERR_CUDA: return "CUDA error";
+    case UPIPE_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    default: return "unknown error";
+  }
+}

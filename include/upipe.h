@@ -1,0 +1,130 @@
+/*
+ * upipe.h - C ABI of libupipe: the causal GQA attention layer computed one
+ * head chunk at a time with one reused workspace, on a single GB300 (sm_103a).
+ *
+ * The operation.  Untied Ulysses / UPipe ("Untied Ulysses: Memory-Efficient
+ * Context Parallelism via Headwise Chunking"; memeeeeeex.com article, section
+ * "Untied Ulysses (UPipe)"; talk transcript on liquidgold.cc): the query heads
+ * a GPU owns are split into chunks processed one after another; each chunk
+ * (re)computes its heads, runs their attention over the whole sequence, and
+ * stores its partial result, while the next chunk reuses the buffers the
+ * previous one allocated.  On one GPU this is the rank-local work of one
+ * Ulysses rank with the all-to-all exchanges left out.  Per chunk c of
+ * ``chunk_heads`` query heads h (kv head floor(h / (Hq/Hkv))):
+ *     q_h = RoPE(Norm_q(x Wq_h^T)),  k = RoPE(Norm_k(x Wk_g^T)),  v = x Wv_g^T
+ *     o_h = softmax(q_h k^T / sqrt(d), causal) v,  lse_h = log-sum-exp of a row
+ *     out += sum_{h in c} o_h Wo[:, h*d:(h+1)*d]^T
+ * Norm is the per-head RMSNorm of the Qwen3 geometry (qk_norm = 1) and the
+ * identity otherwise; RoPE rotates pairs (i, i + d/2) by pos * theta^(-2i/d).
+ *
+ * Conventions for every call.
+ *  - bf16 tensors are passed as upipe_bf16 (raw 16-bit storage); all matrices
+ *    are row-major with the nn.Linear weight layout [out_features, in_features]:
+ *      x, dout [S, hidden];  Wq [Hq*d, hidden];  Wk, Wv [Hkv*d, hidden];
+ *      Wo [hidden, Hq*d];    q_norm_w, k_norm_w [d] (fp32; NULL means ones).
+ *  - Pointers named x, W*, out, lse, d*, workspace are DEVICE pointers of the
+ *    current CUDA device; every buffer must be 16-byte aligned.
+ *  - ``stream`` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *    enqueue work on it and return; nothing is synchronised.  Two calls in
+ *    flight at once must not share a workspace.
+ *  - Ownership: the caller owns every buffer.  The library allocates no device
+ *    or host memory of its own; all temporaries live in ``workspace``.
+ *  - Errors: every argument is validated on the host before the first launch;
+ *    a failed check returns a code and launches nothing.  A device-side wait
+ *    that exceeds its time limit is reported by upipe_last_error().
+ */
+#ifndef UPIPE_H_
+#define UPIPE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t upipe_bf16;
+
+/* Geometry of one attention layer and its head chunking.
+ *   S            tokens (full sequence), 1 <= S <= 2^31 - 256
+ *   hidden       model width, a multiple of 128
+ *   Hq, Hkv      query and key/value heads; Hkv divides Hq
+ *   d            head dimension: 64 or 128
+ *   chunk_heads  query heads per chunk; divides Hq, and either
+ *                (Hq/Hkv) divides chunk_heads or chunk_heads divides (Hq/Hkv)
+ *   rope_theta   RoPE base (> 0)
+ *   qk_norm      0: no q/k normalisation (Llama); 1: per-head RMSNorm on q and
+ *                k before RoPE (Qwen3)
+ *   norm_eps     RMSNorm epsilon (added to mean(v^2) inside the root) */
+typedef struct {
+  int64_t S;
+  int32_t hidden, Hq, Hkv, d, chunk_heads;
+  double rope_theta;
+  int32_t qk_norm;
+  float norm_eps;
+} upipe_shape_t;
+
+enum {
+  UPIPE_OK = 0,
+  UPIPE_ERR_INVALID_ARG = 1,          /* NULL pointer, bad size, misalignment */
+  UPIPE_ERR_UNSUPPORTED = 2,          /* a shape this build does not handle  */
+  UPIPE_ERR_WORKSPACE_TOO_SMALL = 3,  /* ws_bytes < upipe_workspace_bytes()  */
+  UPIPE_ERR_CUDA = 4,                 /* a CUDA runtime/driver call failed    */
+  UPIPE_ERR_DEVICE_TIMEOUT = 5        /* a kernel's bounded wait expired      */
+};
+
+/* Workspace bytes needed by upipe_attn_fwd (mode 0) or upipe_attn_bwd
+ * (mode 1) for this shape, or 0 if the shape is invalid.  Pure host function.
+ * The bytes are affine in chunk_heads: the per-chunk Q/O (and backward) parts
+ * scale with chunk_heads, the K/V part is one KV group (or chunk_heads/(Hq/Hkv)
+ * groups when a chunk spans several), plus a RoPE table of
+ * ((S >> 10) + 1 + 1024) * d/2 float2 entries.  "The next chunk reuses the
+ * buffers the previous chunk allocated" (memeeeeeex.com, "Untied Ulysses
+ * (UPipe)"): this one allocation is that buffer. */
+size_t upipe_workspace_bytes(const upipe_shape_t* shape, int mode);
+
+/* Forward of the layer, chunk by chunk (the UPipe loop).
+ *   out   [S, hidden] fp32, overwritten (the first chunk stores, later chunks
+ *         add their Wo-slice partial results)
+ *   lse   [Hq, S] fp32 natural-log log-sum-exp of each head's scaled scores
+ *   attn_o_debug  NULL, or [S, Hq*d] bf16: receives every head's attention
+ *         output o_h at columns h*d (for chunk-invariance checks)
+ *   workspace / ws_bytes: device buffer of at least
+ *         upipe_workspace_bytes(shape, 0) bytes, 256-byte aligned
+ * Returns UPIPE_OK or an error code (nothing launched on error). */
+int upipe_attn_fwd(const upipe_shape_t* shape, const upipe_bf16* x, const upipe_bf16* Wq,
+                   const upipe_bf16* Wk, const upipe_bf16* Wv, const upipe_bf16* Wo,
+                   const float* q_norm_w, const float* k_norm_w, float* out, float* lse,
+                   void* workspace, size_t ws_bytes, upipe_bf16* attn_o_debug, void* stream);
+
+/* Backward of the layer for L = sum(out * dout), chunk by chunk, recomputing
+ * each chunk's Q/K/V and attention output in the reused workspace (activation
+ * recomputation: aipmzone.com / dimanyen.com, "activation checkpointing").
+ *   dout  [S, hidden] bf16 upstream gradient
+ *   lse   [Hq, S] fp32 from upipe_attn_fwd on the same inputs
+ *   dx    [S, hidden] fp32, overwritten
+ *   dWq [Hq*d, hidden], dWk/dWv [Hkv*d, hidden], dWo [hidden, Hq*d]: fp32,
+ *         overwritten
+ *   dq_norm_w, dk_norm_w [d] fp32, overwritten when qk_norm = 1 (may be NULL
+ *         when qk_norm = 0)
+ *   workspace: at least upipe_workspace_bytes(shape, 1) bytes. */
+int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x, const upipe_bf16* Wq,
+                   const upipe_bf16* Wk, const upipe_bf16* Wv, const upipe_bf16* Wo,
+                   const float* q_norm_w, const float* k_norm_w, const upipe_bf16* dout,
+                   const float* lse, float* dx, float* dWq, float* dWk, float* dWv, float* dWo,
+                   float* dq_norm_w, float* dk_norm_w, void* workspace, size_t ws_bytes,
+                   void* stream);
+
+/* Synchronises the current device, then returns and clears the device error
+ * word (UPIPE_OK or UPIPE_ERR_DEVICE_TIMEOUT), or UPIPE_ERR_CUDA if the
+ * device reports a CUDA error. */
+int upipe_last_error(void);
+
+/* Static description of an error code. */
+const char* upipe_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* UPIPE_H_ */
