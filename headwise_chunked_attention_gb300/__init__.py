@@ -1,0 +1,11 @@
+"""Headwise-chunked causal GQA attention (Untied Ulysses / UPipe) on GB300.
+
+Thin Python binding of the C ABI in ``include/upipe.h``: argument marshalling
+only.  Every step of the layer runs in the CUDA kernels of ``libupipe.so``;
+PyTorch only provides device memory and the current stream.  There is no CPU
+fallback: without the built library every call raises.
+"""
+from ._binding import (  # noqa: F401
+    UpipeError, Shape, attn_bwd, attn_fwd, last_error, lib, lib_path,
+    workspace_bytes, ERR_NAMES,
+)

@@ -1,0 +1,130 @@
+"""ctypes marshalling for libupipe (include/upipe.h).  No computation here."""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libupipe.so")
+_lib = None
+
+ERR_NAMES = {0: "UPIPE_OK", 1: "UPIPE_ERR_INVALID_ARG", 2: "UPIPE_ERR_UNSUPPORTED",
+             3: "UPIPE_ERR_WORKSPACE_TOO_SMALL", 4: "UPIPE_ERR_CUDA",
+             5: "UPIPE_ERR_DEVICE_TIMEOUT"}
+
+
+class UpipeError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {ERR_NAMES.get(code, code)}")
+
+
+class Shape(ctypes.Structure):
+    """upipe_shape_t."""
+    _fields_ = [("S", ctypes.c_int64), ("hidden", ctypes.c_int32),
+                ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+                ("d", ctypes.c_int32), ("chunk_heads", ctypes.c_int32),
+                ("rope_theta", ctypes.c_double), ("qk_norm", ctypes.c_int32),
+                ("norm_eps", ctypes.c_float)]
+
+    @classmethod
+    def of(cls, w, chunk_heads: Optional[int] = None, S: Optional[int] = None):
+        """From any object with S, hidden, Hq, Hkv, d, rope_theta, qk_norm,
+        norm_eps (e.g. a workload) and a chunk size."""
+        ch = chunk_heads if chunk_heads is not None else w.chunk_heads[0]
+        return cls(S if S is not None else w.S, w.hidden, w.Hq, w.Hkv, w.d, ch,
+                   float(w.rope_theta), int(bool(w.qk_norm)), float(w.norm_eps))
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """Load libupipe.so (built by ``build()``); raise if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"libupipe.so not built ({_LIB_PATH}); run "
+                "headwise_chunked_attention_gb300.build.build()")
+        L = ctypes.CDLL(_LIB_PATH)
+        P = ctypes.c_void_p
+        L.upipe_workspace_bytes.argtypes = [ctypes.POINTER(Shape), ctypes.c_int]
+        L.upipe_workspace_bytes.restype = ctypes.c_size_t
+        L.upipe_attn_fwd.argtypes = [ctypes.POINTER(Shape)] + [P] * 9 + [ctypes.c_size_t, P, P]
+        L.upipe_attn_fwd.restype = ctypes.c_int
+        L.upipe_attn_bwd.argtypes = ([ctypes.POINTER(Shape)] + [P] * 17 +
+                                     [ctypes.c_size_t, P])
+        L.upipe_attn_bwd.restype = ctypes.c_int
+        L.upipe_last_error.argtypes = []
+        L.upipe_last_error.restype = ctypes.c_int
+        L.upipe_strerror.argtypes = [ctypes.c_int]
+        L.upipe_strerror.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def workspace_bytes(shape: Shape, mode: int = 0) -> int:
+    return int(lib().upipe_workspace_bytes(ctypes.byref(shape), mode))
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise UpipeError(rc, where)
+
+
+def attn_fwd(shape: Shape, x, Wq, Wk, Wv, Wo, out, lse, workspace,
+             q_norm_w=None, k_norm_w=None, attn_o_debug=None, stream=None):
+    """upipe_attn_fwd on torch tensors (bf16 inputs, fp32 out/lse, uint8
+    workspace); enqueues on ``stream`` (default: current stream)."""
+    bf = torch.bfloat16
+    rc = lib().upipe_attn_fwd(
+        ctypes.byref(shape), _ptr(x, bf, "x"), _ptr(Wq, bf, "Wq"), _ptr(Wk, bf, "Wk"),
+        _ptr(Wv, bf, "Wv"), _ptr(Wo, bf, "Wo"), _ptr(q_norm_w, torch.float32, "q_norm_w"),
+        _ptr(k_norm_w, torch.float32, "k_norm_w"), _ptr(out, torch.float32, "out"),
+        _ptr(lse, torch.float32, "lse"), _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(),
+        _ptr(attn_o_debug, bf, "attn_o_debug"), _stream(stream))
+    _check(rc, "upipe_attn_fwd")
+
+
+def attn_bwd(shape: Shape, x, Wq, Wk, Wv, Wo, dout, lse, dx, dWq, dWk, dWv, dWo,
+             workspace, q_norm_w=None, k_norm_w=None, dq_norm_w=None,
+             dk_norm_w=None, stream=None):
+    """upipe_attn_bwd on torch tensors."""
+    bf, f = torch.bfloat16, torch.float32
+    rc = lib().upipe_attn_bwd(
+        ctypes.byref(shape), _ptr(x, bf, "x"), _ptr(Wq, bf, "Wq"), _ptr(Wk, bf, "Wk"),
+        _ptr(Wv, bf, "Wv"), _ptr(Wo, bf, "Wo"), _ptr(q_norm_w, f, "q_norm_w"),
+        _ptr(k_norm_w, f, "k_norm_w"), _ptr(dout, bf, "dout"), _ptr(lse, f, "lse"),
+        _ptr(dx, f, "dx"), _ptr(dWq, f, "dWq"), _ptr(dWk, f, "dWk"), _ptr(dWv, f, "dWv"),
+        _ptr(dWo, f, "dWo"), _ptr(dq_norm_w, f, "dq_norm_w"), _ptr(dk_norm_w, f, "dk_norm_w"),
+        _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+    _check(rc, "upipe_attn_bwd")
+
+
+def last_error() -> int:
+    return int(lib().upipe_last_error())

@@ -1,0 +1,119 @@
+"""GPU forward parity: the CUDA path (through the C ABI) against the float64
+oracle on the same seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from workloads import WORKLOADS, Workload, make_inputs, sample_rows
+from tests._util import f64, assert_close, LSE_ABS
+
+pytestmark = pytest.mark.gpu
+
+
+def U():
+    import headwise_chunked_attention_gb300 as mod
+    mod.lib()
+    return mod
+
+
+def run_fwd(w, ch, inp, debug=True):
+    u = U()
+    dev = "cuda"
+    t = {k: v.to(dev) for k, v in inp.items()}
+    shape = u.Shape.of(w, ch)
+    out = torch.empty(w.S, w.hidden, device=dev, dtype=torch.float32)
+    lse = torch.empty(w.Hq, w.S, device=dev, dtype=torch.float32)
+    ws = torch.empty(u.workspace_bytes(shape, 0), device=dev, dtype=torch.uint8)
+    o = torch.empty(w.S, w.Hq * w.d, device=dev, dtype=torch.bfloat16) if debug else None
+    u.attn_fwd(shape, t["x"], t["Wq"], t["Wk"], t["Wv"], t["Wo"], out, lse, ws,
+               t.get("q_gamma"), t.get("k_gamma"), o)
+    torch.cuda.synchronize()
+    assert u.last_error() == 0
+    return out, lse, o
+
+
+def oracle_fwd(w, inp, rows=None, store=None):
+    a = {k: f64(v) for k, v in inp.items()}
+    return O.layer_forward(w, a["x"], a["Wq"], a["Wk"], a["Wv"], a["Wo"],
+                           a.get("q_gamma"), a.get("k_gamma"), rows=rows,
+                           store_dtype=store)
+
+
+def check_full(w, ch, inp):
+    out, lse, o = run_fwd(w, ch, inp)
+    ref = oracle_fwd(w, inp)
+    refb = oracle_fwd(w, inp, store="bf16")
+    assert_close(f64(out), ref["out"], "out")
+    o_g = f64(o).reshape(w.S, w.Hq, w.d).transpose(1, 0, 2)
+    assert_close(o_g, refb["o"], "attention output")
+    dl = np.abs(f64(lse) - refb["lse"]).max()
+    assert dl <= LSE_ABS, f"lse max abs err {dl:.3e}"
+    return out, lse, o
+
+
+SMALL = [
+    WORKLOADS["tiny-s2048"],
+    # d=128 GQA, one kv head, ragged S, several chunk sizes
+    Workload("d128-s1000", S=1000, hidden=256, Hq=4, Hkv=1, d=128,
+             chunk_heads=(1, 2, 4), rope_theta=5e5),
+    Workload("d128-qknorm-s777", S=777, hidden=384, Hq=4, Hkv=2, d=128,
+             chunk_heads=(1, 2, 4), rope_theta=1e6, qk_norm=True),
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_forward_matches_oracle(w):
+    inp = make_inputs(w, seed=0, norm_gains="random")
+    for ch in w.chunk_heads:
+        check_full(w, ch, inp)
+
+
+@pytest.mark.parametrize("S", [1, 2, 127, 128, 129, 255, 256, 257, 300])
+def test_forward_ragged_and_tiny_lengths(S):
+    w = Workload("ragged", S=S, hidden=256, Hq=2, Hkv=1, d=128, chunk_heads=(1,),
+                 rope_theta=1e4)
+    check_full(w, 1, make_inputs(w, seed=S))
+
+
+def test_per_head_output_bit_identical_across_chunk_sizes():
+    w = Workload("chunks", S=1536, hidden=512, Hq=8, Hkv=2, d=128,
+                 chunk_heads=(1, 2, 4, 8), rope_theta=5e5, qk_norm=True)
+    inp = make_inputs(w, seed=3, norm_gains="random")
+    outs = {}
+    for ch in w.chunk_heads:
+        _, lse, o = run_fwd(w, ch, inp)
+        outs[ch] = (o.cpu(), lse.cpu())
+    o1, l1 = outs[1]
+    for ch in w.chunk_heads[1:]:
+        assert torch.equal(outs[ch][0].view(torch.int16), o1.view(torch.int16)), ch
+        assert torch.equal(outs[ch][1], l1), ch
+
+
+def test_chunked_out_close_to_unchunked():
+    w = WORKLOADS["llama3.2-3b-s65536"].with_(S=4096)
+    inp = make_inputs(w, seed=1)
+    ref, _, _ = run_fwd(w, 24, inp, debug=False)
+    for ch in (3, 6):
+        out, _, _ = run_fwd(w, ch, inp, debug=False)
+        assert_close(f64(out), f64(ref), f"out ch={ch} vs ch=24", 1e-3, 1e-4)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,ch", [("llama3.2-3b-s65536", 3),
+                                     ("llama3.2-3b-s65536", 24)])
+def test_forward_sampled_rows_full_size(name, ch):
+    w = WORKLOADS[name]
+    inp = make_inputs(w, seed=0, device="cuda")
+    out, lse, o = run_fwd(w, ch, inp)
+    rows = sample_rows(w.S, 64)
+    xg = inp["x"]
+    src = lambda lo, hi: f64(xg[lo:hi])
+    small = {k: v for k, v in inp.items() if k != "x"}
+    a = {k: f64(v) for k, v in small.items()}
+    ref = O.layer_forward(w, src, a["Wq"], a["Wk"], a["Wv"], a["Wo"], rows=rows)
+    refb = O.layer_forward(w, src, a["Wq"], a["Wk"], a["Wv"], a["Wo"], rows=rows,
+                           store_dtype="bf16")
+    assert_close(f64(out[rows]), ref["out"], "out rows")
+    dl = np.abs(f64(lse[:, rows]) - refb["lse"]).max()
+    assert dl <= LSE_ABS, dl
