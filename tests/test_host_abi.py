@@ -1,0 +1,111 @@
+"""CPU-only checks of the C ABI: the library builds, loads and exports every
+function include/upipe.h declares; the workspace planner; host-side argument
+validation (no call here reaches the GPU: every case fails validation first)."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+from workloads import WORKLOADS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def u():
+    import headwise_chunked_attention_gb300 as mod
+    if not os.path.exists(mod.lib_path()):
+        from headwise_chunked_attention_gb300.build import build
+        build()
+    mod.lib()
+    return mod
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "upipe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(upipe_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_exports_every_declared_function(u):
+    names = declared_functions()
+    assert {"upipe_attn_fwd", "upipe_attn_bwd", "upipe_workspace_bytes"} <= set(names)
+    L = u.lib()
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def ws(u, w, ch, mode=0, **kw):
+    return u.workspace_bytes(u.Shape.of(w.with_(**kw) if kw else w, ch), mode)
+
+
+def test_workspace_closed_form(u):
+    al = lambda b: (b + 255) // 256 * 256
+    for w in WORKLOADS.values():
+        g = w.Hq // w.Hkv
+        for ch in w.chunk_heads:
+            kvc = max(1, ch // g)
+            S, d = w.S, w.d
+            expect = (al(((S >> 10) + 1) * (d // 2) * 8) + al(1024 * (d // 2) * 8)
+                      + 2 * al(S * ch * d * 2) + 2 * al(S * kvc * d * 2))
+            assert ws(u, w, ch) == expect, (w.name, ch)
+            assert ws(u, w, ch, 1) > ws(u, w, ch)
+
+
+def test_workspace_affine_in_chunk_heads_and_golden_reduction(u):
+    w = WORKLOADS["qwen3-32b-rank-s1m"]
+    b = {ch: ws(u, w, ch) for ch in (1, 2, 4, 8)}
+    slope = (b[8] - b[1]) / 7
+    for ch in (2, 4):
+        assert b[ch] == b[1] + slope * (ch - 1)
+    qo = lambda ch: slope * ch             # the part that scales with chunk_heads
+    gold = json.load(open(os.path.join(ROOT, "tests", "golden", "paper_figures.json")))
+    want = gold["attention_intermediate_memory_reduction_qwen3_32b"]["value"]
+    assert abs((1 - qo(1) / qo(8)) - want) < 1e-12
+    # the Q/O part of the forward workspace is 4 GiB at 8 heads, 0.5 GiB at 1
+    assert qo(8) == 4 * 2 ** 30 and qo(1) == 2 ** 29
+
+
+def test_invalid_shapes_give_zero_workspace(u):
+    w = WORKLOADS["tiny-s2048"]
+    bad = [dict(S=0), dict(Hq=5), dict(Hkv=3), dict(d=96), dict(hidden=200),
+           dict(rope_theta=0.0), dict(rope_theta=float("nan"))]
+    for kw in bad:
+        assert ws(u, w, 2, **kw) == 0, kw
+    assert ws(u, w, 3) == 0                   # 3 does not divide Hq = 4
+    assert u.workspace_bytes(u.Shape.of(w, 2), 7) == 0
+
+
+def _fwd(u, shape, ptrs=None, ws_bytes=1 << 40, dbg=None):
+    L = u.lib()
+    p = ptrs or [0x100000 + 0x1000 * i for i in range(10)]
+    return L.upipe_attn_fwd(ctypes.byref(shape) if shape is not None else None,
+                            *p[:5], None, None, p[5], p[6], p[7], ws_bytes, dbg, None)
+
+
+def test_validation_codes_before_any_launch(u):
+    w = WORKLOADS["tiny-s2048"]
+    sh = u.Shape.of(w, 2)
+    assert _fwd(u, None) == 1
+    assert _fwd(u, u.Shape.of(w, 3)) == 1
+    assert _fwd(u, u.Shape.of(w.with_(d=96), 2)) == 2
+    ptrs = [0x100000 + 0x1000 * i for i in range(10)]
+    ptrs[0] = 0
+    assert _fwd(u, sh, ptrs) == 1                       # NULL x
+    ptrs = [0x100000 + 0x1000 * i for i in range(10)]
+    ptrs[2] += 8
+    assert _fwd(u, sh, ptrs) == 1                       # misaligned Wk
+    assert _fwd(u, sh, ws_bytes=1000) == 3              # workspace too small
+    L = u.lib()
+    for code, text in [(0, b"ok"), (3, b"workspace too small"), (5, b"device wait timed out")]:
+        assert L.upipe_strerror(code) == text
+
+
+def test_binding_marshals_error_codes(u):
+    import torch
+    w = WORKLOADS["tiny-s2048"]
+    x = torch.zeros(4, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        u.attn_fwd(u.Shape.of(w, 2), x, x, x, x, x, x, x, x)   # CPU tensors refused
