@@ -1,0 +1,378 @@
+#!/usr/bin/env python
+"""Benchmark of the headwise-chunked causal GQA attention layer on GB300.
+
+One step = one pass of the whole hot path over the layer: for every head
+chunk, the fused Q/K/V projection (+RoPE, +qk-RMSNorm), causal attention over
+the full sequence and the Wo-slice accumulate (``--pass fwd``; with
+``--pass fwdbwd`` also the chunked backward with recomputation).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--chunk-heads C] [--pass fwd|fwdbwd]
+
+Prints ONE JSON line on rank 0.  Under torchrun (N > 1) every rank runs an
+independent replica of the workload (the path has no exchange step on one
+GPU): ``value`` is the sum of all ranks' FLOPs over the max-over-ranks time.
+``--impl reference`` times the float64 CPU oracle (the only reference this
+method has) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attn-layer TFLOP/s & % BF16 tensor peak; peak workspace GB vs head-chunk size"
+DEFAULT_WORKLOAD = "llama3.2-3b-s65536"
+
+
+def layer_flops(w, mode="fwd"):
+    """Model FLOPs of one layer pass (unmasked causal pairs S(S+1)/2)."""
+    S, hid, d = w.S, w.hidden, w.d
+    pairs = S * (S + 1) / 2
+    proj = 2.0 * S * hid * d * (w.Hq + 2 * w.Hkv)
+    attn = 4.0 * d * w.Hq * pairs
+    wo = 2.0 * S * w.Hq * d * hid
+    if mode == "fwd":
+        return proj + attn + wo, attn
+    # backward: dX and dW of every projection (2x each GEMM) and the
+    # attention backward (10 d per pair per head)
+    bwd = 2 * (proj + wo) + 10.0 * d * w.Hq * pairs
+    return proj + attn + wo + bwd, attn
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return j["bf16_tflops"], j.get("bf16_tflops_sustained", j["bf16_tflops"]), \
+            j["hbm_gbs"], "measured"
+    return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks --
+
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.f = None
+
+    def __enter__(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.f.flush()
+        rows = [l.split(",") for l in open(self.f.name).read().strip().splitlines() if l]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- oracle --
+
+def oracle_sample(w, inp, rows_per_head=64, groups=1):
+    """Time the float64 oracle on a bounded sample of the workload: the full
+    K/V projection of ``groups`` kv heads plus ``rows_per_head`` sampled query
+    rows of each of their query heads.  Returns (TFLOP/s, seconds, flops)."""
+    import numpy as np
+    import torch
+
+    import oracle as O
+    from workloads import sample_rows
+    a = {k: v.to("cpu", torch.float64).numpy() for k, v in inp.items() if k != "x"}
+    xb = inp["x"]
+    x_src = lambda lo, hi: xb[lo:hi].to("cpu", torch.float64).numpy()
+    rows = np.asarray(sample_rows(w.S, rows_per_head))
+    g = w.Hq // w.Hkv
+    t0 = time.perf_counter()
+    flops = 0.0
+    for kvh in range(groups):
+        K, V = O.project_kv(x_src, a["Wk"], a["Wv"], w, kvh, w.S, a.get("k_gamma"))
+        flops += 2 * 2.0 * w.S * w.hidden * w.d
+        xq = np.concatenate([x_src(int(r), int(r) + 1) for r in rows])
+        for h in range(kvh * g, (kvh + 1) * g):
+            q = O.attention_layer._qk_post(xq @ a["Wq"][h * w.d:(h + 1) * w.d].T, rows, w,
+                                           a.get("q_gamma"), None)
+            O.causal_attention(q, K, V, rows)
+            flops += 2.0 * len(rows) * w.hidden * w.d + 4.0 * w.d * float(np.sum(rows + 1))
+    dt = time.perf_counter() - t0
+    return flops / dt / 1e12, dt, flops
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ------------------------------------------------------------------ main --
+
+def config_of(w, ch, args):
+    return {"workload": w.name, "S": w.S, "hidden": w.hidden, "Hq": w.Hq, "Hkv": w.Hkv,
+            "d": w.d, "chunk_heads": ch, "qk_norm": bool(w.qk_norm),
+            "rope_theta": w.rope_theta, "pass": args.pass_, "parallelism": "replicas",
+            "l2": "inputs larger than L2 (x alone is %.0f MB)" % (w.S * w.hidden * 2 / 1e6)}
+
+
+def run_reference(args, w, ch):
+    import torch
+    from workloads import make_inputs
+    inp = make_inputs(w.with_(S=w.S), seed=0, device="cpu") if w.S <= 65536 else \
+        make_inputs(w, seed=0, device="cuda")
+    times, tf = [], []
+    for i in range(args.warmup + args.steps):
+        v, dt, fl = oracle_sample(w, inp)
+        if i >= args.warmup:
+            times.append(dt)
+            tf.append(v)
+    value = sum(tf) / len(tf)
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * sum(times) / len(times), 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w, ch, args),
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores(),
+                             "kind": "oracle",
+                             "sample": "per step: full K/V projection of 1 kv head + 64 "
+                                       "sampled query rows of each of its query heads"},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--chunk-heads", type=int, default=None)
+    ap.add_argument("--pass", dest="pass_", default="fwd", choices=["fwd", "fwdbwd"])
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    from workloads import WORKLOADS, make_inputs
+    w = WORKLOADS[args.workload]
+    ch = args.chunk_heads or w.chunk_heads[0]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, w, ch)
+        return
+
+    import torch
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import headwise_chunked_attention_gb300 as u
+
+    dev = torch.device("cuda", local)
+    inp = make_inputs(w, seed=rank, device=str(dev), with_grad=args.pass_ == "fwdbwd")
+    shape = u.Shape.of(w, ch)
+    mode = 1 if args.pass_ == "fwdbwd" else 0
+    torch.cuda.synchronize()
+    base_alloc = torch.cuda.memory_allocated()
+    torch.cuda.reset_peak_memory_stats()
+    ws = torch.empty(u.workspace_bytes(shape, mode), dtype=torch.uint8, device=dev)
+    peak_ws = torch.cuda.max_memory_allocated() - base_alloc
+    out = torch.empty(w.S, w.hidden, device=dev)
+    lse = torch.empty(w.Hq, w.S, device=dev)
+    grads = None
+    if mode:
+        grads = {n: torch.empty(inp[s].shape, device=dev) for n, s in
+                 [("dx", "x"), ("dWq", "Wq"), ("dWk", "Wk"), ("dWv", "Wv"), ("dWo", "Wo")]}
+        grads["dqg"] = torch.empty(w.d, device=dev) if w.qk_norm else None
+        grads["dkg"] = torch.empty(w.d, device=dev) if w.qk_norm else None
+
+    def step(sh=shape, wsb=ws):
+        u.attn_fwd(sh, inp["x"], inp["Wq"], inp["Wk"], inp["Wv"], inp["Wo"], out, lse, wsb,
+                   inp.get("q_gamma"), inp.get("k_gamma"))
+        if mode:
+            u.attn_bwd(sh, inp["x"], inp["Wq"], inp["Wk"], inp["Wv"], inp["Wo"], inp["dout"],
+                       lse, grads["dx"], grads["dWq"], grads["dWk"], grads["dWv"],
+                       grads["dWo"], wsb, inp.get("q_gamma"), inp.get("k_gamma"),
+                       grads["dqg"], grads["dkg"])
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def timed(fn, k):
+        barrier()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(k):
+            fn()
+        e.record()
+        barrier()
+        t = s.elapsed_time(e) / 1e3
+        if dist is not None:
+            tt = torch.tensor([t], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            t = float(tt.item())
+        return t
+
+    flops, attn_flops = layer_flops(w, args.pass_)
+    nchunks = w.Hq // ch
+    for _ in range(args.warmup):
+        step()
+    rc = u.last_error()
+    if rc != 0:
+        raise RuntimeError(f"device error {rc}")
+
+    # ---- device-resident timed region (+ live attention-kernel timing)
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = getattr(props, "uuid", None)
+    gpu_id = ("GPU-" + str(gpu_id)) if gpu_id is not None and not str(gpu_id).startswith("GPU-") \
+        else (str(gpu_id) if gpu_id is not None else str(local))
+    kt = u.KernelTimer(0, args.steps * nchunks * (2 if mode else 1))
+    with Clocks(gpu_id) as clk, kt:
+        t = timed(step, args.steps)
+    clocks = clk.summary()
+    durs = kt.durations_ms()
+    value = world * flops * args.steps / t / 1e12
+
+    # ---- end to end: pinned host x -> device, layer, out -> pinned host
+    x_host = inp["x"].cpu().pin_memory()
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+    def e2e_step():
+        inp["x"].copy_(x_host, non_blocking=True)
+        step()
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    t_e2e = timed(e2e_step, max(1, args.steps // 2))
+    e2e_value = world * flops * max(1, args.steps // 2) / t_e2e / 1e12
+
+    # ---- roofline of the dominant kernel (attention forward)
+    burst, sustained, hbm, src = peaks()
+    avg_attn_ms = sum(durs) / max(1, len(durs))
+    pairs = w.S * (w.S + 1) / 2
+    attn_launch_flops = 4.0 * w.d * ch * pairs
+    achieved = attn_launch_flops / (avg_attn_ms / 1e3) / 1e12 if durs else None
+
+    # ---- chunk sweep: throughput and workspace against chunk_heads
+    sweep = []
+    if not args.no_sweep:
+        for c in w.chunk_heads:
+            sh = u.Shape.of(w, c)
+            wb = u.workspace_bytes(sh, mode)
+            del ws
+            torch.cuda.synchronize()
+            a0 = torch.cuda.memory_allocated()
+            torch.cuda.reset_peak_memory_stats()
+            ws = torch.empty(wb, dtype=torch.uint8, device=dev)
+            pk = torch.cuda.max_memory_allocated() - a0
+            step(sh, ws)
+            k = max(2, args.steps // 3)
+            tc = timed(lambda: step(sh, ws), k)
+            sweep.append({"chunk_heads": c, "tflops": round(flops * k / tc / 1e12, 2),
+                          "workspace_gb": round(wb / 1e9, 4), "peak_alloc_gb": round(pk / 1e9, 4)})
+
+    launches_per_step = 1 + 3 * nchunks
+    if mode:
+        groups = w.Hkv if ch < w.Hq // w.Hkv else nchunks
+        launches_per_step += 1 + 8 * nchunks + 6 * groups
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config_of(w, ch, args),
+        "frac_of_bf16_peak": round(value / world / burst, 4),
+        "peak_workspace_gb": round(peak_ws / 1e9, 4),
+        "workspace_gb_planned": round(u.workspace_bytes(shape, mode) / 1e9, 4),
+        "chunk_sweep": sweep,
+        "roofline": {"kernel": "attn_fwd_kernel", "bound": "tensor",
+                     "achieved": round(achieved, 2) if achieved else None,
+                     "peak": sustained, "unit": "TFLOP/s",
+                     "frac": round(achieved / sustained, 4) if achieved else None,
+                     "frac_of_burst": round(achieved / burst, 4) if achieved else None,
+                     "peak_kind": f"sustained bf16 ({src})",
+                     "launches_timed": len(durs), "avg_launch_ms": round(avg_attn_ms, 4),
+                     "flops_per_launch": attn_launch_flops, "traffic": None},
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(x_host.numel() * 2),
+                "d2h_bytes_per_step": int(out_host.numel() * 4)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu:
+        v, dt, fl = oracle_sample(w, {k: v for k, v in inp.items()})
+        line["cpu_baseline"] = {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores(),
+                                "kind": "oracle", "seconds": round(dt, 2),
+                                "sample": "full K/V projection of 1 kv head + 64 sampled "
+                                          "query rows of each of its query heads (float64)"}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -62,6 +62,10 @@ def lib():
         L.upipe_attn_bwd.restype = ctypes.c_int
         L.upipe_last_error.argtypes = []
         L.upipe_last_error.restype = ctypes.c_int
+        L.upipe_profile_attach.argtypes = [ctypes.c_int, P, P, ctypes.c_int]
+        L.upipe_profile_attach.restype = None
+        L.upipe_profile_count.argtypes = []
+        L.upipe_profile_count.restype = ctypes.c_int
         L.upipe_strerror.argtypes = [ctypes.c_int]
         L.upipe_strerror.restype = ctypes.c_char_p
         _lib = L
@@ -124,6 +128,35 @@ def attn_bwd(shape: Shape, x, Wq, Wk, Wv, Wo, dout, lse, dx, dWq, dWk, dWv, dWo,
         _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
         _stream(stream))
     _check(rc, "upipe_attn_bwd")
+
+
+class KernelTimer:
+    """Times every launch of one library kernel (0: attention forward,
+    1: attention backward) with CUDA events while the context is open."""
+
+    def __init__(self, kernel: int, capacity: int):
+        self.kernel = kernel
+        self.starts = [torch.cuda.Event(enable_timing=True) for _ in range(capacity)]
+        self.ends = [torch.cuda.Event(enable_timing=True) for _ in range(capacity)]
+        for e in self.starts + self.ends:
+            e.record()          # materialise the event handles
+        torch.cuda.synchronize()
+        arr = ctypes.c_void_p * capacity
+        self._s = arr(*[e.cuda_event for e in self.starts])
+        self._e = arr(*[e.cuda_event for e in self.ends])
+        self.count = 0
+
+    def __enter__(self):
+        lib().upipe_profile_attach(self.kernel, self._s, self._e, len(self.starts))
+        return self
+
+    def __exit__(self, *exc):
+        self.count = int(lib().upipe_profile_count())
+        lib().upipe_profile_attach(-1, None, None, 0)
+
+    def durations_ms(self):
+        torch.cuda.synchronize()
+        return [s.elapsed_time(e) for s, e in zip(self.starts[:self.count], self.ends[:self.count])]
 
 
 def last_error() -> int:

@@ -38,6 +38,25 @@ struct DeviceState {
   int* err = nullptr;
 };
 
+// measurement hook (upipe_profile_attach)
+struct Profile {
+  int kernel = -1;
+  void* const* starts = nullptr;
+  void* const* ends = nullptr;
+  int capacity = 0;
+  int count = 0;
+};
+Profile g_prof;
+
+inline void prof_begin(int kernel, cudaStream_t st) {
+  if (g_prof.kernel == kernel && g_prof.count < g_prof.capacity)
+    cudaEventRecord(static_cast<cudaEvent_t>(g_prof.starts[g_prof.count]), st);
+}
+inline void prof_end(int kernel, cudaStream_t st) {
+  if (g_prof.kernel == kernel && g_prof.count < g_prof.capacity)
+    cudaEventRecord(static_cast<cudaEvent_t>(g_prof.ends[g_prof.count++]), st);
+}
+
 constexpr int kMaxDevices = 64;
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -245,7 +264,10 @@ int attention_chunk(const Geo& g, const DeviceState* ds, cudaStream_t st, const 
   a.lse = lse;
   a.lse_stride = g.S;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
-  UPIPE_CUDA(launch_attn_fwd(qm, km, vm, a, d, ds->err, st));
+  prof_begin(0, st);
+  const cudaError_t e = launch_attn_fwd(qm, km, vm, a, d, ds->err, st);
+  prof_end(0, st);
+  UPIPE_CUDA(e);
   return UPIPE_OK;
 }
 
@@ -483,7 +505,10 @@ extern "C" int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x_,
       a.dV = dV;
       a.ld_dkv = g.kvc * d;
       a.scale = (float)(1.0 / std::sqrt((double)d));
-      UPIPE_CUDA(launch_attn_bwd(a, st));
+      prof_begin(1, st);
+      const cudaError_t e = launch_attn_bwd(a, st);
+      prof_end(1, st);
+      UPIPE_CUDA(e);
     }
     // 4. dQ -> gradient of the Q projection output (RoPE^T, RMSNorm backward),
     //    bf16 into the dO buffer (dO is dead now); dx += dA_q Wq_c;
@@ -537,6 +562,17 @@ extern "C" int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x_,
   }
   return UPIPE_OK;
 }
+
+extern "C" void upipe_profile_attach(int kernel, void* const* start_events,
+                                     void* const* end_events, int capacity) {
+  g_prof.kernel = capacity > 0 ? kernel : -1;
+  g_prof.starts = start_events;
+  g_prof.ends = end_events;
+  g_prof.capacity = capacity > 0 ? capacity : 0;
+  g_prof.count = 0;
+}
+
+extern "C" int upipe_profile_count(void) { return g_prof.count; }
 
 extern "C" int upipe_last_error(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return UPIPE_ERR_CUDA;

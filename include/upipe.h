@@ -115,6 +115,20 @@ int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x, const upipe_
                    float* dq_norm_w, float* dk_norm_w, void* workspace, size_t ws_bytes,
                    void* stream);
 
+/* Measurement hook (no counterpart on the pages; used by the benchmark to
+ * time one kernel live inside a layer call).  While attached, each launch of
+ * the selected kernel made by upipe_attn_fwd / upipe_attn_bwd records
+ * start_events[i] just before and end_events[i] just after itself on the
+ * call's stream, for i = 0, 1, ... < capacity; later launches are not timed.
+ *   kernel 0: the attention forward kernel;  kernel 1: the attention backward
+ *   start_events/end_events: caller-created cudaEvent_t handles (timing
+ *   enabled), owned by the caller.  capacity 0 detaches.
+ * upipe_profile_count() returns how many launches were recorded since the
+ * last attach.  Host-side state shared by all threads: not thread-safe. */
+void upipe_profile_attach(int kernel, void* const* start_events, void* const* end_events,
+                          int capacity);
+int upipe_profile_count(void);
+
 /* Synchronises the current device, then returns and clears the device error
  * word (UPIPE_OK or UPIPE_ERR_DEVICE_TIMEOUT), or UPIPE_ERR_CUDA if the
  * device reports a CUDA error. */

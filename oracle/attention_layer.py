@@ -220,7 +220,7 @@ def layer_forward(geom, x: ArrayOrRows, Wq, Wk, Wv, Wo, q_gamma=None,
 
 
 def layer_backward(geom, x: np.ndarray, Wq, Wk, Wv, Wo, dout: np.ndarray,
-                   q_gamma=None, k_gamma=None):
+                   q_gamma=None, k_gamma=None, store_dtype: Optional[str] = None):
     """Gradients of L = sum(out * dout) w.r.t. x, Wq, Wk, Wv, Wo and the norm
     gains, by the chain rule in float64 over the full sequence (small S).
 
@@ -229,6 +229,10 @@ def layer_backward(geom, x: np.ndarray, Wq, Wk, Wv, Wo, dout: np.ndarray,
     dq = ds k / sqrt(d);  dk += ds^T q / sqrt(d);  then RoPE transpose and the
     RMSNorm backward give the gradient of the projection outputs a = x W^T,
     and dW = da^T x, dx += da W.
+
+    ``store_dtype="bf16"`` runs the attention on q, k, v rounded to bf16 (the
+    workspace precision, as in ``layer_forward``); the rounding is treated as
+    the identity by the chain rule.
     """
     x = np.asarray(x, dtype=np.float64)
     dout = np.asarray(dout, dtype=np.float64)
@@ -243,12 +247,14 @@ def layer_backward(geom, x: np.ndarray, Wq, Wk, Wv, Wo, dout: np.ndarray,
     dgq = np.zeros(d) if geom.qk_norm else None
     dgk = np.zeros(d) if geom.qk_norm else None
 
+    rnd = bf16_round if store_dtype == "bf16" else (lambda t: t)
+
     def pre(a, gamma):
         if geom.qk_norm:
             y, r = rms_norm(a, gamma, geom.norm_eps)
         else:
             y, r = a, None
-        return apply_rope(y, cos, sin), r
+        return rnd(apply_rope(y, cos, sin)), r
 
     def post_grad(dqk, a, r, gamma):
         dy = apply_rope_transpose(dqk, cos, sin)
@@ -259,7 +265,7 @@ def layer_backward(geom, x: np.ndarray, Wq, Wk, Wv, Wo, dout: np.ndarray,
     for kvh in range(Hkv):
         sl = slice(kvh * d, (kvh + 1) * d)
         ak = x @ Wk[sl].T
-        v = x @ Wv[sl].T
+        v = rnd(x @ Wv[sl].T)
         k, rk = pre(ak, k_gamma)
         dk = np.zeros((S, d))
         dv = np.zeros((S, d))

@@ -42,9 +42,10 @@ def oracle_fwd(w, inp, rows=None, store=None):
 
 def check_full(w, ch, inp):
     out, lse, o = run_fwd(w, ch, inp)
-    ref = oracle_fwd(w, inp)
     refb = oracle_fwd(w, inp, store="bf16")
-    assert_close(f64(out), ref["out"], "out")
+    # q, k, v, P and O are bf16 by design (the workspace precision): the
+    # tolerance applies against the oracle that stores q, k, v in bf16
+    assert_close(f64(out), refb["out"], "out")
     o_g = f64(o).reshape(w.S, w.Hq, w.d).transpose(1, 0, 2)
     assert_close(o_g, refb["o"], "attention output")
     dl = np.abs(f64(lse) - refb["lse"]).max()
@@ -111,9 +112,8 @@ def test_forward_sampled_rows_full_size(name, ch):
     src = lambda lo, hi: f64(xg[lo:hi])
     small = {k: v for k, v in inp.items() if k != "x"}
     a = {k: f64(v) for k, v in small.items()}
-    ref = O.layer_forward(w, src, a["Wq"], a["Wk"], a["Wv"], a["Wo"], rows=rows)
     refb = O.layer_forward(w, src, a["Wq"], a["Wk"], a["Wv"], a["Wo"], rows=rows,
                            store_dtype="bf16")
-    assert_close(f64(out[rows]), ref["out"], "out rows")
+    assert_close(f64(out[rows]), refb["out"], "out rows")
     dl = np.abs(f64(lse[:, rows]) - refb["lse"]).max()
     assert dl <= LSE_ABS, dl
