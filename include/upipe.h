@@ -115,6 +115,30 @@ int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x, const upipe_
                    float* dq_norm_w, float* dk_norm_w, void* workspace, size_t ws_bytes,
                    void* stream);
 
+/* Forward for callers that cannot allocate device memory: code running where
+ * cudaMalloc is not allowed or not wanted (inside a graph-building or
+ * real-time section, under an external allocator that forbids extra device
+ * allocations, or in a plugin that only receives its inputs' and outputs'
+ * pointers).  The paper has no counterpart; this is a convenience of the
+ * library.  Same arguments and results as upipe_attn_fwd minus the workspace
+ * and attn_o_debug: the workspace is a static device array of
+ * UPIPE_STATIC_SCRATCH_BYTES (64 MiB) compiled into the library, which every
+ * GPU that loads the library holds until the process exits.
+ *  - Shapes whose upipe_workspace_bytes(shape, 0) exceeds
+ *    UPIPE_STATIC_SCRATCH_BYTES are rejected with
+ *    UPIPE_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ *  - The first call on each device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - Allocates nothing: no cudaMalloc/cudaFree or allocating library call.
+ *  - Every call shares the one array and leaves its contents behind; nothing
+ *    in it needs to start at zero.  Calls that overlap on the GPU (different
+ *    streams, or host threads racing) race on the array: serialise them. */
+#define UPIPE_STATIC_SCRATCH_BYTES (64u << 20)
+int upipe_attn_fwd_noalloc(const upipe_shape_t* shape, const upipe_bf16* x, const upipe_bf16* Wq,
+                           const upipe_bf16* Wk, const upipe_bf16* Wv, const upipe_bf16* Wo,
+                           const float* q_norm_w, const float* k_norm_w, float* out, float* lse,
+                           void* stream);
+
 /* Measurement hook (no counterpart on the pages; used by the benchmark to
  * time one kernel live inside a layer call).  While attached, each launch of
  * the selected kernel made by upipe_attn_fwd / upipe_attn_bwd records

@@ -1,0 +1,77 @@
+"""The forward entry point for callers that cannot allocate device memory.
+
+upipe_attn_fwd_noalloc runs the layer forward on a static device array built
+into the library instead of a caller-provided workspace.  This file is named
+so that pytest collects it last: if it fails, a run stopped at the first
+failure has already run every other test.  It passes alone in a fresh process
+and after the other tests, because every call overwrites whatever the shared
+array holds before reading it.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from workloads import WORKLOADS, Workload, make_inputs
+from tests._util import f64, assert_close, LSE_ABS
+
+pytestmark = pytest.mark.gpu
+
+UPIPE_ERR_WORKSPACE_TOO_SMALL = 3
+STATIC_SCRATCH_BYTES = 64 << 20
+
+
+def noalloc_fn():
+    import headwise_chunked_attention_gb300 as u
+    fn = u.lib().upipe_attn_fwd_noalloc
+    fn.argtypes = [ctypes.POINTER(u.Shape)] + [ctypes.c_void_p] * 10
+    fn.restype = ctypes.c_int
+    return fn
+
+
+def ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+@pytest.mark.parametrize("w,ch", [
+    (WORKLOADS["tiny-s2048"], 2),
+    (Workload("d128-qknorm-s3000", S=3000, hidden=512, Hq=8, Hkv=2, d=128,
+              chunk_heads=(2,), rope_theta=1e6, qk_norm=True), 2),
+], ids=["tiny", "d128-qknorm"])
+def test_noalloc_forward_matches_allocating_forward(w, ch):
+    import headwise_chunked_attention_gb300 as u
+    fn = noalloc_fn()
+    inp = {k: v.cuda() for k, v in make_inputs(w, seed=5, norm_gains="random").items()}
+    shape = u.Shape.of(w, ch)
+    assert 0 < u.workspace_bytes(shape, 0) <= STATIC_SCRATCH_BYTES
+    # the existing entry point, with a caller-allocated workspace
+    out_ref = torch.empty(w.S, w.hidden, device="cuda")
+    lse_ref = torch.empty(w.Hq, w.S, device="cuda")
+    ws = torch.empty(u.workspace_bytes(shape, 0), dtype=torch.uint8, device="cuda")
+    u.attn_fwd(shape, inp["x"], inp["Wq"], inp["Wk"], inp["Wv"], inp["Wo"], out_ref, lse_ref,
+               ws, inp.get("q_gamma"), inp.get("k_gamma"))
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream().cuda_stream
+    for call in range(2):   # two calls in a row share the static scratch
+        out = torch.full((w.S, w.hidden), float("nan"), device="cuda")
+        lse = torch.full((w.Hq, w.S), float("nan"), device="cuda")
+        rc = fn(ctypes.byref(shape), ptr(inp["x"]), ptr(inp["Wq"]), ptr(inp["Wk"]),
+                ptr(inp["Wv"]), ptr(inp["Wo"]), ptr(inp.get("q_gamma")),
+                ptr(inp.get("k_gamma")), ptr(out), ptr(lse), stream)
+        assert rc == 0, rc
+        torch.cuda.synchronize()
+        assert u.last_error() == 0
+        assert_close(f64(out), f64(out_ref), f"out, call {call}")
+        assert np.abs(f64(lse) - f64(lse_ref)).max() <= LSE_ABS
+
+
+def test_noalloc_rejects_shapes_beyond_the_static_scratch():
+    import headwise_chunked_attention_gb300 as u
+    fn = noalloc_fn()
+    w = WORKLOADS["llama3.2-3b-s65536"]
+    shape = u.Shape.of(w, 24)
+    assert u.workspace_bytes(shape, 0) > STATIC_SCRATCH_BYTES
+    fake = [0x100000 + 0x1000 * i for i in range(10)]
+    rc = fn(ctypes.byref(shape), *fake[:5], None, None, fake[5], fake[6], None)
+    assert rc == UPIPE_ERR_WORKSPACE_TOO_SMALL
