@@ -2,7 +2,10 @@
 //   * the RoPE angle table (built in float64, stored as fp32 cos/sin pairs);
 //   * the backward of the q/k post-processing: RoPE transpose, then (Qwen3
 //     geometry) the RMSNorm backward with its gain gradient;
-//   * fp32 -> bf16 conversion of an accumulated gradient.
+//   * fp32 -> bf16 hi/lo split of an accumulated gradient.
+// Gradients leave these kernels as two bf16 tensors, hi = bf16(v) and
+// lo = bf16(v - hi), which the dX / dW GEMMs consume as two bf16 operands: the
+// tensor cores then see ~16 significant bits of the fp32 gradient instead of 8.
 #include <cmath>
 
 #include "internal.h"
@@ -95,13 +98,14 @@ __global__ void __launch_bounds__(256) qk_bwd_kernel(const QkBwdArgs a) {
       dy[k + E / 2] = gb * c - ga * sn;
     }
     bf16* op = a.out + s * a.ld_out + h * D;
+    bf16* lp = a.out_lo + s * a.ld_out + h * D;
     if (norm) {
-      const bf16* yp = a.yhat + s * a.ld_yhat + h * D;
+      const float* yp = a.yhat + s * a.ld_yhat + h * D;
       const float rs = a.rstd[(long long)h * a.S + s];
       float yh[E], dot = 0.f;
 #pragma unroll
       for (int k = 0; k < E; ++k) {
-        yh[k] = __bfloat162float(yp[lane + 32 * k]);
+        yh[k] = yp[lane + 32 * k];
         dgam[k] = fmaf(dy[k], yh[k], dgam[k]);
         dot = fmaf(dy[k] * gam[k], yh[k], dot);
       }
@@ -109,11 +113,13 @@ __global__ void __launch_bounds__(256) qk_bwd_kernel(const QkBwdArgs a) {
       for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
       const float mean = dot * (1.0f / D);
 #pragma unroll
-      for (int k = 0; k < E; ++k)
-        op[lane + 32 * k] = __float2bfloat16((dy[k] * gam[k] - yh[k] * mean) * rs);
-    } else {
+      for (int k = 0; k < E; ++k) dy[k] = (dy[k] * gam[k] - yh[k] * mean) * rs;
+    }
 #pragma unroll
-      for (int k = 0; k < E; ++k) op[lane + 32 * k] = __float2bfloat16(dy[k]);
+    for (int k = 0; k < E; ++k) {
+      const bf16 hi = __float2bfloat16(dy[k]);
+      op[lane + 32 * k] = hi;
+      lp[lane + 32 * k] = __float2bfloat16(dy[k] - __bfloat162float(hi));
     }
   }
   if (norm && a.dgamma) {
@@ -137,28 +143,34 @@ cudaError_t launch_qk_bwd(const QkBwdArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-// ------------------------------------------------------------ fp32->bf16 --
-__global__ void f32_to_bf16_kernel(const float* __restrict__ in, int ld_in, bf16* __restrict__ out,
-                                   int ld_out, long long S, int cols4) {
+// ---------------------------------------------------------- fp32->bf16x2 --
+__global__ void f32_to_bf16x2_kernel(const float* __restrict__ in, int ld_in,
+                                     bf16* __restrict__ hi, bf16* __restrict__ lo, int ld_out,
+                                     long long S, int cols4) {
   const long long total = S * cols4;
   for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
        t += (long long)gridDim.x * blockDim.x) {
     const long long r = t / cols4;
     const int c = (int)(t - r * cols4) * 4;
     const float4 v = *reinterpret_cast<const float4*>(in + r * ld_in + c);
-    uint2 w;
-    w.x = pack_bf16(v.x, v.y);
-    w.y = pack_bf16(v.z, v.w);
-    *reinterpret_cast<uint2*>(out + r * ld_out + c) = w;
+    uint2 wh, wl;
+    wh.x = pack_bf16(v.x, v.y);
+    wh.y = pack_bf16(v.z, v.w);
+    const float2 h0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wh.x));
+    const float2 h1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wh.y));
+    wl.x = pack_bf16(v.x - h0.x, v.y - h0.y);
+    wl.y = pack_bf16(v.z - h1.x, v.w - h1.y);
+    *reinterpret_cast<uint2*>(hi + r * ld_out + c) = wh;
+    *reinterpret_cast<uint2*>(lo + r * ld_out + c) = wl;
   }
 }
 
-cudaError_t launch_f32_to_bf16(const float* in, int ld_in, bf16* out, int ld_out, long long S,
-                               int cols, cudaStream_t stream) {
+cudaError_t launch_f32_to_bf16x2(const float* in, int ld_in, bf16* hi, bf16* lo, int ld_out,
+                                 long long S, int cols, cudaStream_t stream) {
   if (S <= 0 || cols <= 0) return cudaSuccess;
   const long long total = S * (cols / 4);
   const int blocks = (int)std::min<long long>((total + 255) / 256, 152 * 16);
-  f32_to_bf16_kernel<<<blocks, 256, 0, stream>>>(in, ld_in, out, ld_out, S, cols / 4);
+  f32_to_bf16x2_kernel<<<blocks, 256, 0, stream>>>(in, ld_in, hi, lo, ld_out, S, cols / 4);
   return cudaGetLastError();
 }
 

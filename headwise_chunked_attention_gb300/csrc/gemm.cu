@@ -84,16 +84,11 @@ __device__ __forceinline__ void epi_proj_row(const EpiParams& ep, const ProjSeg&
     for (int i = 0; i < D; ++i) ss = fmaf(v[i], v[i], ss);
     const float rs = rsqrtf(ss * (1.0f / D) + ep.eps);
     if (sg.yhat) {
-      bf16* yp = sg.yhat + m * sg.ld_yhat + n_local;
+      float* yp = sg.yhat + m * sg.ld_yhat + n_local;
 #pragma unroll
-      for (int i = 0; i < D; i += 8) {
-        uint4 w;
-        w.x = pack_bf16(v[i + 0] * rs, v[i + 1] * rs);
-        w.y = pack_bf16(v[i + 2] * rs, v[i + 3] * rs);
-        w.z = pack_bf16(v[i + 4] * rs, v[i + 5] * rs);
-        w.w = pack_bf16(v[i + 6] * rs, v[i + 7] * rs);
-        *reinterpret_cast<uint4*>(yp + i) = w;
-      }
+      for (int i = 0; i < D; i += 4)
+        *reinterpret_cast<float4*>(yp + i) =
+            make_float4(v[i] * rs, v[i + 1] * rs, v[i + 2] * rs, v[i + 3] * rs);
     }
 #pragma unroll
     for (int i = 0; i < D; ++i) {
@@ -329,12 +324,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               uint32_t* wp = &w.x;
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
-                const float a = __uint_as_float(r[i + 2 * j]);
-                const float b = __uint_as_float(r[i + 2 * j + 1]);
+                // D uses the bf16 dO the attention backward will read, so that
+                // sum_j dS_ij stays consistent with dP
+                wp[j] = pack_bf16(__uint_as_float(r[i + 2 * j]), __uint_as_float(r[i + 2 * j + 1]));
+                const float2 dv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wp[j]));
                 const float2 of = __bfloat1622float2(o2[j]);
-                dot = fmaf(a, of.x, dot);
-                dot = fmaf(b, of.y, dot);
-                wp[j] = pack_bf16(a, b);
+                dot = fmaf(dv.x, of.x, dot);
+                dot = fmaf(dv.y, of.y, dot);
               }
               *reinterpret_cast<uint4*>(dp + i) = w;
             }

@@ -43,7 +43,7 @@ struct ProjSeg {
   int col0;
   int mode;
   const float* gamma;  // RMSNorm gain [d], nullptr means ones
-  bf16* yhat;          // optional: normalised, pre-gain, pre-RoPE values (bf16)
+  float* yhat;         // optional: normalised, pre-gain, pre-RoPE values (fp32)
   int ld_yhat;
   float* rstd;         // optional: 1/sqrt(mean(a^2)+eps) per (head, row): [heads][rows]
 };
@@ -124,9 +124,10 @@ struct QkBwdArgs {
   long long S;
   int heads, d;
   const float* g; int ld_g;          // [S, ld_g] fp32
-  bf16* out; int ld_out;             // [S, ld_out] bf16
+  bf16* out; int ld_out;             // [S, ld_out] bf16, high part
+  bf16* out_lo;                      // [S, ld_out] bf16, low part (value - high)
   int mode;                          // PROJ_ROPE or PROJ_NORM_ROPE
-  const bf16* yhat; int ld_yhat;     // saved normalised values (norm mode)
+  const float* yhat; int ld_yhat;    // saved normalised values (norm mode, fp32)
   const float* rstd;                 // [heads][S]
   const float* gamma;                // [d] or nullptr
   float* dgamma;                     // [d] accumulated (norm mode)
@@ -134,8 +135,9 @@ struct QkBwdArgs {
 };
 cudaError_t launch_qk_bwd(const QkBwdArgs& a, cudaStream_t stream);
 
-// fp32 [S, ld_in] -> bf16 [S, ld_out] for ``cols`` columns.
-cudaError_t launch_f32_to_bf16(const float* in, int ld_in, bf16* out, int ld_out, long long S,
-                               int cols, cudaStream_t stream);
+// fp32 [S, ld_in] -> bf16 high part and bf16 low part (value - high),
+// [S, ld_out] each, for ``cols`` columns: hi + lo carries ~16 significant bits.
+cudaError_t launch_f32_to_bf16x2(const float* in, int ld_in, bf16* hi, bf16* lo, int ld_out,
+                                 long long S, int cols, cudaStream_t stream);
 
 }  // namespace upipe

@@ -157,7 +157,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 struct Layout {
   size_t rope_hi, rope_lo, q, k, v, o;            // forward
-  size_t dO, D, dq, dk, dv, yq, rq, yk, rk;       // backward
+  size_t dO, D, dq, dk, dv, dklo, dvlo, yq, rq, yk, rk;  // backward
   size_t total;
 };
 
@@ -182,10 +182,12 @@ Layout plan(const Geo& g, int mode) {
     L.dq = take(S * ch * d * 4);
     L.dk = take(S * kvc * d * 4);
     L.dv = take(S * kvc * d * 4);
+    L.dklo = take(S * kvc * d * 2);
+    L.dvlo = take(S * kvc * d * 2);
     if (g.norm) {
-      L.yq = take(S * ch * d * 2);
+      L.yq = take(S * ch * d * 4);
       L.rq = take(ch * S * 4);
-      L.yk = take(S * kvc * d * 2);
+      L.yk = take(S * kvc * d * 4);
       L.rk = take(kvc * S * 4);
     }
   }
@@ -215,7 +217,7 @@ T* at(void* ws, size_t off) {
 int project_chunk(const Geo& g, const DeviceState* ds, cudaStream_t st, const CUtensorMap& xmap,
                   const bf16* Wq, const bf16* Wk, const bf16* Wv, const float* qgw,
                   const float* kgw, float eps, int h0, int kv0, bool new_group, bf16* Q, bf16* K,
-                  bf16* V, const float2* rhi, const float2* rlo, bf16* yq, float* rq, bf16* yk,
+                  bf16* V, const float2* rhi, const float2* rlo, float* yq, float* rq, float* yk,
                   float* rk) {
   const int d = g.d;
   CUtensorMap bm[3];
@@ -389,9 +391,11 @@ extern "C" int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x_,
   float* dQ = at<float>(workspace, L.dq);
   float* dK = at<float>(workspace, L.dk);
   float* dV = at<float>(workspace, L.dv);
-  bf16* yq = g.norm ? at<bf16>(workspace, L.yq) : nullptr;
+  bf16* dKlo = at<bf16>(workspace, L.dklo);
+  bf16* dVlo = at<bf16>(workspace, L.dvlo);
+  float* yq = g.norm ? at<float>(workspace, L.yq) : nullptr;
   float* rq = g.norm ? at<float>(workspace, L.rq) : nullptr;
-  bf16* yk = g.norm ? at<bf16>(workspace, L.yk) : nullptr;
+  float* yk = g.norm ? at<float>(workspace, L.yk) : nullptr;
   float* rk = g.norm ? at<float>(workspace, L.rk) : nullptr;
 
   UPIPE_CUDA(launch_rope_table(rhi, rlo, g.S, d, shape->rope_theta, st));
@@ -510,9 +514,10 @@ extern "C" int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x_,
       prof_end(1, st);
       UPIPE_CUDA(e);
     }
-    // 4. dQ -> gradient of the Q projection output (RoPE^T, RMSNorm backward),
-    //    bf16 into the dO buffer (dO is dead now); dx += dA_q Wq_c;
-    //    dWq_c = dA_q^T x
+    // 4. dQ -> gradient of the Q projection output (RoPE^T, RMSNorm backward)
+    //    as bf16 hi (into the dO buffer: dO is dead now) + lo (into the O
+    //    buffer: O is dead after the dO / dWo GEMMs); dx += dA_q Wq_c;
+    //    dWq_c = dA_q^T x, each as a hi and a lo GEMM
     {
       QkBwdArgs q{};
       q.S = g.S;
@@ -521,6 +526,7 @@ extern "C" int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x_,
       q.g = dQ;
       q.ld_g = g.ch * d;
       q.out = dO;
+      q.out_lo = Ows;
       q.ld_out = g.ch * d;
       q.mode = g.norm ? PROJ_NORM_ROPE : PROJ_ROPE;
       q.yhat = yq;
@@ -531,10 +537,13 @@ extern "C" int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x_,
       q.rope_hi = rhi;
       q.rope_lo = rlo;
       UPIPE_CUDA(launch_qk_bwd(q, st));
-      UPIPE_TRY(dx_gemm(dO, g.ch * d, g.ch * d, Wq + (size_t)h0 * d * g.hidden));
-      UPIPE_TRY(dw_gemm(dO, g.ch * d, g.ch * d, dWq + (size_t)h0 * d * g.hidden));
+      for (bf16* part : {dO, Ows}) {
+        UPIPE_TRY(dx_gemm(part, g.ch * d, g.ch * d, Wq + (size_t)h0 * d * g.hidden));
+        UPIPE_TRY(dw_gemm(part, g.ch * d, g.ch * d, dWq + (size_t)h0 * d * g.hidden));
+      }
     }
-    // 5. at the group's last chunk: dK -> dA_k (bf16 over K), dV -> bf16 over V
+    // 5. at the group's last chunk: dK -> dA_k (hi over K, lo beside it),
+    //    dV -> hi over V and lo beside it
     if (last_of_group) {
       QkBwdArgs q{};
       q.S = g.S;
@@ -543,6 +552,7 @@ extern "C" int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x_,
       q.g = dK;
       q.ld_g = g.kvc * d;
       q.out = K;
+      q.out_lo = dKlo;
       q.ld_out = g.kvc * d;
       q.mode = g.norm ? PROJ_NORM_ROPE : PROJ_ROPE;
       q.yhat = yk;
@@ -553,11 +563,15 @@ extern "C" int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x_,
       q.rope_hi = rhi;
       q.rope_lo = rlo;
       UPIPE_CUDA(launch_qk_bwd(q, st));
-      UPIPE_CUDA(launch_f32_to_bf16(dV, g.kvc * d, V, g.kvc * d, g.S, g.kvc * d, st));
-      UPIPE_TRY(dx_gemm(K, g.kvc * d, g.kvc * d, Wk + (size_t)kv0 * d * g.hidden));
-      UPIPE_TRY(dx_gemm(V, g.kvc * d, g.kvc * d, Wv + (size_t)kv0 * d * g.hidden));
-      UPIPE_TRY(dw_gemm(K, g.kvc * d, g.kvc * d, dWk + (size_t)kv0 * d * g.hidden));
-      UPIPE_TRY(dw_gemm(V, g.kvc * d, g.kvc * d, dWv + (size_t)kv0 * d * g.hidden));
+      UPIPE_CUDA(launch_f32_to_bf16x2(dV, g.kvc * d, V, dVlo, g.kvc * d, g.S, g.kvc * d, st));
+      for (int part = 0; part < 2; ++part) {
+        const bf16* gk = part ? dKlo : K;
+        const bf16* gv = part ? dVlo : V;
+        UPIPE_TRY(dx_gemm(gk, g.kvc * d, g.kvc * d, Wk + (size_t)kv0 * d * g.hidden));
+        UPIPE_TRY(dx_gemm(gv, g.kvc * d, g.kvc * d, Wv + (size_t)kv0 * d * g.hidden));
+        UPIPE_TRY(dw_gemm(gk, g.kvc * d, g.kvc * d, dWk + (size_t)kv0 * d * g.hidden));
+        UPIPE_TRY(dw_gemm(gv, g.kvc * d, g.kvc * d, dWv + (size_t)kv0 * d * g.hidden));
+      }
     }
   }
   return UPIPE_OK;
