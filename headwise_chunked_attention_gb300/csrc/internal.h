@@ -110,7 +110,7 @@ struct AttnBwdArgs {
   float scale;                  // 1/sqrt(d)
 };
 
-cudaError_t launch_attn_bwd(const AttnBwdArgs& a, cudaStream_t stream);
+cudaError_t launch_attn_bwd(const AttnBwdArgs& a, int* err, cudaStream_t stream);
 
 // ---------------------------------------------------------- elementwise --
 

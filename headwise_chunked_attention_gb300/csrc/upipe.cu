@@ -510,7 +510,7 @@ extern "C" int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x_,
       a.ld_dkv = g.kvc * d;
       a.scale = (float)(1.0 / std::sqrt((double)d));
       prof_begin(1, st);
-      const cudaError_t e = launch_attn_bwd(a, st);
+      const cudaError_t e = launch_attn_bwd(a, ds->err, st);
       prof_end(1, st);
       UPIPE_CUDA(e);
     }
