@@ -49,6 +49,28 @@ def layer_flops(w, mode="fwd"):
     return proj + attn + wo + bwd, attn
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
+# ncu capture, keyed by kernel, workload and chunk size, with the sha256 of the
+# kernel's source file at capture time: a changed kernel reports null.
+NCU_TRAFFIC = {
+    # ("attn_fwd_kernel", "llama3.2-3b-s65536", 3): (bytes, "sha256 prefix of attn_fwd.cu"),
+}
+KERNEL_SOURCES = {"attn_fwd_kernel": "attn_fwd.cu", "attn_bwd_kernel": "attn_bwd.cu"}
+
+
+def kernel_source_sha(kernel):
+    import hashlib
+    path = os.path.join(ROOT, "headwise_chunked_attention_gb300", "csrc", KERNEL_SOURCES[kernel])
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def traffic_of(kernel, workload, ch):
+    ent = NCU_TRAFFIC.get((kernel, workload, ch))
+    if ent is None or ent[1] != kernel_source_sha(kernel):
+        return None
+    return ent[0]
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -306,12 +328,30 @@ def main():
     t_e2e = timed(e2e_step, max(1, args.steps // 2))
     e2e_value = world * flops * max(1, args.steps // 2) / t_e2e / 1e12
 
-    # ---- roofline of the dominant kernel (attention forward)
+    # ---- roofline of the attention kernels (algorithmic FLOPs per launch over
+    # the live CUDA-event launch time)
     burst, sustained, hbm, src = peaks()
-    avg_attn_ms = sum(durs) / max(1, len(durs))
     pairs = w.S * (w.S + 1) / 2
-    attn_launch_flops = 4.0 * w.d * ch * pairs
-    achieved = attn_launch_flops / (avg_attn_ms / 1e3) / 1e12 if durs else None
+
+    def roofline(kernel, durations, flops_per_pair):
+        avg_ms = sum(durations) / max(1, len(durations))
+        fl = flops_per_pair * w.d * ch * pairs
+        ach = fl / (avg_ms / 1e3) / 1e12 if durations else None
+        return {"kernel": kernel, "bound": "tensor",
+                "achieved": round(ach, 2) if ach else None, "peak": sustained,
+                "unit": "TFLOP/s", "frac": round(ach / sustained, 4) if ach else None,
+                "frac_of_burst": round(ach / burst, 4) if ach else None,
+                "peak_kind": f"sustained bf16 ({src})", "launches_timed": len(durations),
+                "avg_launch_ms": round(avg_ms, 4), "flops_per_launch": fl,
+                "traffic": traffic_of(kernel, w.name, ch)}
+
+    roof_fwd = roofline("attn_fwd_kernel", durs, 4.0)
+    roof_bwd = None
+    if mode:
+        kb = u.KernelTimer(1, max(1, args.steps // 2) * nchunks)
+        with kb:
+            timed(step, max(1, args.steps // 2))
+        roof_bwd = roofline("attn_bwd_kernel", kb.durations_ms(), 10.0)
 
     # ---- chunk sweep: throughput and workspace against chunk_heads
     sweep = []
@@ -349,14 +389,8 @@ def main():
         "peak_workspace_gb": round(peak_ws / 1e9, 4),
         "workspace_gb_planned": round(u.workspace_bytes(shape, mode) / 1e9, 4),
         "chunk_sweep": sweep,
-        "roofline": {"kernel": "attn_fwd_kernel", "bound": "tensor",
-                     "achieved": round(achieved, 2) if achieved else None,
-                     "peak": sustained, "unit": "TFLOP/s",
-                     "frac": round(achieved / sustained, 4) if achieved else None,
-                     "frac_of_burst": round(achieved / burst, 4) if achieved else None,
-                     "peak_kind": f"sustained bf16 ({src})",
-                     "launches_timed": len(durs), "avg_launch_ms": round(avg_attn_ms, 4),
-                     "flops_per_launch": attn_launch_flops, "traffic": None},
+        "roofline": roof_bwd if roof_bwd else roof_fwd,
+        "roofline_attn_fwd": roof_fwd,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(x_host.numel() * 2),
                 "d2h_bytes_per_step": int(out_host.numel() * 4)},
@@ -364,11 +398,14 @@ def main():
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu:
-        v, dt, fl = oracle_sample(w, {k: v for k, v in inp.items()})
+        groups = min(w.Hkv, 4)
+        v, dt, fl = oracle_sample(w, {k: v for k, v in inp.items()}, rows_per_head=256,
+                                  groups=groups)
         line["cpu_baseline"] = {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores(),
                                 "kind": "oracle", "seconds": round(dt, 2),
-                                "sample": "full K/V projection of 1 kv head + 64 sampled "
-                                          "query rows of each of its query heads (float64)"}
+                                "sample": f"float64 oracle: full K/V projection of {groups} kv "
+                                          "head(s) + 256 sampled query rows of each of their "
+                                          "query heads (attention over all earlier keys)"}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

@@ -15,6 +15,8 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -195,14 +197,26 @@ Layout plan(const Geo& g, int mode) {
   return L;
 }
 
-int cuda_fail(cudaError_t e) { return e == cudaSuccess ? UPIPE_OK : UPIPE_ERR_CUDA; }
+// UPIPE_VERBOSE=1 in the environment prints the CUDA error behind an
+// UPIPE_ERR_CUDA return to stderr.
+int cuda_fail_at(cudaError_t e, const char* what, int line) {
+  if (e == cudaSuccess) return UPIPE_OK;
+  static const bool verbose = [] {
+    const char* v = std::getenv("UPIPE_VERBOSE");
+    return v && *v && *v != '0';
+  }();
+  if (verbose)
+    std::fprintf(stderr, "upipe: %s failed (upipe.cu:%d): %s\n", what, line,
+                 cudaGetErrorString(e));
+  return UPIPE_ERR_CUDA;
+}
 
 #define UPIPE_TRY(expr)                 \
   do {                                  \
     int _rc = (expr);                   \
     if (_rc != UPIPE_OK) return _rc;    \
   } while (0)
-#define UPIPE_CUDA(expr) UPIPE_TRY(cuda_fail(expr))
+#define UPIPE_CUDA(expr) UPIPE_TRY(cuda_fail_at((expr), #expr, __LINE__))
 #define UPIPE_MAP(...) \
   do { if (!make_tmap_bf16(__VA_ARGS__)) return UPIPE_ERR_CUDA; } while (0)
 
