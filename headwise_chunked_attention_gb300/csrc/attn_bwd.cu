@@ -10,22 +10,29 @@
 // dimanyen.com "activation checkpointing"; per-chunk recomputation of the
 // heads, memeeeeeex.com "Untied Ulysses (UPipe)").
 //
-// One CTA owns 128 keys (one KV tile) of one head and walks the 128-query
-// tiles from its diagonal to the end of the sequence.
-//   warps 0-3  softmax-gradient warps: one key row (TMEM lane) per thread;
-//              P^T and dS^T from S^T and dP^T, the dQ read-out and its fp32
-//              reduction into global memory, the final dK/dV reduction
-//   warp 4     TMEM owner and tcgen05.mma issuer
-//   warp 5     TMA producer: K, V once, then Q_i, dO_i through 2 stages
-// TMEM (512 columns):
-//   [  0,128)  S^T = K Q_i^T (fp32); then P^T (bf16, cols 0..63) and
-//              dS^T (bf16, cols 64..127), the A operands of the dV / dK MMAs
-//   [128,256)  dP^T = V dO_i^T (fp32); then dQ_i = dS K (fp32, D columns)
-//   [256,384)  dV accumulator (D columns)     [384,512) dK accumulator
-// dS^T is also written to shared memory (128-byte swizzle, query-contiguous)
-// where it is the MN-major A operand of dQ = dS K.  Per query tile the tensor
-// core runs 5 MMAs of 128 x 128 x {d or 128}; MMAs issued by one thread
-// complete in order, which makes the reuse of the TMEM regions safe.
+// One CTA owns 128 keys (one KV tile) of one head and walks the queries from
+// its diagonal to the end of the sequence in sub-tiles of 64.  Two TMEM slots
+// alternate between sub-tiles so that the softmax-gradient work of sub-tile u
+// overlaps the tensor core's gradient MMAs of u-1 and score MMAs of u+1.
+//   warps 0-3  softmax gradient: one key row (TMEM lane) per thread; P^T and
+//              dS^T from S^T and dP^T
+//   warps 4-7  epilogue: dQ^T read-out (one d index per thread), staged in
+//              shared memory as a [64 queries x 32 d] fp32 block per warp and
+//              added into global dQ by one TMA reduce-add (the reduction runs
+//              in L2); at the end the dK / dV reduction
+//   warp 8     TMEM owner and tcgen05.mma issuer
+//   warp 9     TMA producer: K, V once, then Q_u, dO_u through 2 stages
+// TMEM (512 columns), slot s in {0, 1} at column 128 s:
+//   [+0, +64)   S^T_u = K Q_u^T (fp32); then P^T_u (bf16, +0..31) and
+//               dS^T_u (bf16, +32..63), A operands of the dV / dK MMAs
+//   [+64,+128)  dP^T_u = V dO_u^T (fp32); then dQ^T_u = K^T dS^T_u (fp32)
+//   [256, 256+d) dV accumulator      [384, 384+d) dK accumulator
+// dS^T_u is also written to shared memory (one 128-byte swizzled row per key)
+// where it is the MN-major B operand of dQ^T = K^T dS^T.  MMAs issued by one
+// thread complete in order, which makes the reuse of the TMEM slots safe.
+// For d = 64 the dQ^T MMA still runs with M = 128: its A operand reads past
+// the 64-wide K tile into the V tile (inside this CTA's shared memory) and
+// the extra 64 output rows are never stored.
 #include <algorithm>
 
 #include "internal.h"
@@ -35,21 +42,28 @@ namespace upipe {
 
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int BT = 128;  // keys per CTA = queries per step
+constexpr int kThreads = 320;
+constexpr int BK = 128;  // keys per CTA
+constexpr int BQ = 64;   // queries per sub-tile
+constexpr int NST = 2;   // Q/dO stages
 
 template <int D>
 struct BwdCfg {
-  static constexpr uint32_t TILE = BT * D * 2;           // K, V, Q or dO tile
-  static constexpr uint32_t BLOCK = BT * 64 * 2;         // one 64-column swizzled block
+  static constexpr uint32_t KV_TILE = BK * D * 2;
+  static constexpr uint32_t KV_BLOCK = BK * 64 * 2;      // 64-column block of K or V
+  static constexpr uint32_t Q_TILE = BQ * D * 2;
+  static constexpr uint32_t Q_BLOCK = BQ * 64 * 2;       // 64-column block of Q or dO
   static constexpr uint32_t K_OFF = 0;
-  static constexpr uint32_t V_OFF = TILE;
-  static constexpr uint32_t Q_OFF = 2 * TILE;            // [2] stages
-  static constexpr uint32_t DO_OFF = 4 * TILE;           // [2] stages
-  static constexpr uint32_t DS_OFF = 6 * TILE;           // dS^T [128 keys][128 queries] bf16
-  static constexpr uint32_t BAR_OFF = DS_OFF + BT * BT * 2;
-  static constexpr uint32_t SMEM_BYTES = BAR_OFF + 128 + 1024;
-  static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 384;
+  static constexpr uint32_t V_OFF = KV_TILE;
+  static constexpr uint32_t ST_OFF = 2 * KV_TILE;        // NST x (Q tile, dO tile)
+  static constexpr uint32_t ST_BYTES = 2 * Q_TILE;
+  static constexpr uint32_t DS_OFF = ST_OFF + NST * ST_BYTES;   // 2 x [128 keys][64 q] bf16
+  static constexpr uint32_t DS_BYTES = BK * BQ * 2;
+  static constexpr uint32_t DQS_OFF = DS_OFF + 2 * DS_BYTES;    // 4 warps x [64 q][32 d] fp32
+  static constexpr uint32_t DQS_BYTES = BQ * 32 * 4;
+  static constexpr uint32_t LD_OFF = DQS_OFF + 4 * DQS_BYTES;   // 4 warps x (64 lse + 64 D)
+  static constexpr uint32_t BAR_OFF = LD_OFF + 4 * 2 * BQ * 4;
+  static constexpr uint32_t SMEM_BYTES = BAR_OFF + 256 + 1024;
 };
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -62,22 +76,22 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
     const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
     const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap domap,
-    const AttnBwdArgs a, int* __restrict__ err) {
+    const __grid_constant__ CUtensorMap dqmap, const AttnBwdArgs a, int* __restrict__ err) {
   using Cfg = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::BAR_OFF);
   uint64_t* kv_full = bars + 0;
-  uint64_t* q_full = bars + 1;    // [2]
-  uint64_t* q_empty = bars + 3;   // [2]
-  uint64_t* s_full = bars + 5;
-  uint64_t* p_ready = bars + 6;
-  uint64_t* dq_full = bars + 7;
-  uint64_t* dq_free = bars + 8;
-  uint64_t* mma_done = bars + 9;
-  uint64_t* drain_bar = bars + 10;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
+  uint64_t* q_full = bars + 1;            // [NST]
+  uint64_t* q_empty = q_full + NST;       // [NST]
+  uint64_t* s_full = q_empty + NST;       // [2]
+  uint64_t* p_ready = s_full + 2;         // [2]
+  uint64_t* dq_full = p_ready + 2;        // [2]
+  uint64_t* dq_free = dq_full + 2;        // [2]
+  uint64_t* mma_done = dq_free + 2;
+  uint64_t* drain_bar = mma_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -86,31 +100,33 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
   const int jt = blockIdx.x;
   const int head = blockIdx.y;
   const int kvh = (a.h0 + head) / a.group - a.kv0;
-  const int k0 = jt * BT;
-  const int n_it = (S + BT - 1) / BT - jt;  // query tiles jt .. end
+  const int k0 = jt * BK;
+  const int n_u = (S - k0 + BQ - 1) / BQ;  // query sub-tiles from the diagonal on
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(&q_full[s], 1);
       mbar_init(&q_empty[s], 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(p_ready, 4);
-    mbar_init(dq_full, 1);
-    mbar_init(dq_free, 4);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_ready[s], 4);
+      mbar_init(&dq_full[s], 1);
+      mbar_init(&dq_free[s], 4);
+    }
     mbar_init(mma_done, 1);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5 && lane == 0) {
+  if (warp == 9 && lane == 0) {
     prefetch_tmap(&qmap);
     prefetch_tmap(&kmap);
     prefetch_tmap(&vmap);
     prefetch_tmap(&domap);
   }
-  if (warp == 4) {
+  if (warp == 8) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -119,25 +135,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 5) {
+  if (warp == 9) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t issued = 0, issued_phase = 0;
-      mbar_expect_tx(kv_full, 2 * Cfg::TILE);
+      mbar_expect_tx(kv_full, 2 * Cfg::KV_TILE);
       for (int b = 0; b < D / 64; ++b) {
-        tma_load_2d(smem + Cfg::K_OFF + b * Cfg::BLOCK, &kmap, kv_full, kvh * D + 64 * b, k0);
-        tma_load_2d(smem + Cfg::V_OFF + b * Cfg::BLOCK, &vmap, kv_full, kvh * D + 64 * b, k0);
+        tma_load_2d(smem + Cfg::K_OFF + b * Cfg::KV_BLOCK, &kmap, kv_full, kvh * D + 64 * b, k0);
+        tma_load_2d(smem + Cfg::V_OFF + b * Cfg::KV_BLOCK, &vmap, kv_full, kvh * D + 64 * b, k0);
       }
-      for (int it = 0; it < n_it; ++it) {
-        const int st = it & 1;
-        const uint32_t ph = (it >> 1) & 1;
+      for (int u = 0; u < n_u; ++u) {
+        const int st = u % NST;
+        const uint32_t ph = (u / NST) & 1;
         if (!mbar_wait(&q_empty[st], ph ^ 1, err, abort_flag)) break;
-        mbar_expect_tx(&q_full[st], 2 * Cfg::TILE);
-        const int q0 = (jt + it) * BT;
+        mbar_expect_tx(&q_full[st], Cfg::ST_BYTES);
+        const int q0 = k0 + u * BQ;
+        uint8_t* base = smem + Cfg::ST_OFF + st * Cfg::ST_BYTES;
         for (int b = 0; b < D / 64; ++b) {
-          tma_load_2d(smem + Cfg::Q_OFF + st * Cfg::TILE + b * Cfg::BLOCK, &qmap, &q_full[st],
-                      head * D + 64 * b, q0);
-          tma_load_2d(smem + Cfg::DO_OFF + st * Cfg::TILE + b * Cfg::BLOCK, &domap, &q_full[st],
+          tma_load_2d(base + b * Cfg::Q_BLOCK, &qmap, &q_full[st], head * D + 64 * b, q0);
+          tma_load_2d(base + Cfg::Q_TILE + b * Cfg::Q_BLOCK, &domap, &q_full[st],
                       head * D + 64 * b, q0);
         }
         issued |= 1u << st;
@@ -145,180 +161,216 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
       }
       if (*abort_flag) {
         mbar_wait_drain(kv_full, 0);
-        for (int s = 0; s < 2; ++s)
+        for (int s = 0; s < NST; ++s)
           if (issued & (1u << s)) mbar_wait_drain(&q_full[s], (issued_phase >> s) & 1u);
       }
     }
-  } else if (warp == 4) {
+  } else if (warp == 8) {
     // ---------------------------------------------------------- MMA issue
     if (lane == 0) {
-      constexpr uint32_t ID_S = idesc_bf16(128, 128, false, false);  // S^T, dP^T
+      constexpr uint32_t ID_S = idesc_bf16(128, BQ, false, false);   // S^T, dP^T
       constexpr uint32_t ID_ACC = idesc_bf16(128, D, false, true);   // dV, dK (A in TMEM)
-      constexpr uint32_t ID_DQ = idesc_bf16(128, D, true, true);     // dQ = dS K
+      constexpr uint32_t ID_DQ = idesc_bf16(128, BQ, true, true);    // dQ^T = K^T dS^T
       const uint32_t kb = smem_u32(smem + Cfg::K_OFF);
       const uint32_t vb = smem_u32(smem + Cfg::V_OFF);
-      const uint32_t dsb = smem_u32(smem + Cfg::DS_OFF);
       bool ok = mbar_wait(kv_full, 0, err, abort_flag);
-      for (int it = 0; it < n_it && ok; ++it) {
-        const int st = it & 1;
-        if (!mbar_wait(&q_full[st], (it >> 1) & 1, err, abort_flag)) break;
-        tc_fence_after();
-        const uint32_t qb = smem_u32(smem + Cfg::Q_OFF + st * Cfg::TILE);
-        const uint32_t dob = smem_u32(smem + Cfg::DO_OFF + st * Cfg::TILE);
-        // S^T = K Q^T  (k over d)
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k / 4) * Cfg::BLOCK + (k % 4) * 32;
-          mma_ss(tmem + Cfg::COL_S, sdesc_sw128(kb + off, 16, 1024),
-                 sdesc_sw128(qb + off, 16, 1024), ID_S, k > 0);
-        }
-        // dP^T = V dO^T, into the region dQ of the previous step used
-        if (it > 0) {
-          if (!mbar_wait(dq_free, (it - 1) & 1, err, abort_flag)) break;
+      for (int u = 0; u <= n_u && ok; ++u) {
+        if (u < n_u) {
+          const int s = u & 1, st = u % NST;
+          if (!mbar_wait(&q_full[st], (u / NST) & 1, err, abort_flag)) break;
+          if (u >= 2 && !mbar_wait(&dq_free[s], ((u - 2) >> 1) & 1, err, abort_flag)) break;
           tc_fence_after();
-        }
+          const uint32_t qb = smem_u32(smem + Cfg::ST_OFF + st * Cfg::ST_BYTES);
+          const uint32_t dob = qb + Cfg::Q_TILE;
+          const uint32_t slot = tmem + 128 * s;
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k / 4) * Cfg::BLOCK + (k % 4) * 32;
-          mma_ss(tmem + Cfg::COL_DP, sdesc_sw128(vb + off, 16, 1024),
-                 sdesc_sw128(dob + off, 16, 1024), ID_S, k > 0);
-        }
-        mma_commit(s_full);
-        if (!mbar_wait(p_ready, it & 1, err, abort_flag)) break;
-        tc_fence_after();
-        // dQ = dS K  (k over keys; A = dS from dS^T in smem, MN-major)
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t ko = (k / 4) * Cfg::KV_BLOCK + (k % 4) * 32;
+            const uint32_t qo = (k / 4) * Cfg::Q_BLOCK + (k % 4) * 32;
+            mma_ss(slot, sdesc_sw128(kb + ko, 16, 1024), sdesc_sw128(qb + qo, 16, 1024), ID_S,
+                   k > 0);
+          }
 #pragma unroll
-        for (int k = 0; k < BT / 16; ++k)
-          mma_ss(tmem + Cfg::COL_DP, sdesc_sw128(dsb + k * 2048, Cfg::BLOCK, 1024),
-                 sdesc_sw128(kb + k * 2048, Cfg::BLOCK, 1024), ID_DQ, k > 0);
-        mma_commit(dq_full);
-        // dV += P^T dO ; dK += dS^T Q  (k over queries; A in TMEM)
-#pragma unroll
-        for (int k = 0; k < BT / 16; ++k) {
-          const uint32_t acc = (it > 0 || k > 0) ? 1u : 0u;
-          mma_ts(tmem + Cfg::COL_DV, tmem + Cfg::COL_S + k * 8,
-                 sdesc_sw128(dob + k * 2048, Cfg::BLOCK, 1024), ID_ACC, acc);
-          mma_ts(tmem + Cfg::COL_DK, tmem + Cfg::COL_S + 64 + k * 8,
-                 sdesc_sw128(qb + k * 2048, Cfg::BLOCK, 1024), ID_ACC, acc);
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t ko = (k / 4) * Cfg::KV_BLOCK + (k % 4) * 32;
+            const uint32_t qo = (k / 4) * Cfg::Q_BLOCK + (k % 4) * 32;
+            mma_ss(slot + 64, sdesc_sw128(vb + ko, 16, 1024), sdesc_sw128(dob + qo, 16, 1024),
+                   ID_S, k > 0);
+          }
+          mma_commit(&s_full[s]);
         }
-        mma_commit(&q_empty[st]);
+        if (u >= 1) {
+          const int v = u - 1, sv = v & 1, stv = v % NST;
+          if (!mbar_wait(&p_ready[sv], (v >> 1) & 1, err, abort_flag)) break;
+          tc_fence_after();
+          const uint32_t qb = smem_u32(smem + Cfg::ST_OFF + stv * Cfg::ST_BYTES);
+          const uint32_t dob = qb + Cfg::Q_TILE;
+          const uint32_t slot = tmem + 128 * sv;
+          const uint32_t dsb = smem_u32(smem + Cfg::DS_OFF + sv * Cfg::DS_BYTES);
+          // dV += P^T dO ; dK += dS^T Q   (k over the sub-tile's 64 queries)
+#pragma unroll
+          for (int k = 0; k < BQ / 16; ++k) {
+            const uint32_t acc = (v > 0 || k > 0) ? 1u : 0u;
+            mma_ts(tmem + 256, slot + k * 8, sdesc_sw128(dob + k * 2048, Cfg::Q_BLOCK, 1024),
+                   ID_ACC, acc);
+            mma_ts(tmem + 384, slot + 32 + k * 8,
+                   sdesc_sw128(qb + k * 2048, Cfg::Q_BLOCK, 1024), ID_ACC, acc);
+          }
+          // dQ^T = K^T dS^T  (k over the 128 keys; both operands MN-major)
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma_ss(slot + 64, sdesc_sw128(kb + k * 2048, Cfg::KV_BLOCK, 1024),
+                   sdesc_sw128(dsb + k * 2048, Cfg::Q_BLOCK, 1024), ID_DQ, k > 0);
+          mma_commit(&dq_full[sv]);
+          mma_commit(&q_empty[stv]);
+        }
       }
       mma_commit(mma_done);
     }
-  } else {
-    // ------------------------------------- softmax gradient + epilogue warps
+  } else if (warp < 4) {
+    // ------------------------------------------------- softmax gradient
     const int r = warp * 32 + lane;  // key row within the tile (TMEM lane)
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     const float sl2 = a.scale * 1.4426950408889634f;
     const float* lse_g = a.lse + (long long)head * a.lse_stride;
     const float* D_g = a.D + (long long)head * S;
-    uint8_t* ds_row = smem + Cfg::DS_OFF + r * 128;
-    bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
-      const int q0 = (jt + it) * BT;
-      // lse (log2 units) and D of this tile's 128 queries: lane l holds
-      // queries l + 32m; a column's value is broadcast with a shuffle whose
-      // source lane and register are compile-time constants
-      float lse_r[4], dd_r[4];
+    float* ld_w = reinterpret_cast<float*>(smem + Cfg::LD_OFF) + warp * 2 * BQ;  // this warp's
+    // lse (log2 units) and D of the queries of sub-tile u, loaded one sub-tile
+    // ahead: lane l holds queries l and l + 32
+    float nl[2], nd[2];
+    auto fetch = [&](int u) {
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int q = q0 + 32 * m + lane;
-        lse_r[m] = q < S ? lse_g[q] * 1.4426950408889634f : INFINITY;
-        dd_r[m] = q < S ? D_g[q] : 0.f;
+      for (int m = 0; m < 2; ++m) {
+        const int q = k0 + u * BQ + 32 * m + lane;
+        nl[m] = q < S ? lse_g[q] * 1.4426950408889634f : INFINITY;
+        nd[m] = q < S ? D_g[q] : 0.f;
       }
-      ok = __all_sync(0xffffffffu, mbar_wait(s_full, it & 1, err, abort_flag));
-      if (!ok) break;
-      tc_fence_after();
-      const bool diag = (it == 0);
-      float p[128];
+    };
+    fetch(0);
+    for (int u = 0; u < n_u; ++u) {
+      const int s = u & 1;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int m = 0; m < 2; ++m) {
+        ld_w[32 * m + lane] = nl[m];
+        ld_w[BQ + 32 * m + lane] = nd[m];
+      }
+      __syncwarp();
+      if (u + 1 < n_u) fetch(u + 1);
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[s], (u >> 1) & 1, err, abort_flag))) break;
+      tc_fence_after();
+      const uint32_t slot = tmem + lane_off + 128 * s;
+      const float4* lse4 = reinterpret_cast<const float4*>(ld_w);
+      const float4* dd4 = reinterpret_cast<const float4*>(ld_w + BQ);
+      const int mask_from = r - u * BQ;  // columns c < mask_from hold key > query: masked
+      float p[BQ];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
         uint32_t rr[32];
-        tmem_ld32(tmem + lane_off + Cfg::COL_S + 32 * c, rr);
+        tmem_ld32(slot + 32 * h, rr);
         tmem_ld_wait(rr);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int q = 32 * c + i;
-          const float lq = __shfl_sync(0xffffffffu, lse_r[c], i);
-          float v = ex2(fmaf(__uint_as_float(rr[i]), sl2, -lq));
-          if (diag && r > q) v = 0.f;
-          p[q] = v;
-        }
-      }
-      // P^T (bf16) over the first half of S^T
+        for (int i = 0; i < 32; i += 4) {
+          const float4 l4 = lse4[(32 * h + i) / 4];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) pk[i] = pack_bf16(p[64 * h + 2 * i], p[64 * h + 2 * i + 1]);
-        tmem_st32(tmem + lane_off + Cfg::COL_S + 32 * h, pk);
-      }
-      // dS^T = P^T (dP^T - D): TMEM (second half of S^T) and shared memory
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t rr[32];
-          tmem_ld32(tmem + lane_off + Cfg::COL_DP + 64 * h + 32 * c, rr);
-          tmem_ld_wait(rr);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int q = 64 * h + 32 * c + 2 * i;
-            const float D0 = __shfl_sync(0xffffffffu, dd_r[q >> 5], q & 31);
-            const float D1 = __shfl_sync(0xffffffffu, dd_r[(q + 1) >> 5], (q + 1) & 31);
-            const float d0 = p[q] * (__uint_as_float(rr[2 * i]) - D0);
-            const float d1 = p[q + 1] * (__uint_as_float(rr[2 * i + 1]) - D1);
-            pk[16 * c + i] = pack_bf16(d0, d1);
+          for (int e = 0; e < 4; ++e) {
+            const int c = 32 * h + i + e;
+            const float v = ex2(fmaf(__uint_as_float(rr[i + e]), sl2, -lv[e]));
+            p[c] = (c < mask_from) ? 0.f : v;
           }
         }
-        tmem_st32(tmem + lane_off + Cfg::COL_S + 64 + 32 * h, pk);
-        uint8_t* blk = ds_row + h * Cfg::BLOCK;
+      }
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pk[i] = pack_bf16(p[2 * i], p[2 * i + 1]);
+        tmem_st32(slot, pk);
+      }
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t rr[32];
+          tmem_ld32(slot + 64 + 32 * h, rr);
+          tmem_ld_wait(rr);
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 d4 = dd4[(32 * h + i) / 4];
+            const int c = 32 * h + i;
+            const float g0 = p[c] * (__uint_as_float(rr[i]) - d4.x);
+            const float g1 = p[c + 1] * (__uint_as_float(rr[i + 1]) - d4.y);
+            const float g2 = p[c + 2] * (__uint_as_float(rr[i + 2]) - d4.z);
+            const float g3 = p[c + 3] * (__uint_as_float(rr[i + 3]) - d4.w);
+            pk[c / 2] = pack_bf16(g0, g1);
+            pk[c / 2 + 1] = pack_bf16(g2, g3);
+          }
+        }
+        tmem_st32(slot + 32, pk);
+        uint8_t* row = smem + Cfg::DS_OFF + s * Cfg::DS_BYTES + r * 128;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch)
-          *reinterpret_cast<uint4*>(blk + ((ch ^ (r & 7)) << 4)) =
+          *reinterpret_cast<uint4*>(row + ((ch ^ (r & 7)) << 4)) =
               make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
       }
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_ready);
-      // dQ rows (query q0 + r): read out, free the region, reduce to global
-      ok = __all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, err, abort_flag));
+      if (lane == 0) mbar_arrive(&p_ready[s]);
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ epilogue
+    const int qw = warp & 3;
+    const int t = qw * 32 + lane;  // dQ^T: d index; dK/dV: key row
+    const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
+    bool ok = true;
+    for (int u = 0; u < n_u; ++u) {
+      const int s = u & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&dq_full[s], (u >> 1) & 1, err, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      float dq[D];
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(tmem + lane_off + Cfg::COL_DP + 32 * c, rr);
-        tmem_ld_wait(rr);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) dq[32 * c + i] = __uint_as_float(rr[i]);
-      }
+      uint32_t lo[32], hi[32];
+      tmem_ld32(tmem + lane_off + 128 * s + 64, lo);
+      tmem_ld_wait(lo);
+      tmem_ld32(tmem + lane_off + 128 * s + 96, hi);
+      tmem_ld_wait(hi);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(dq_free);
-      if (q0 + r < S) {
-        float* dst = a.dQ + (long long)(q0 + r) * a.ld_dq + head * D;
+      if (lane == 0) mbar_arrive(&dq_free[s]);
+      const int q0 = k0 + u * BQ;
+      if (qw * 32 < D) {
+        // [64 queries][32 d] fp32 block of this warp, 128-byte swizzled rows
+        uint8_t* blk = smem + Cfg::DQS_OFF + qw * Cfg::DQS_BYTES;
+        if (lane == 0) bulk_wait_read<0>();   // the previous reduce has read the block
+        __syncwarp();
+        const uint32_t cb = (uint32_t)(lane >> 2), cw = (uint32_t)(lane & 3) * 4;
 #pragma unroll
-        for (int i = 0; i < D; i += 4)
-          red_add_v4_f32(dst + i, dq[i] * a.scale, dq[i + 1] * a.scale, dq[i + 2] * a.scale,
-                         dq[i + 3] * a.scale);
+        for (int c = 0; c < 32; ++c) {
+          *reinterpret_cast<float*>(blk + c * 128 + ((cb ^ (c & 7)) << 4) + cw) =
+              __uint_as_float(lo[c]) * a.scale;
+          *reinterpret_cast<float*>(blk + (32 + c) * 128 + ((cb ^ ((32 + c) & 7)) << 4) + cw) =
+              __uint_as_float(hi[c]) * a.scale;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_2d(&dqmap, blk, head * D + 32 * qw, q0);
+          bulk_commit();
+        }
       }
     }
-    // final dK, dV of this CTA's keys
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(mma_done, 0, err, abort_flag));
     if (ok) {
       tc_fence_after();
-      const int key = k0 + r;
+      const int key = k0 + t;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t rv[32], rk[32];
-        tmem_ld32(tmem + lane_off + Cfg::COL_DV + 32 * c, rv);
+        tmem_ld32(tmem + lane_off + 256 + 32 * c, rv);
         tmem_ld_wait(rv);
-        tmem_ld32(tmem + lane_off + Cfg::COL_DK + 32 * c, rk);
+        tmem_ld32(tmem + lane_off + 384 + 32 * c, rk);
         tmem_ld_wait(rk);
         if (key < S) {
           const long long off = (long long)key * a.ld_dkv + kvh * D + 32 * c;
@@ -339,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
   // --------------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == 8) {
     if (*abort_flag) {
       if (lane == 0) {
         mma_commit(drain_bar);
@@ -363,14 +415,15 @@ static cudaError_t launch_bwd_t(const AttnBwdArgs& a, int* err, cudaStream_t str
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  CUtensorMap qm, km, vm, dm;
-  if (!make_tmap_bf16(&qm, a.Q, a.S, (uint64_t)a.heads * D, a.ldq, BT, 64) ||
-      !make_tmap_bf16(&km, a.K, a.S, (uint64_t)a.ldkv, a.ldkv, BT, 64) ||
-      !make_tmap_bf16(&vm, a.V, a.S, (uint64_t)a.ldkv, a.ldkv, BT, 64) ||
-      !make_tmap_bf16(&dm, a.dO, a.S, (uint64_t)a.heads * D, a.ld_do, BT, 64))
+  CUtensorMap qm, km, vm, dm, dqm;
+  if (!make_tmap_f32(&dqm, a.dQ, a.S, (uint64_t)a.ld_dq, a.ld_dq, BQ, 32) ||
+      !make_tmap_bf16(&qm, a.Q, a.S, (uint64_t)a.heads * D, a.ldq, BQ, 64) ||
+      !make_tmap_bf16(&km, a.K, a.S, (uint64_t)a.ldkv, a.ldkv, BK, 64) ||
+      !make_tmap_bf16(&vm, a.V, a.S, (uint64_t)a.ldkv, a.ldkv, BK, 64) ||
+      !make_tmap_bf16(&dm, a.dO, a.S, (uint64_t)a.heads * D, a.ld_do, BQ, 64))
     return cudaErrorInvalidValue;
-  dim3 grid((a.S + BT - 1) / BT, a.heads);
-  attn_bwd_kernel<D><<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(qm, km, vm, dm, a, err);
+  dim3 grid((a.S + BK - 1) / BK, a.heads);
+  attn_bwd_kernel<D><<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(qm, km, vm, dm, dqm, a, err);
   return cudaGetLastError();
 }
 

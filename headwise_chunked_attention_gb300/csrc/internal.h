@@ -19,6 +19,10 @@ using bf16 = __nv_bfloat16;
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                     uint64_t ld, uint32_t box_rows, uint32_t box_cols);
 
+// The same for an fp32 matrix; box_cols * 4 must be 128 (128-byte swizzle).
+bool make_tmap_f32(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                   uint64_t ld, uint32_t box_rows, uint32_t box_cols);
+
 // ------------------------------------------------------------------ GEMM --
 
 enum EpiKind : int {
