@@ -12,14 +12,15 @@
 //
 // One CTA owns 128 keys (one KV tile) of one head and walks the queries from
 // its diagonal to the end of the sequence in sub-tiles of 64.  Two TMEM slots
-// alternate between sub-tiles so that the softmax-gradient work of sub-tile u
-// overlaps the tensor core's gradient MMAs of u-1 and score MMAs of u+1.
-//   warps 0-3  softmax gradient: one key row (TMEM lane) per thread; P^T and
-//              dS^T from S^T and dP^T
-//   warps 4-7  epilogue: dQ^T read-out (one d index per thread), staged in
-//              shared memory as a [64 queries x 32 d] fp32 block per warp and
-//              added into global dQ by one TMA reduce-add (the reduction runs
-//              in L2); at the end the dK / dV reduction
+// alternate between sub-tiles, each with its own warpgroup, so that the
+// softmax-gradient work of one slot overlaps the tensor core's work on the
+// other slot and the two warpgroups overlap each other.
+//   warps 0-3  warpgroup of slot 0 (even sub-tiles), warps 4-7 of slot 1 (odd):
+//              softmax gradient with one key row (TMEM lane) per thread (P^T,
+//              dS^T from S^T, dP^T), then the dQ^T read-out with one d index
+//              per thread, staged in shared memory as [32 queries x 32 d] fp32
+//              blocks and added into global dQ by TMA reduce-add (the
+//              reduction runs in L2); at the end dV (slot 0) / dK (slot 1)
 //   warp 8     TMEM owner and tcgen05.mma issuer
 //   warp 9     TMA producer: K, V once, then Q_u, dO_u through 2 stages
 // TMEM (512 columns), slot s in {0, 1} at column 128 s:
@@ -59,10 +60,10 @@ struct BwdCfg {
   static constexpr uint32_t ST_BYTES = 2 * Q_TILE;
   static constexpr uint32_t DS_OFF = ST_OFF + NST * ST_BYTES;   // 2 x [128 keys][64 q] bf16
   static constexpr uint32_t DS_BYTES = BK * BQ * 2;
-  static constexpr uint32_t DQS_OFF = DS_OFF + 2 * DS_BYTES;    // 4 warps x [64 q][32 d] fp32
-  static constexpr uint32_t DQS_BYTES = BQ * 32 * 4;
-  static constexpr uint32_t LD_OFF = DQS_OFF + 4 * DQS_BYTES;   // 4 warps x (64 lse + 64 D)
-  static constexpr uint32_t BAR_OFF = LD_OFF + 4 * 2 * BQ * 4;
+  static constexpr uint32_t DQS_OFF = DS_OFF + 2 * DS_BYTES;    // 8 warps x [32 q][32 d] fp32
+  static constexpr uint32_t DQS_BYTES = 32 * 32 * 4;
+  static constexpr uint32_t LD_OFF = DQS_OFF + 8 * DQS_BYTES;   // 8 warps x (64 lse + 64 D)
+  static constexpr uint32_t BAR_OFF = LD_OFF + 8 * 2 * BQ * 4;
   static constexpr uint32_t SMEM_BYTES = BAR_OFF + 256 + 1024;
 };
 
@@ -113,7 +114,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
       mbar_init(&s_full[s], 1);
       mbar_init(&p_ready[s], 4);
       mbar_init(&dq_full[s], 1);
-      mbar_init(&dq_free[s], 4);
+      mbar_init(&dq_free[s], 4);   // the 4 warps of slot s's warpgroup
     }
     mbar_init(mma_done, 1);
     mbar_init(drain_bar, 1);
@@ -167,18 +168,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
     }
   } else if (warp == 8) {
     // ---------------------------------------------------------- MMA issue
-    if (lane == 0) {
+    {  // whole warp; one elected lane issues
       constexpr uint32_t ID_S = idesc_bf16(128, BQ, false, false);   // S^T, dP^T
       constexpr uint32_t ID_ACC = idesc_bf16(128, D, false, true);   // dV, dK (A in TMEM)
       constexpr uint32_t ID_DQ = idesc_bf16(128, BQ, true, true);    // dQ^T = K^T dS^T
       const uint32_t kb = smem_u32(smem + Cfg::K_OFF);
       const uint32_t vb = smem_u32(smem + Cfg::V_OFF);
-      bool ok = mbar_wait(kv_full, 0, err, abort_flag);
+      bool ok = mbar_wait_warp(kv_full, 0, err, abort_flag);
       for (int u = 0; u <= n_u && ok; ++u) {
         if (u < n_u) {
           const int s = u & 1, st = u % NST;
-          if (!mbar_wait(&q_full[st], (u / NST) & 1, err, abort_flag)) break;
-          if (u >= 2 && !mbar_wait(&dq_free[s], ((u - 2) >> 1) & 1, err, abort_flag)) break;
+          if (!mbar_wait_warp(&q_full[st], (u / NST) & 1, err, abort_flag)) break;
+          if (u >= 2 && !mbar_wait_warp(&dq_free[s], ((u - 2) >> 1) & 1, err, abort_flag)) break;
           tc_fence_after();
           const uint32_t qb = smem_u32(smem + Cfg::ST_OFF + st * Cfg::ST_BYTES);
           const uint32_t dob = qb + Cfg::Q_TILE;
@@ -187,21 +188,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t ko = (k / 4) * Cfg::KV_BLOCK + (k % 4) * 32;
             const uint32_t qo = (k / 4) * Cfg::Q_BLOCK + (k % 4) * 32;
-            mma_ss(slot, sdesc_sw128(kb + ko, 16, 1024), sdesc_sw128(qb + qo, 16, 1024), ID_S,
+            mma_ss_w(slot, sdesc_sw128(kb + ko, 16, 1024), sdesc_sw128(qb + qo, 16, 1024), ID_S,
                    k > 0);
           }
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t ko = (k / 4) * Cfg::KV_BLOCK + (k % 4) * 32;
             const uint32_t qo = (k / 4) * Cfg::Q_BLOCK + (k % 4) * 32;
-            mma_ss(slot + 64, sdesc_sw128(vb + ko, 16, 1024), sdesc_sw128(dob + qo, 16, 1024),
+            mma_ss_w(slot + 64, sdesc_sw128(vb + ko, 16, 1024), sdesc_sw128(dob + qo, 16, 1024),
                    ID_S, k > 0);
           }
-          mma_commit(&s_full[s]);
+          mma_commit_w(&s_full[s]);
         }
         if (u >= 1) {
           const int v = u - 1, sv = v & 1, stv = v % NST;
-          if (!mbar_wait(&p_ready[sv], (v >> 1) & 1, err, abort_flag)) break;
+          if (!mbar_wait_warp(&p_ready[sv], (v >> 1) & 1, err, abort_flag)) break;
           tc_fence_after();
           const uint32_t qb = smem_u32(smem + Cfg::ST_OFF + stv * Cfg::ST_BYTES);
           const uint32_t dob = qb + Cfg::Q_TILE;
@@ -211,32 +212,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
 #pragma unroll
           for (int k = 0; k < BQ / 16; ++k) {
             const uint32_t acc = (v > 0 || k > 0) ? 1u : 0u;
-            mma_ts(tmem + 256, slot + k * 8, sdesc_sw128(dob + k * 2048, Cfg::Q_BLOCK, 1024),
+            mma_ts_w(tmem + 256, slot + k * 8, sdesc_sw128(dob + k * 2048, Cfg::Q_BLOCK, 1024),
                    ID_ACC, acc);
-            mma_ts(tmem + 384, slot + 32 + k * 8,
+            mma_ts_w(tmem + 384, slot + 32 + k * 8,
                    sdesc_sw128(qb + k * 2048, Cfg::Q_BLOCK, 1024), ID_ACC, acc);
           }
           // dQ^T = K^T dS^T  (k over the 128 keys; both operands MN-major)
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            mma_ss(slot + 64, sdesc_sw128(kb + k * 2048, Cfg::KV_BLOCK, 1024),
+            mma_ss_w(slot + 64, sdesc_sw128(kb + k * 2048, Cfg::KV_BLOCK, 1024),
                    sdesc_sw128(dsb + k * 2048, Cfg::Q_BLOCK, 1024), ID_DQ, k > 0);
-          mma_commit(&dq_full[sv]);
-          mma_commit(&q_empty[stv]);
+          mma_commit_w(&dq_full[sv]);
+          mma_commit_w(&q_empty[stv]);
         }
       }
-      mma_commit(mma_done);
+      mma_commit_w(mma_done);
     }
-  } else if (warp < 4) {
-    // ------------------------------------------------- softmax gradient
-    const int r = warp * 32 + lane;  // key row within the tile (TMEM lane)
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+  } else {
+    // --------------------- slot warpgroups: softmax gradient, dQ, dK / dV
+    const int wg = warp >> 2;        // slot served by this warpgroup
+    const int qw = warp & 3;
+    const int r = qw * 32 + lane;    // TMEM lane: key row of S^T/dP^T, d index of dQ^T
+    const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
+    const uint32_t slot = tmem + lane_off + 128 * wg;
     const float sl2 = a.scale * 1.4426950408889634f;
     const float* lse_g = a.lse + (long long)head * a.lse_stride;
     const float* D_g = a.D + (long long)head * S;
     float* ld_w = reinterpret_cast<float*>(smem + Cfg::LD_OFF) + warp * 2 * BQ;  // this warp's
-    // lse (log2 units) and D of the queries of sub-tile u, loaded one sub-tile
-    // ahead: lane l holds queries l and l + 32
+    uint8_t* stage_w = smem + Cfg::DQS_OFF + warp * Cfg::DQS_BYTES;              // this warp's
+    uint8_t* ds_rows = smem + Cfg::DS_OFF + wg * Cfg::DS_BYTES + r * 128;
+    // lse (log2 units) and D of the queries of a sub-tile, loaded one sub-tile
+    // of this slot ahead: lane l holds queries l and l + 32
     float nl[2], nd[2];
     auto fetch = [&](int u) {
 #pragma unroll
@@ -246,19 +252,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
         nd[m] = q < S ? D_g[q] : 0.f;
       }
     };
-    fetch(0);
-    for (int u = 0; u < n_u; ++u) {
-      const int s = u & 1;
+    if (wg < n_u) fetch(wg);
+    bool ok = true;
+    for (int u = wg; u < n_u; u += 2) {
+      const uint32_t ph = (u >> 1) & 1;
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
         ld_w[32 * m + lane] = nl[m];
         ld_w[BQ + 32 * m + lane] = nd[m];
       }
       __syncwarp();
-      if (u + 1 < n_u) fetch(u + 1);
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[s], (u >> 1) & 1, err, abort_flag))) break;
+      if (u + 2 < n_u) fetch(u + 2);
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[wg], ph, err, abort_flag));
+      if (!ok) break;
       tc_fence_after();
-      const uint32_t slot = tmem + lane_off + 128 * s;
       const float4* lse4 = reinterpret_cast<const float4*>(ld_w);
       const float4* dd4 = reinterpret_cast<const float4*>(ld_w + BQ);
       const int mask_from = r - u * BQ;  // columns c < mask_from hold key > query: masked
@@ -271,14 +278,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
           const float4 l4 = lse4[(32 * h + i) / 4];
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = 32 * h + i + e;
-            const float v = ex2(fmaf(__uint_as_float(rr[i + e]), sl2, -lv[e]));
-            p[c] = (c < mask_from) ? 0.f : v;
-          }
+          p[32 * h + i] = ex2(fmaf(__uint_as_float(rr[i]), sl2, -l4.x));
+          p[32 * h + i + 1] = ex2(fmaf(__uint_as_float(rr[i + 1]), sl2, -l4.y));
+          p[32 * h + i + 2] = ex2(fmaf(__uint_as_float(rr[i + 2]), sl2, -l4.z));
+          p[32 * h + i + 3] = ex2(fmaf(__uint_as_float(rr[i + 3]), sl2, -l4.w));
         }
+      }
+      if (mask_from > 0) {  // only the two sub-tiles on the diagonal
+#pragma unroll
+        for (int c = 0; c < BQ; ++c)
+          if (c < mask_from) p[c] = 0.f;
       }
       {
         uint32_t pk[32];
@@ -306,83 +315,71 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
           }
         }
         tmem_st32(slot + 32, pk);
-        uint8_t* row = smem + Cfg::DS_OFF + s * Cfg::DS_BYTES + r * 128;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch)
-          *reinterpret_cast<uint4*>(row + ((ch ^ (r & 7)) << 4)) =
+          *reinterpret_cast<uint4*>(ds_rows + ((ch ^ (r & 7)) << 4)) =
               make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
       }
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_ready[s]);
-    }
-  } else if (warp < 8) {
-    // ------------------------------------------------------------ epilogue
-    const int qw = warp & 3;
-    const int t = qw * 32 + lane;  // dQ^T: d index; dK/dV: key row
-    const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
-    bool ok = true;
-    for (int u = 0; u < n_u; ++u) {
-      const int s = u & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&dq_full[s], (u >> 1) & 1, err, abort_flag));
+      if (lane == 0) mbar_arrive(&p_ready[wg]);
+
+      // dQ^T of this sub-tile: read out, free the slot, reduce into global dQ
+      ok = __all_sync(0xffffffffu, mbar_wait(&dq_full[wg], ph, err, abort_flag));
       if (!ok) break;
       tc_fence_after();
       uint32_t lo[32], hi[32];
-      tmem_ld32(tmem + lane_off + 128 * s + 64, lo);
+      tmem_ld32(slot + 64, lo);
       tmem_ld_wait(lo);
-      tmem_ld32(tmem + lane_off + 128 * s + 96, hi);
+      tmem_ld32(slot + 96, hi);
       tmem_ld_wait(hi);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&dq_free[s]);
-      const int q0 = k0 + u * BQ;
+      if (lane == 0) mbar_arrive(&dq_free[wg]);
       if (qw * 32 < D) {
-        // [64 queries][32 d] fp32 block of this warp, 128-byte swizzled rows
-        uint8_t* blk = smem + Cfg::DQS_OFF + qw * Cfg::DQS_BYTES;
-        if (lane == 0) bulk_wait_read<0>();   // the previous reduce has read the block
-        __syncwarp();
+        const int q0 = k0 + u * BQ;
         const uint32_t cb = (uint32_t)(lane >> 2), cw = (uint32_t)(lane & 3) * 4;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          *reinterpret_cast<float*>(blk + c * 128 + ((cb ^ (c & 7)) << 4) + cw) =
-              __uint_as_float(lo[c]) * a.scale;
-          *reinterpret_cast<float*>(blk + (32 + c) * 128 + ((cb ^ ((32 + c) & 7)) << 4) + cw) =
-              __uint_as_float(hi[c]) * a.scale;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_reduce_add_2d(&dqmap, blk, head * D + 32 * qw, q0);
-          bulk_commit();
+        for (int half = 0; half < 2; ++half) {
+          if (lane == 0) bulk_wait_read<0>();   // the previous reduce has read the block
+          __syncwarp();
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            *reinterpret_cast<float*>(stage_w + c * 128 + ((cb ^ (c & 7)) << 4) + cw) =
+                __uint_as_float(half ? hi[c] : lo[c]) * a.scale;
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_2d(&dqmap, stage_w, head * D + 32 * qw, q0 + 32 * half);
+            bulk_commit();
+          }
         }
       }
     }
     if (lane == 0) bulk_wait_all();
     __syncwarp();
+    // dV (slot-0 warpgroup) and dK (slot-1 warpgroup) of this CTA's keys
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(mma_done, 0, err, abort_flag));
     if (ok) {
       tc_fence_after();
-      const int key = k0 + t;
+      const int key = k0 + r;
+      float* dst = wg == 0 ? a.dV : a.dK;
+      const float mul = wg == 0 ? 1.f : a.scale;
+      const uint32_t col = wg == 0 ? 256u : 384u;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
-        uint32_t rv[32], rk[32];
-        tmem_ld32(tmem + lane_off + 256 + 32 * c, rv);
+        uint32_t rv[32];
+        tmem_ld32(tmem + lane_off + col + 32 * c, rv);
         tmem_ld_wait(rv);
-        tmem_ld32(tmem + lane_off + 384 + 32 * c, rk);
-        tmem_ld_wait(rk);
         if (key < S) {
           const long long off = (long long)key * a.ld_dkv + kvh * D + 32 * c;
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            red_add_v4_f32(a.dV + off + i, __uint_as_float(rv[i]), __uint_as_float(rv[i + 1]),
-                           __uint_as_float(rv[i + 2]), __uint_as_float(rv[i + 3]));
-            red_add_v4_f32(a.dK + off + i, __uint_as_float(rk[i]) * a.scale,
-                           __uint_as_float(rk[i + 1]) * a.scale,
-                           __uint_as_float(rk[i + 2]) * a.scale,
-                           __uint_as_float(rk[i + 3]) * a.scale);
-          }
+          for (int i = 0; i < 32; i += 4)
+            red_add_v4_f32(dst + off + i, __uint_as_float(rv[i]) * mul,
+                           __uint_as_float(rv[i + 1]) * mul, __uint_as_float(rv[i + 2]) * mul,
+                           __uint_as_float(rv[i + 3]) * mul);
         }
       }
     }
@@ -416,7 +413,7 @@ static cudaError_t launch_bwd_t(const AttnBwdArgs& a, int* err, cudaStream_t str
     attr_set = true;
   }
   CUtensorMap qm, km, vm, dm, dqm;
-  if (!make_tmap_f32(&dqm, a.dQ, a.S, (uint64_t)a.ld_dq, a.ld_dq, BQ, 32) ||
+  if (!make_tmap_f32(&dqm, a.dQ, a.S, (uint64_t)a.ld_dq, a.ld_dq, 32, 32) ||
       !make_tmap_bf16(&qm, a.Q, a.S, (uint64_t)a.heads * D, a.ldq, BQ, 64) ||
       !make_tmap_bf16(&km, a.K, a.S, (uint64_t)a.ldkv, a.ldkv, BK, 64) ||
       !make_tmap_bf16(&vm, a.V, a.S, (uint64_t)a.ldkv, a.ldkv, BK, 64) ||

@@ -139,14 +139,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 8) {
     // ---------------------------------------------------------- MMA issue
-    if (lane == 0) {
+    {  // whole warp; one elected lane issues
       constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
       constexpr uint32_t IDESC_O = idesc_bf16(128, D, false, true);
       const uint32_t q_base = smem_u32(smem + Cfg::Q_OFF);
       const uint32_t slot_base = smem_u32(smem + Cfg::SLOT_OFF);
       uint32_t p_phase[2] = {0, 0};
       const int n0 = n_kv - 1;
-      bool ok = mbar_wait(q_full, 0, err, abort_flag);
+      bool ok = mbar_wait_warp(q_full, 0, err, abort_flag);
       for (int j = 0; j <= n_kv && ok; ++j) {
         const int kidx = 2 * j;
         const int vidx = 2 * j - 1;  // V_{j-1}
@@ -154,17 +154,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int vslot = j >= 1 ? vidx % kSlots : 0;
         const uint32_t v_addr = slot_base + vslot * Cfg::TILE_BYTES;
         if (j < n_kv) {
-          if (!mbar_wait(&slot_full[kidx % kSlots], (kidx / kSlots) & 1, err, abort_flag)) break;
+          if (!mbar_wait_warp(&slot_full[kidx % kSlots], (kidx / kSlots) & 1, err, abort_flag)) break;
         }
         if (j >= 1) {
-          if (!mbar_wait(&slot_full[vslot], (vidx / kSlots) & 1, err, abort_flag)) break;
+          if (!mbar_wait_warp(&slot_full[vslot], (vidx / kSlots) & 1, err, abort_flag)) break;
         }
         tc_fence_after();
         for (int t = 0; t < 2 && ok; ++t) {
           const int nt = t == 0 ? n0 : n_kv;
           // O_t += P_t(j-1) V_{j-1}
           if (j >= 1 && j - 1 < nt) {
-            if (!mbar_wait(&p_full[t], p_phase[t], err, abort_flag)) { ok = false; break; }
+            if (!mbar_wait_warp(&p_full[t], p_phase[t], err, abort_flag)) { ok = false; break; }
             p_phase[t] ^= 1;
             tc_fence_after();
             const uint32_t o_tmem = tmem + Cfg::O_COL + t * D;
@@ -172,10 +172,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               const uint64_t bd = sdesc_sw128(v_addr + k * 2048, Cfg::BLOCK_BYTES, 1024);
-              mma_ts(o_tmem, p_tmem + k * 8, bd, IDESC_O, (j - 1 > 0 || k > 0) ? 1u : 0u);
+              mma_ts_w(o_tmem, p_tmem + k * 8, bd, IDESC_O, (j - 1 > 0 || k > 0) ? 1u : 0u);
             }
-            if (t == 1) mma_commit(&slot_empty[vslot]);
-            if (j - 1 == nt - 1) mma_commit(&o_done[t]);
+            if (t == 1) mma_commit_w(&slot_empty[vslot]);
+            if (j - 1 == nt - 1) mma_commit_w(&o_done[t]);
           }
           // S_t = Q_t K_j^T
           if (j < nt) {
@@ -186,10 +186,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t off = (k / 4) * Cfg::BLOCK_BYTES + (k % 4) * 32;
               const uint64_t ad = sdesc_sw128(qa + off, 16, 1024);
               const uint64_t bd = sdesc_sw128(k_addr + off, 16, 1024);
-              mma_ss(s_tmem, ad, bd, IDESC_S, k > 0 ? 1u : 0u);
+              mma_ss_w(s_tmem, ad, bd, IDESC_S, k > 0 ? 1u : 0u);
             }
-            mma_commit(&s_full[t]);
-            if (t == 1) mma_commit(&slot_empty[kidx % kSlots]);
+            mma_commit_w(&s_full[t]);
+            if (t == 1) mma_commit_w(&slot_empty[kidx % kSlots]);
           }
         }
       }

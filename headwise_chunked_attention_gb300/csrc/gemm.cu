@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issue
-    if (lane == 0) {
+    {  // whole warp; one elected lane issues
       constexpr uint32_t IDESC = idesc_bf16(BM, BN, A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
@@ -238,11 +238,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const TileCoord tc = tile_coord(t, num_m, num_n, kb_total, ksplit);
         const int acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
-        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, err, abort_flag)) break;
+        if (!mbar_wait_warp(&acc_empty[acc], acc_phase ^ 1, err, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb = tc.kb0; kb < tc.kb1; ++kb) {
-          if (!mbar_wait(&full[stage], phase, err, abort_flag)) { ok = false; break; }
+          if (!mbar_wait_warp(&full[stage], phase, err, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * Cfg::STAGE_BYTES);
           const uint32_t sb = sa + A_STAGE_BYTES;
@@ -253,14 +253,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             else ad = sdesc_sw128(sa + k * 2048, 8192, 1024);
             if (!B_MN) bd = sdesc_sw128(sb + k * 32, 16, 1024);
             else bd = sdesc_sw128(sb + k * 2048, 8192, 1024);
-            mma_ss(d_tmem, ad, bd, IDESC, (kb > tc.kb0 || k > 0) ? 1u : 0u);
+            mma_ss_w(d_tmem, ad, bd, IDESC, (kb > tc.kb0 || k > 0) ? 1u : 0u);
           }
-          mma_commit(&empty[stage]);
+          mma_commit_w(&empty[stage]);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         // an empty K range (split-K remainder) commits without MMAs; the
         // epilogue skips such tiles by the same test
-        mma_commit(&acc_full[acc]);
+        mma_commit_w(&acc_full[acc]);
       }
     }
   } else {
