@@ -18,11 +18,11 @@
 //   warps 0-3  warpgroup of slot 0 (even sub-tiles), warps 4-7 of slot 1 (odd):
 //              softmax gradient with one key row (TMEM lane) per thread (P^T,
 //              dS^T from S^T, dP^T), then the dQ^T read-out with one d index
-//              per thread, staged in shared memory as [32 queries x 32 d] fp32
+//              per thread, staged in shared memory as [16 queries x 32 d] fp32
 //              blocks and added into global dQ by TMA reduce-add (the
 //              reduction runs in L2); at the end dV (slot 0) / dK (slot 1)
 //   warp 8     TMEM owner and tcgen05.mma issuer
-//   warp 9     TMA producer: K, V once, then Q_u, dO_u through 2 stages
+//   warp 9     TMA producer: K, V once, then Q_u, dO_u through 3 stages
 // TMEM (512 columns), slot s in {0, 1} at column 128 s:
 //   [+0, +64)   S^T_u = K Q_u^T (fp32); then P^T_u (bf16, +0..31) and
 //               dS^T_u (bf16, +32..63), A operands of the dV / dK MMAs
@@ -46,7 +46,8 @@ namespace {
 constexpr int kThreads = 320;
 constexpr int BK = 128;  // keys per CTA
 constexpr int BQ = 64;   // queries per sub-tile
-constexpr int NST = 2;   // Q/dO stages
+constexpr int NST = 3;   // Q/dO stages
+constexpr int DQR = 16;  // query rows per dQ staging round
 
 template <int D>
 struct BwdCfg {
@@ -60,8 +61,8 @@ struct BwdCfg {
   static constexpr uint32_t ST_BYTES = 2 * Q_TILE;
   static constexpr uint32_t DS_OFF = ST_OFF + NST * ST_BYTES;   // 2 x [128 keys][64 q] bf16
   static constexpr uint32_t DS_BYTES = BK * BQ * 2;
-  static constexpr uint32_t DQS_OFF = DS_OFF + 2 * DS_BYTES;    // 8 warps x [32 q][32 d] fp32
-  static constexpr uint32_t DQS_BYTES = 32 * 32 * 4;
+  static constexpr uint32_t DQS_OFF = DS_OFF + 2 * DS_BYTES;    // 8 warps x [16 q][32 d] fp32
+  static constexpr uint32_t DQS_BYTES = DQR * 32 * 4;
   static constexpr uint32_t LD_OFF = DQS_OFF + 8 * DQS_BYTES;   // 8 warps x (64 lse + 64 D)
   static constexpr uint32_t BAR_OFF = LD_OFF + 8 * 2 * BQ * 4;
   static constexpr uint32_t SMEM_BYTES = BAR_OFF + 256 + 1024;
@@ -270,18 +271,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
       const float4* dd4 = reinterpret_cast<const float4*>(ld_w + BQ);
       const int mask_from = r - u * BQ;  // columns c < mask_from hold key > query: masked
       float p[BQ];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t rr[32];
-        tmem_ld32(slot + 32 * h, rr);
+      {
+        uint32_t rr[64];
+        tmem_ld64(slot, rr);
         tmem_ld_wait(rr);
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 l4 = lse4[(32 * h + i) / 4];
-          p[32 * h + i] = ex2(fmaf(__uint_as_float(rr[i]), sl2, -l4.x));
-          p[32 * h + i + 1] = ex2(fmaf(__uint_as_float(rr[i + 1]), sl2, -l4.y));
-          p[32 * h + i + 2] = ex2(fmaf(__uint_as_float(rr[i + 2]), sl2, -l4.z));
-          p[32 * h + i + 3] = ex2(fmaf(__uint_as_float(rr[i + 3]), sl2, -l4.w));
+        for (int i = 0; i < BQ; i += 4) {
+          const float4 l4 = lse4[i / 4];
+          p[i] = ex2(fmaf(__uint_as_float(rr[i]), sl2, -l4.x));
+          p[i + 1] = ex2(fmaf(__uint_as_float(rr[i + 1]), sl2, -l4.y));
+          p[i + 2] = ex2(fmaf(__uint_as_float(rr[i + 2]), sl2, -l4.z));
+          p[i + 3] = ex2(fmaf(__uint_as_float(rr[i + 3]), sl2, -l4.w));
         }
       }
       if (mask_from > 0) {  // only the two sub-tiles on the diagonal
@@ -297,19 +297,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
       }
       {
         uint32_t pk[32];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t rr[32];
-          tmem_ld32(slot + 64 + 32 * h, rr);
+        {
+          uint32_t rr[64];
+          tmem_ld64(slot + 64, rr);
           tmem_ld_wait(rr);
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const float4 d4 = dd4[(32 * h + i) / 4];
-            const int c = 32 * h + i;
-            const float g0 = p[c] * (__uint_as_float(rr[i]) - d4.x);
-            const float g1 = p[c + 1] * (__uint_as_float(rr[i + 1]) - d4.y);
-            const float g2 = p[c + 2] * (__uint_as_float(rr[i + 2]) - d4.z);
-            const float g3 = p[c + 3] * (__uint_as_float(rr[i + 3]) - d4.w);
+          for (int c = 0; c < BQ; c += 4) {
+            const float4 d4 = dd4[c / 4];
+            const float g0 = p[c] * (__uint_as_float(rr[c]) - d4.x);
+            const float g1 = p[c + 1] * (__uint_as_float(rr[c + 1]) - d4.y);
+            const float g2 = p[c + 2] * (__uint_as_float(rr[c + 2]) - d4.z);
+            const float g3 = p[c + 3] * (__uint_as_float(rr[c + 3]) - d4.w);
             pk[c / 2] = pack_bf16(g0, g1);
             pk[c / 2 + 1] = pack_bf16(g2, g3);
           }
@@ -342,17 +340,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
         const int q0 = k0 + u * BQ;
         const uint32_t cb = (uint32_t)(lane >> 2), cw = (uint32_t)(lane & 3) * 4;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        for (int rd = 0; rd < BQ / DQR; ++rd) {
           if (lane == 0) bulk_wait_read<0>();   // the previous reduce has read the block
           __syncwarp();
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
+          for (int c = 0; c < DQR; ++c) {
+            const int q = rd * DQR + c;   // compile-time after unrolling
             *reinterpret_cast<float*>(stage_w + c * 128 + ((cb ^ (c & 7)) << 4) + cw) =
-                __uint_as_float(half ? hi[c] : lo[c]) * a.scale;
+                __uint_as_float(q < 32 ? lo[q & 31] : hi[q & 31]) * a.scale;
+          }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_reduce_add_2d(&dqmap, stage_w, head * D + 32 * qw, q0 + 32 * half);
+            tma_reduce_add_2d(&dqmap, stage_w, head * D + 32 * qw, q0 + rd * DQR);
             bulk_commit();
           }
         }
@@ -413,7 +413,7 @@ static cudaError_t launch_bwd_t(const AttnBwdArgs& a, int* err, cudaStream_t str
     attr_set = true;
   }
   CUtensorMap qm, km, vm, dm, dqm;
-  if (!make_tmap_f32(&dqm, a.dQ, a.S, (uint64_t)a.ld_dq, a.ld_dq, 32, 32) ||
+  if (!make_tmap_f32(&dqm, a.dQ, a.S, (uint64_t)a.ld_dq, a.ld_dq, DQR, 32) ||
       !make_tmap_bf16(&qm, a.Q, a.S, (uint64_t)a.heads * D, a.ldq, BQ, 64) ||
       !make_tmap_bf16(&km, a.K, a.S, (uint64_t)a.ldkv, a.ldkv, BK, 64) ||
       !make_tmap_bf16(&vm, a.V, a.S, (uint64_t)a.ldkv, a.ldkv, BK, 64) ||
