@@ -61,11 +61,14 @@ struct BwdCfg {
   static constexpr uint32_t ST_BYTES = 2 * Q_TILE;
   static constexpr uint32_t DS_OFF = ST_OFF + NST * ST_BYTES;   // 2 x [128 keys][64 q] bf16
   static constexpr uint32_t DS_BYTES = BK * BQ * 2;
-  static constexpr uint32_t DQS_OFF = DS_OFF + 2 * DS_BYTES;    // 8 warps x [16 q][32 d] fp32
+  // 8 warps x 2 buffers x [16 q][32 d] fp32
+  static constexpr uint32_t DQS_OFF = DS_OFF + 2 * DS_BYTES;
   static constexpr uint32_t DQS_BYTES = DQR * 32 * 4;
-  static constexpr uint32_t LD_OFF = DQS_OFF + 8 * DQS_BYTES;   // 8 warps x (64 lse + 64 D)
-  static constexpr uint32_t BAR_OFF = LD_OFF + 8 * 2 * BQ * 4;
-  static constexpr uint32_t SMEM_BYTES = BAR_OFF + 256 + 1024;
+  // 2 warpgroups x 2 parities x (64 lse + 64 D)
+  static constexpr uint32_t LD_OFF = DQS_OFF + 8 * 2 * DQS_BYTES;
+  static constexpr uint32_t BAR_OFF = LD_OFF + 2 * 2 * 2 * BQ * 4;
+  // the dynamic shared memory base is 1024-byte aligned (checked at entry)
+  static constexpr uint32_t SMEM_BYTES = BAR_OFF + 256;
 };
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -81,8 +84,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
     const __grid_constant__ CUtensorMap dqmap, const AttnBwdArgs a, int* __restrict__ err) {
   using Cfg = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  uint8_t* smem = smem_raw;
+  if (smem_u32(smem) & 1023u) {  // swizzled tiles need 1024-byte alignment: refuse, no access
+    if (threadIdx.x == 0) atomicCAS(err, 0, kErrDeviceTimeout);
+    return;
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::BAR_OFF);
   uint64_t* kv_full = bars + 0;
   uint64_t* q_full = bars + 1;            // [NST]
@@ -239,8 +245,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
     const float sl2 = a.scale * 1.4426950408889634f;
     const float* lse_g = a.lse + (long long)head * a.lse_stride;
     const float* D_g = a.D + (long long)head * S;
-    float* ld_w = reinterpret_cast<float*>(smem + Cfg::LD_OFF) + warp * 2 * BQ;  // this warp's
-    uint8_t* stage_w = smem + Cfg::DQS_OFF + warp * Cfg::DQS_BYTES;              // this warp's
+    // lse/D of the current sub-tile, shared by the warpgroup and double-buffered
+    // by sub-tile parity (every warp writes the same values before reading)
+    float* ld_wg = reinterpret_cast<float*>(smem + Cfg::LD_OFF) + wg * 2 * (2 * BQ);
+    uint8_t* stage_w = smem + Cfg::DQS_OFF + warp * 2 * Cfg::DQS_BYTES;  // this warp's 2 buffers
+    uint32_t round = 0;  // dQ staging rounds issued by this warp
     uint8_t* ds_rows = smem + Cfg::DS_OFF + wg * Cfg::DS_BYTES + r * 128;
     // lse (log2 units) and D of the queries of a sub-tile, loaded one sub-tile
     // of this slot ahead: lane l holds queries l and l + 32
@@ -257,6 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
     bool ok = true;
     for (int u = wg; u < n_u; u += 2) {
       const uint32_t ph = (u >> 1) & 1;
+      float* ld_w = ld_wg + ph * (2 * BQ);
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
         ld_w[32 * m + lane] = nl[m];
@@ -340,19 +350,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
         const int q0 = k0 + u * BQ;
         const uint32_t cb = (uint32_t)(lane >> 2), cw = (uint32_t)(lane & 3) * 4;
 #pragma unroll
-        for (int rd = 0; rd < BQ / DQR; ++rd) {
-          if (lane == 0) bulk_wait_read<0>();   // the previous reduce has read the block
+        for (int rd = 0; rd < BQ / DQR; ++rd, ++round) {
+          uint8_t* buf = stage_w + (round & 1) * Cfg::DQS_BYTES;
+          if (lane == 0) bulk_wait_read<1>();   // the reduce two rounds back has read buf
           __syncwarp();
 #pragma unroll
           for (int c = 0; c < DQR; ++c) {
             const int q = rd * DQR + c;   // compile-time after unrolling
-            *reinterpret_cast<float*>(stage_w + c * 128 + ((cb ^ (c & 7)) << 4) + cw) =
+            *reinterpret_cast<float*>(buf + c * 128 + ((cb ^ (c & 7)) << 4) + cw) =
                 __uint_as_float(q < 32 ? lo[q & 31] : hi[q & 31]) * a.scale;
           }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_reduce_add_2d(&dqmap, stage_w, head * D + 32 * qw, q0 + rd * DQR);
+            tma_reduce_add_2d(&dqmap, buf, head * D + 32 * qw, q0 + rd * DQR);
             bulk_commit();
           }
         }
