@@ -15,14 +15,19 @@
 // alternate between sub-tiles, each with its own warpgroup, so that the
 // softmax-gradient work of one slot overlaps the tensor core's work on the
 // other slot and the two warpgroups overlap each other.
-//   warps 0-3  warpgroup of slot 0 (even sub-tiles), warps 4-7 of slot 1 (odd):
-//              softmax gradient with one key row (TMEM lane) per thread (P^T,
-//              dS^T from S^T, dP^T), then the dQ^T read-out with one d index
-//              per thread, staged in shared memory as [16 queries x 32 d] fp32
-//              blocks and added into global dQ by TMA reduce-add (the
-//              reduction runs in L2); at the end dV (slot 0) / dK (slot 1)
-//   warp 8     TMEM owner and tcgen05.mma issuer
-//   warp 9     TMA producer: K, V once, then Q_u, dO_u through 3 stages
+//   warps 0-3    warpgroup of slot 0 (even sub-tiles), warps 4-7 of slot 1 (odd):
+//                softmax gradient with one key row (TMEM lane) per thread
+//                (P^T, dS^T from S^T, dP^T)
+//   warps 8-11   epilogue warpgroup: dQ^T read-out of every sub-tile with one
+//                d index per thread, staged in shared memory as [16 queries x
+//                32 d] fp32 blocks and added into global dQ by TMA reduce-add
+//                (the reduction runs in L2); at the end dK and dV
+//   warp 12      TMEM owner and tcgen05.mma issuer
+//   warp 13      TMA producer: K, V once, then Q_u, dO_u through 3 stages
+//   warps 14-15  idle (they complete warpgroup 3 for register reallocation)
+// Registers are moved with setmaxnreg from warpgroups 2 and 3 to the two
+// softmax warpgroups: 168 + 168 + 104 + 40 per thread, x 128 threads each =
+// 61440 of the 65536 the block is launched with (512 threads x 128).
 // TMEM (512 columns), slot s in {0, 1} at column 128 s:
 //   [+0, +64)   S^T_u = K Q_u^T (fp32); then P^T_u (bf16, +0..31) and
 //               dS^T_u (bf16, +32..63), A operands of the dV / dK MMAs
@@ -43,7 +48,9 @@ namespace upipe {
 
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 512;
+constexpr int kWarpMma = 12;
+constexpr int kWarpTma = 13;
 constexpr int BK = 128;  // keys per CTA
 constexpr int BQ = 64;   // queries per sub-tile
 constexpr int NST = 3;   // Q/dO stages
@@ -61,11 +68,12 @@ struct BwdCfg {
   static constexpr uint32_t ST_BYTES = 2 * Q_TILE;
   static constexpr uint32_t DS_OFF = ST_OFF + NST * ST_BYTES;   // 2 x [128 keys][64 q] bf16
   static constexpr uint32_t DS_BYTES = BK * BQ * 2;
-  // 8 warps x 2 buffers x [16 q][32 d] fp32
+  // 4 epilogue warps x 4 buffers x [16 q][32 d] fp32
   static constexpr uint32_t DQS_OFF = DS_OFF + 2 * DS_BYTES;
   static constexpr uint32_t DQS_BYTES = DQR * 32 * 4;
+  static constexpr int NDQS = 4;
   // 2 warpgroups x 2 parities x (64 lse + 64 D)
-  static constexpr uint32_t LD_OFF = DQS_OFF + 8 * 2 * DQS_BYTES;
+  static constexpr uint32_t LD_OFF = DQS_OFF + 4 * NDQS * DQS_BYTES;
   static constexpr uint32_t BAR_OFF = LD_OFF + 2 * 2 * 2 * BQ * 4;
   // the dynamic shared memory base is 1024-byte aligned (checked at entry)
   static constexpr uint32_t SMEM_BYTES = BAR_OFF + 256;
@@ -121,20 +129,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
       mbar_init(&s_full[s], 1);
       mbar_init(&p_ready[s], 4);
       mbar_init(&dq_full[s], 1);
-      mbar_init(&dq_free[s], 4);   // the 4 warps of slot s's warpgroup
+      mbar_init(&dq_free[s], 4);   // the 4 epilogue warps
     }
     mbar_init(mma_done, 1);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9 && lane == 0) {
+  if (warp == kWarpTma && lane == 0) {
     prefetch_tmap(&qmap);
     prefetch_tmap(&kmap);
     prefetch_tmap(&vmap);
     prefetch_tmap(&domap);
   }
-  if (warp == 8) {
+  if (warp == kWarpMma) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -143,7 +151,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 9) {
+  const int wgroup = warp >> 2;
+  if (wgroup == 3) {
+  setmaxnreg_dec<40>();
+  if (warp == kWarpTma) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t issued = 0, issued_phase = 0;
@@ -173,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
           if (issued & (1u << s)) mbar_wait_drain(&q_full[s], (issued_phase >> s) & 1u);
       }
     }
-  } else if (warp == 8) {
+  } else if (warp == kWarpMma) {
     // ---------------------------------------------------------- MMA issue
     {  // whole warp; one elected lane issues
       constexpr uint32_t ID_S = idesc_bf16(128, BQ, false, false);   // S^T, dP^T
@@ -235,9 +246,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
       }
       mma_commit_w(mma_done);
     }
-  } else {
-    // --------------------- slot warpgroups: softmax gradient, dQ, dK / dV
-    const int wg = warp >> 2;        // slot served by this warpgroup
+  }
+  } else if (wgroup < 2) {
+    // ------------------------------- slot warpgroups: softmax gradient
+    setmaxnreg_inc<168>();
+    const int wg = wgroup;           // slot served by this warpgroup
     const int qw = warp & 3;
     const int r = qw * 32 + lane;    // TMEM lane: key row of S^T/dP^T, d index of dQ^T
     const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
@@ -248,8 +261,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
     // lse/D of the current sub-tile, shared by the warpgroup and double-buffered
     // by sub-tile parity (every warp writes the same values before reading)
     float* ld_wg = reinterpret_cast<float*>(smem + Cfg::LD_OFF) + wg * 2 * (2 * BQ);
-    uint8_t* stage_w = smem + Cfg::DQS_OFF + warp * 2 * Cfg::DQS_BYTES;  // this warp's 2 buffers
-    uint32_t round = 0;  // dQ staging rounds issued by this warp
     uint8_t* ds_rows = smem + Cfg::DS_OFF + wg * Cfg::DS_BYTES + r * 128;
     // lse (log2 units) and D of the queries of a sub-tile, loaded one sub-tile
     // of this slot ahead: lane l holds queries l and l + 32
@@ -257,9 +268,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
     auto fetch = [&](int u) {
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
-        const int q = k0 + u * BQ + 32 * m + lane;
-        nl[m] = q < S ? lse_g[q] * 1.4426950408889634f : INFINITY;
-        nd[m] = q < S ? D_g[q] : 0.f;
+        const int q = min(k0 + u * BQ + 32 * m + lane, S - 1);  // clamp: masked below
+        nl[m] = ld_nc_f32(lse_g + q);
+        nd[m] = ld_nc_f32(D_g + q);
       }
     };
     if (wg < n_u) fetch(wg);
@@ -269,8 +280,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
       float* ld_w = ld_wg + ph * (2 * BQ);
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
-        ld_w[32 * m + lane] = nl[m];
-        ld_w[BQ + 32 * m + lane] = nd[m];
+        const bool live = k0 + u * BQ + 32 * m + lane < S;  // queries past S: P = 0
+        ld_w[32 * m + lane] = live ? nl[m] * 1.4426950408889634f : INFINITY;
+        ld_w[BQ + 32 * m + lane] = live ? nd[m] : 0.f;
       }
       __syncwarp();
       if (u + 2 < n_u) fetch(u + 2);
@@ -280,53 +292,64 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
       const float4* lse4 = reinterpret_cast<const float4*>(ld_w);
       const float4* dd4 = reinterpret_cast<const float4*>(ld_w + BQ);
       const int mask_from = r - u * BQ;  // columns c < mask_from hold key > query: masked
-      float p[BQ];
-      {
-        uint32_t rr[64];
-        tmem_ld64(slot, rr);
-        tmem_ld_wait(rr);
+      uint8_t* row = ds_rows;
+      // two halves of 32 queries: P^T, then dS^T = P^T (dP^T - D).  dS^T goes
+      // over the second half of S^T, so the first half's dS^T is stored to
+      // TMEM only after the second half of S^T has been read.
+      uint32_t ds0[16];
 #pragma unroll
-        for (int i = 0; i < BQ; i += 4) {
-          const float4 l4 = lse4[i / 4];
-          p[i] = ex2(fmaf(__uint_as_float(rr[i]), sl2, -l4.x));
-          p[i + 1] = ex2(fmaf(__uint_as_float(rr[i + 1]), sl2, -l4.y));
-          p[i + 2] = ex2(fmaf(__uint_as_float(rr[i + 2]), sl2, -l4.z));
-          p[i + 3] = ex2(fmaf(__uint_as_float(rr[i + 3]), sl2, -l4.w));
-        }
-      }
-      if (mask_from > 0) {  // only the two sub-tiles on the diagonal
-#pragma unroll
-        for (int c = 0; c < BQ; ++c)
-          if (c < mask_from) p[c] = 0.f;
-      }
-      {
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) pk[i] = pack_bf16(p[2 * i], p[2 * i + 1]);
-        tmem_st32(slot, pk);
-      }
-      {
-        uint32_t pk[32];
+      for (int h = 0; h < 2; ++h) {
+        float p[32];
         {
-          uint32_t rr[64];
-          tmem_ld64(slot + 64, rr);
+          uint32_t rr[32];
+          tmem_ld32(slot + 32 * h, rr);
           tmem_ld_wait(rr);
 #pragma unroll
-          for (int c = 0; c < BQ; c += 4) {
-            const float4 d4 = dd4[c / 4];
-            const float g0 = p[c] * (__uint_as_float(rr[c]) - d4.x);
-            const float g1 = p[c + 1] * (__uint_as_float(rr[c + 1]) - d4.y);
-            const float g2 = p[c + 2] * (__uint_as_float(rr[c + 2]) - d4.z);
-            const float g3 = p[c + 3] * (__uint_as_float(rr[c + 3]) - d4.w);
-            pk[c / 2] = pack_bf16(g0, g1);
-            pk[c / 2 + 1] = pack_bf16(g2, g3);
+          for (int i = 0; i < 32; i += 4) {
+            const float4 l4 = lse4[(32 * h + i) / 4];
+            p[i] = ex2(fmaf(__uint_as_float(rr[i]), sl2, -l4.x));
+            p[i + 1] = ex2(fmaf(__uint_as_float(rr[i + 1]), sl2, -l4.y));
+            p[i + 2] = ex2(fmaf(__uint_as_float(rr[i + 2]), sl2, -l4.z));
+            p[i + 3] = ex2(fmaf(__uint_as_float(rr[i + 3]), sl2, -l4.w));
           }
         }
-        tmem_st32(slot + 32, pk);
+        if (h == 1) tmem_st16(slot + 32, ds0);  // S^T fully read now
+        if (mask_from > 32 * h) {  // only the two sub-tiles on the diagonal
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          *reinterpret_cast<uint4*>(ds_rows + ((ch ^ (r & 7)) << 4)) =
-              make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+          for (int i = 0; i < 32; ++i)
+            if (32 * h + i < mask_from) p[i] = 0.f;
+        }
+        {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(p[2 * i], p[2 * i + 1]);
+          tmem_st16(slot + 16 * h, pk);
+        }
+        {
+          uint32_t rr[32], pk[16];
+          tmem_ld32(slot + 64 + 32 * h, rr);
+          tmem_ld_wait(rr);
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 d4 = dd4[(32 * h + i) / 4];
+            pk[i / 2] = pack_bf16(p[i] * (__uint_as_float(rr[i]) - d4.x),
+                                  p[i + 1] * (__uint_as_float(rr[i + 1]) - d4.y));
+            pk[i / 2 + 1] = pack_bf16(p[i + 2] * (__uint_as_float(rr[i + 2]) - d4.z),
+                                      p[i + 3] * (__uint_as_float(rr[i + 3]) - d4.w));
+          }
+          if (h == 0) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ds0[i] = pk[i];
+          } else {
+            tmem_st16(slot + 48, pk);
+          }
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            const int c = 4 * h + ch;  // 16-byte chunk of the 128-byte row
+            *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) =
+                make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+          }
+        }
       }
       tmem_st_wait();
       fence_proxy_async_smem();
@@ -334,25 +357,36 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_ready[wg]);
 
-      // dQ^T of this sub-tile: read out, free the slot, reduce into global dQ
-      ok = __all_sync(0xffffffffu, mbar_wait(&dq_full[wg], ph, err, abort_flag));
+    }
+  } else {
+    // ------------------------------------------ epilogue: dQ, then dK / dV
+    setmaxnreg_dec<104>();
+    const int qw = warp & 3;
+    const int t = qw * 32 + lane;    // TMEM lane: d index of dQ^T, key row of dK/dV
+    const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
+    uint8_t* stage_w = smem + Cfg::DQS_OFF + qw * Cfg::NDQS * Cfg::DQS_BYTES;
+    uint32_t round = 0;  // dQ staging rounds issued by this warp
+    bool ok = true;
+    for (int u = 0; u < n_u; ++u) {
+      const int s = u & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&dq_full[s], (u >> 1) & 1, err, abort_flag));
       if (!ok) break;
       tc_fence_after();
       uint32_t lo[32], hi[32];
-      tmem_ld32(slot + 64, lo);
+      tmem_ld32(tmem + lane_off + 128 * s + 64, lo);
       tmem_ld_wait(lo);
-      tmem_ld32(slot + 96, hi);
+      tmem_ld32(tmem + lane_off + 128 * s + 96, hi);
       tmem_ld_wait(hi);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&dq_free[wg]);
+      if (lane == 0) mbar_arrive(&dq_free[s]);
       if (qw * 32 < D) {
         const int q0 = k0 + u * BQ;
         const uint32_t cb = (uint32_t)(lane >> 2), cw = (uint32_t)(lane & 3) * 4;
 #pragma unroll
         for (int rd = 0; rd < BQ / DQR; ++rd, ++round) {
-          uint8_t* buf = stage_w + (round & 1) * Cfg::DQS_BYTES;
-          if (lane == 0) bulk_wait_read<1>();   // the reduce two rounds back has read buf
+          uint8_t* buf = stage_w + (round % Cfg::NDQS) * Cfg::DQS_BYTES;
+          if (lane == 0) bulk_wait_read<Cfg::NDQS - 1>();   // buf's previous reduce has read it
           __syncwarp();
 #pragma unroll
           for (int c = 0; c < DQR; ++c) {
@@ -371,26 +405,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
     }
     if (lane == 0) bulk_wait_all();
     __syncwarp();
-    // dV (slot-0 warpgroup) and dK (slot-1 warpgroup) of this CTA's keys
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(mma_done, 0, err, abort_flag));
     if (ok) {
       tc_fence_after();
-      const int key = k0 + r;
-      float* dst = wg == 0 ? a.dV : a.dK;
-      const float mul = wg == 0 ? 1.f : a.scale;
-      const uint32_t col = wg == 0 ? 256u : 384u;
+      const int key = k0 + t;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
-        uint32_t rv[32];
-        tmem_ld32(tmem + lane_off + col + 32 * c, rv);
+        uint32_t rv[32], rk[32];
+        tmem_ld32(tmem + lane_off + 256 + 32 * c, rv);
         tmem_ld_wait(rv);
+        tmem_ld32(tmem + lane_off + 384 + 32 * c, rk);
+        tmem_ld_wait(rk);
         if (key < S) {
           const long long off = (long long)key * a.ld_dkv + kvh * D + 32 * c;
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            red_add_v4_f32(dst + off + i, __uint_as_float(rv[i]) * mul,
-                           __uint_as_float(rv[i + 1]) * mul, __uint_as_float(rv[i + 2]) * mul,
-                           __uint_as_float(rv[i + 3]) * mul);
+          for (int i = 0; i < 32; i += 4) {
+            red_add_v4_f32(a.dV + off + i, __uint_as_float(rv[i]), __uint_as_float(rv[i + 1]),
+                           __uint_as_float(rv[i + 2]), __uint_as_float(rv[i + 3]));
+            red_add_v4_f32(a.dK + off + i, __uint_as_float(rk[i]) * a.scale,
+                           __uint_as_float(rk[i + 1]) * a.scale,
+                           __uint_as_float(rk[i + 2]) * a.scale,
+                           __uint_as_float(rk[i + 3]) * a.scale);
+          }
         }
       }
     }
@@ -399,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
   // --------------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == kWarpMma) {
     if (*abort_flag) {
       if (lane == 0) {
         mma_commit(drain_bar);
