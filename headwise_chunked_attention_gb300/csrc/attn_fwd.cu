@@ -23,6 +23,12 @@
 // skips the O read-modify-write.  The diagonal KV tile of each query tile is
 // the only one masked; KV tiles beyond it are never loaded (causal skipping).
 // Grid: heaviest query blocks first, all heads of a block together.
+// Long rows: the tensor core's fp32 accumulation of O drifts over hundreds of
+// thousands of MMA steps (measured: the error grows linearly with position
+// past ~1M keys), so every kFlushTiles KV tiles each softmax thread folds its
+// O row out of TMEM into an fp32 row in global memory (IEEE adds, rescaled to
+// the current row max) and the next PV MMA restarts the TMEM accumulator.  The
+// rows live in a per-SM slot (one CTA per SM), so the scratch is bounded.
 #include <algorithm>
 
 #include "internal.h"
@@ -34,6 +40,12 @@ namespace {
 
 constexpr int kThreads = 320;
 constexpr int kSlots = 4;
+
+__device__ __forceinline__ uint32_t sm_id() {
+  uint32_t v;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(v));
+  return v;
+}
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
@@ -79,6 +91,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kvh = (a.h0 + head) / a.group - a.kv0;
   const int q0 = qb * 256;
   const int n_kv = 2 * qb + 2;  // KV tiles of query tile 1; tile 0 has n_kv - 1
+  const uint32_t smid = sm_id();
+  const bool flushing = a.flush != nullptr && smid < (uint32_t)kFlushSlots;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -172,7 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               const uint64_t bd = sdesc_sw128(v_addr + k * 2048, Cfg::BLOCK_BYTES, 1024);
-              mma_ts_w(o_tmem, p_tmem + k * 8, bd, IDESC_O, (j - 1 > 0 || k > 0) ? 1u : 0u);
+              const bool fresh = (j - 1 == 0) || (flushing && (j - 1) % kFlushTiles == 0);
+              mma_ts_w(o_tmem, p_tmem + k * 8, bd, IDESC_O, (!fresh || k > 0) ? 1u : 0u);
             }
             if (t == 1) mma_commit_w(&slot_empty[vslot]);
             if (j - 1 == nt - 1) mma_commit_w(&o_done[t]);
@@ -207,6 +222,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = a.scale_log2;
     float m_run = -INFINITY;
     float l_run = 0.f;
+    bool have_acc = false;  // a folded part of O exists in acc_row
+    float m_acc = 0.f;      // row max the folded part is expressed in
+    float* acc_row = flushing ? a.flush + ((size_t)smid * 256 + 128 * t + r) * D : nullptr;
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
       // warp-uniform: the tcgen05.ld/st below are warp-collective
@@ -263,6 +281,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st32(s_tmem + 32 * h, pk);
       }
       l_run += sum;
+      if (flushing && j > 0 && j % kFlushTiles == 0) {
+        // O in TMEM holds PV(0 .. j-1) since the last fold, in units of m_run
+        const float keep = have_acc ? ex2(m_acc - m_run) : 0.f;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t rr[32];
+          tmem_ld32(o_tmem + 32 * c, rr);
+          tmem_ld_wait(rr);
+          float* ap = acc_row + 32 * c;
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            float4 v = make_float4(__uint_as_float(rr[i]), __uint_as_float(rr[i + 1]),
+                                   __uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3]));
+            if (have_acc) {
+              const float4 o = *reinterpret_cast<const float4*>(ap + i);
+              v.x = fmaf(o.x, keep, v.x); v.y = fmaf(o.y, keep, v.y);
+              v.z = fmaf(o.z, keep, v.z); v.w = fmaf(o.w, keep, v.w);
+            }
+            *reinterpret_cast<float4*>(ap + i) = v;
+          }
+        }
+        have_acc = true;
+        m_acc = m_run;
+      }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -274,12 +316,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv_l = 1.f / l_run;
       const bool live = qpos < a.S;
+      const float keep = have_acc ? ex2(m_acc - m_run) : 0.f;
       bf16* op = a.O + (long long)qpos * a.ldo + head * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t rr[32];
         tmem_ld32(o_tmem + 32 * c, rr);
         tmem_ld_wait(rr);
+        if (have_acc) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            rr[i] = __float_as_uint(fmaf(acc_row[32 * c + i], keep, __uint_as_float(rr[i])));
+        }
         if (live) {
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {

@@ -96,7 +96,14 @@ struct AttnFwdArgs {
   float* lse;       // [heads][S] natural-log LSE (nullptr: not written)
   long long lse_stride;
   float scale_log2; // log2(e) / sqrt(d)
+  float* flush;     // nullptr, or [kFlushSlots][256 rows][d] fp32 per-SM O accumulators
 };
+
+// The attention forward folds its TMEM O accumulator into an fp32 row in
+// global memory every kFlushTiles KV tiles (see attn_fwd.cu); the scratch has
+// one slot per SM id and is needed only when S > kFlushTiles * 128.
+constexpr int kFlushTiles = 512;
+constexpr int kFlushSlots = 256;
 
 cudaError_t launch_attn_fwd(const CUtensorMap& qmap, const CUtensorMap& kmap,
                             const CUtensorMap& vmap, const AttnFwdArgs& a, int d, int* err,

@@ -171,7 +171,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // ----------------------------------------------------------- workspace --
 
 struct Layout {
-  size_t rope_hi, rope_lo, q, k, v, o;            // forward
+  size_t rope_hi, rope_lo, q, k, v, o, flush;     // forward
   size_t dO, D, dq, dk, dv, dklo, dvlo, yq, rq, yk, rk;  // backward
   size_t total;
 };
@@ -191,6 +191,8 @@ Layout plan(const Geo& g, int mode) {
   L.k = take(S * kvc * d * 2);
   L.v = take(S * kvc * d * 2);
   L.o = take(S * ch * d * 2);
+  // per-SM fp32 rows into which long attention rows fold their O accumulator
+  L.flush = S > (size_t)kFlushTiles * 128 ? take((size_t)kFlushSlots * 256 * d * 4) : (size_t)-1;
   if (mode == 1) {
     L.dO = take(S * ch * d * 2);
     L.D = take(ch * S * 4);
@@ -276,7 +278,7 @@ int project_chunk(const Geo& g, const DeviceState* ds, cudaStream_t st, const CU
 
 int attention_chunk(const Geo& g, const DeviceState* ds, cudaStream_t st, const bf16* Q,
                     const bf16* K, const bf16* V, int h0, int kv0, bf16* O, int ldo,
-                    float* lse) {
+                    float* lse, float* flush) {
   const int d = g.d;
   CUtensorMap qm, km, vm;
   UPIPE_MAP(&qm, Q, g.S, (uint64_t)g.ch * d, (uint64_t)g.ch * d, 128, 64);
@@ -293,6 +295,7 @@ int attention_chunk(const Geo& g, const DeviceState* ds, cudaStream_t st, const 
   a.lse = lse;
   a.lse_stride = g.S;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
+  a.flush = flush;
   prof_begin(0, st);
   const cudaError_t e = launch_attn_fwd(qm, km, vm, a, d, ds->err, st);
   prof_end(0, st);
@@ -343,6 +346,7 @@ extern "C" int upipe_attn_fwd(const upipe_shape_t* shape, const upipe_bf16* x_,
   bf16* K = at<bf16>(workspace, L.k);
   bf16* V = at<bf16>(workspace, L.v);
   bf16* Ows = at<bf16>(workspace, L.o);
+  float* flush = L.flush == (size_t)-1 ? nullptr : at<float>(workspace, L.flush);
   UPIPE_CUDA(launch_rope_table(rhi, rlo, g.S, g.d, shape->rope_theta, st));
 
   CUtensorMap xmap;
@@ -357,7 +361,8 @@ extern "C" int upipe_attn_fwd(const upipe_shape_t* shape, const upipe_bf16* x_,
                             nullptr));
     bf16* O = dbg ? dbg + (size_t)h0 * g.d : Ows;
     const int ldo = dbg ? g.Hq * g.d : g.ch * g.d;
-    UPIPE_TRY(attention_chunk(g, ds, st, Q, K, V, h0, kv0, O, ldo, lse + (size_t)h0 * g.S));
+    UPIPE_TRY(attention_chunk(g, ds, st, Q, K, V, h0, kv0, O, ldo, lse + (size_t)h0 * g.S,
+                              flush));
     // out (+)= O_c Wo[:, h0*d : (h0+ch)*d]^T  (the chunk's partial result)
     CUtensorMap om, wom;
     UPIPE_MAP(&om, O, g.S, (uint64_t)g.ch * g.d, ldo, 128, 64);
@@ -413,6 +418,7 @@ extern "C" int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x_,
   bf16* K = at<bf16>(workspace, L.k);
   bf16* V = at<bf16>(workspace, L.v);
   bf16* Ows = at<bf16>(workspace, L.o);
+  float* flush = L.flush == (size_t)-1 ? nullptr : at<float>(workspace, L.flush);
   bf16* dO = at<bf16>(workspace, L.dO);
   float* Dv = at<float>(workspace, L.D);
   float* dQ = at<float>(workspace, L.dq);
@@ -485,7 +491,7 @@ extern "C" int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x_,
       UPIPE_CUDA(cudaMemsetAsync(dK, 0, sizeof(float) * S * g.kvc * d, st));
       UPIPE_CUDA(cudaMemsetAsync(dV, 0, sizeof(float) * S * g.kvc * d, st));
     }
-    UPIPE_TRY(attention_chunk(g, ds, st, Q, K, V, h0, kv0, Ows, g.ch * d, nullptr));
+    UPIPE_TRY(attention_chunk(g, ds, st, Q, K, V, h0, kv0, Ows, g.ch * d, nullptr, flush));
     // 2. dO_c = dout Wo_c, D = rowsum(dO * O); dWo_c = dout^T O_c
     {
       CUtensorMap wom;

@@ -297,6 +297,68 @@ def layer_backward(geom, x: np.ndarray, Wq, Wk, Wv, Wo, dout: np.ndarray,
             "dq_gamma": dgq, "dk_gamma": dgk}
 
 
+def layer_backward_tail(geom, x: ArrayOrRows, Wq, Wk, Wv, Wo, dout_tail: np.ndarray,
+                        n_tail: int, q_gamma=None, k_gamma=None,
+                        store_dtype: Optional[str] = None):
+    """dx for the last ``n_tail`` rows of the sequence, exactly (same chain
+    rule as ``layer_backward``), without the full-sequence cost.
+
+    Row t >= S - n_tail of dx collects dq_t (which needs P and dP of row t
+    against every key j <= t, i.e. the full K and V) and dk_t, dv_t (which
+    need only the queries i >= t, all inside the tail).  ``dout_tail`` holds
+    rows S - n_tail .. S - 1 of dout.  Returns dx_tail [n_tail, hidden].
+    """
+    S = _nrows(x, geom.S)
+    d, Hq, Hkv = geom.d, geom.Hq, geom.Hkv
+    g = Hq // Hkv
+    t0 = S - n_tail
+    rows = np.arange(t0, S)
+    Wq, Wk, Wv, Wo = (np.asarray(w, dtype=np.float64) for w in (Wq, Wk, Wv, Wo))
+    dout_tail = np.asarray(dout_tail, dtype=np.float64)
+    xt = _rows(x, t0, S)
+    cos_t, sin_t = rope_cos_sin(rows, d, geom.rope_theta)
+    scale = 1.0 / math.sqrt(d)
+    rnd = bf16_round if store_dtype == "bf16" else (lambda t: t)
+
+    def pre(a, gamma):
+        if geom.qk_norm:
+            y, r = rms_norm(a, gamma, geom.norm_eps)
+        else:
+            y, r = a, None
+        return rnd(apply_rope(y, cos_t, sin_t)), r
+
+    def post_grad(dqk, a, r, gamma):
+        dy = apply_rope_transpose(dqk, cos_t, sin_t)
+        if geom.qk_norm:
+            return rms_norm_backward(dy, a, r, gamma)[0]
+        return dy
+
+    dx = np.zeros((n_tail, Wq.shape[1]))
+    for kvh in range(Hkv):
+        sl = slice(kvh * d, (kvh + 1) * d)
+        K, V = project_kv(x, Wk, Wv, geom, kvh, S, k_gamma, store_dtype)
+        ak_t = xt @ Wk[sl].T
+        dk_t = np.zeros((n_tail, d))
+        dv_t = np.zeros((n_tail, d))
+        for h in range(kvh * g, (kvh + 1) * g):
+            hs = slice(h * d, (h + 1) * d)
+            aq_t = xt @ Wq[hs].T
+            q_t, rq = pre(aq_t, q_gamma)
+            o_t, _, p_t = causal_attention(q_t, K, V, rows, return_p=True)   # [n, S]
+            do_t = dout_tail @ Wo[:, hs]
+            dp_t = do_t @ V.T
+            D = np.sum(do_t * o_t, axis=1, keepdims=True)
+            ds_t = p_t * (dp_t - D)                                          # [n, S]
+            dq_t = ds_t @ K * scale
+            # keys in the tail receive only tail queries (causal)
+            dk_t += ds_t[:, t0:].T @ q_t * scale
+            dv_t += p_t[:, t0:].T @ do_t
+            dx += post_grad(dq_t, aq_t, rq, q_gamma) @ Wq[hs]
+        _, rk = pre(ak_t, k_gamma)
+        dx += post_grad(dk_t, ak_t, rk, k_gamma) @ Wk[sl] + dv_t @ Wv[sl]
+    return dx
+
+
 def layer_loss(geom, x, Wq, Wk, Wv, Wo, dout, q_gamma=None, k_gamma=None):
     """Scalar L = sum(out * dout); the function whose gradient
     ``layer_backward`` returns (used by the finite-difference pin)."""

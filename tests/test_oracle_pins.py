@@ -278,3 +278,21 @@ def test_backward_matches_finite_differences(qk_norm):
         an = grads[gname]
         err = np.max(np.abs(an - num)) / max(1e-12, np.max(np.abs(num)))
         assert err < 1e-6, (name, err)
+
+
+@pytest.mark.parametrize("qk_norm,store", [(False, None), (True, None), (True, "bf16")])
+def test_tail_backward_equals_full_backward_rows(qk_norm, store):
+    """The tail-rows dx used at million-token sizes equals the last rows of
+    the full chain-rule backward (itself pinned by finite differences)."""
+    rng = np.random.default_rng(18)
+    g = geom(hidden=24, Hq=4, Hkv=2, d=8, qk_norm=qk_norm)
+    S = 40
+    x, Wq, Wk, Wv, Wo = rand_layer(rng, g, S)
+    dout = rng.standard_normal((S, g.hidden))
+    qg = 1 + 0.2 * rng.standard_normal(8) if qk_norm else None
+    kg = 1 + 0.2 * rng.standard_normal(8) if qk_norm else None
+    full = O.layer_backward(g, x, Wq, Wk, Wv, Wo, dout, qg, kg, store_dtype=store)
+    for n in (1, 7, 40):
+        tail = O.layer_backward_tail(g, x, Wq, Wk, Wv, Wo, dout[S - n:], n, qg, kg,
+                                     store_dtype=store)
+        np.testing.assert_allclose(tail, full["dx"][S - n:], atol=1e-12)

@@ -98,22 +98,3 @@ def test_chunked_out_close_to_unchunked():
     for ch in (3, 6):
         out, _, _ = run_fwd(w, ch, inp, debug=False)
         assert_close(f64(out), f64(ref), f"out ch={ch} vs ch=24", 1e-3, 1e-4)
-
-
-@pytest.mark.slow
-@pytest.mark.parametrize("name,ch", [("llama3.2-3b-s65536", 3),
-                                     ("llama3.2-3b-s65536", 24)])
-def test_forward_sampled_rows_full_size(name, ch):
-    w = WORKLOADS[name]
-    inp = make_inputs(w, seed=0, device="cuda")
-    out, lse, o = run_fwd(w, ch, inp)
-    rows = sample_rows(w.S, 64)
-    xg = inp["x"]
-    src = lambda lo, hi: f64(xg[lo:hi])
-    small = {k: v for k, v in inp.items() if k != "x"}
-    a = {k: f64(v) for k, v in small.items()}
-    refb = O.layer_forward(w, src, a["Wq"], a["Wk"], a["Wv"], a["Wo"], rows=rows,
-                           store_dtype="bf16")
-    assert_close(f64(out[rows]), refb["out"], "out rows")
-    dl = np.abs(f64(lse[:, rows]) - refb["lse"]).max()
-    assert dl <= LSE_ABS, dl

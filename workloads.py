@@ -75,11 +75,29 @@ WORKLOADS = {
 WORKLOAD_ORDER = list(WORKLOADS)
 
 
+_BLOCK = 1 << 28  # elements drawn per call for large tensors
+
+
 def _randn(shape, std, gen, device):
-    t = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
-    if std != 1.0:
-        t.mul_(std)
-    return t.to(torch.bfloat16)
+    n = 1
+    for s in shape:
+        n *= s
+    if n <= _BLOCK:
+        t = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+        if std != 1.0:
+            t.mul_(std)
+        return t.to(torch.bfloat16)
+    # large tensors (million-token x): drawn in row blocks so that no full
+    # float32 copy exists; the values are a fixed function of the seed
+    out = torch.empty(shape, device=device, dtype=torch.bfloat16)
+    flat = out.view(-1)
+    for lo in range(0, n, _BLOCK):
+        hi = min(n, lo + _BLOCK)
+        t = torch.randn(hi - lo, generator=gen, device=device, dtype=torch.float32)
+        if std != 1.0:
+            t.mul_(std)
+        flat[lo:hi] = t.to(torch.bfloat16)
+    return out
 
 
 def make_inputs(w: Workload, seed: int = 0, device: str = "cpu",
