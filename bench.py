@@ -80,6 +80,25 @@ def peaks():
     return 1900.0, 1700.0, 6800.0, "fallback"
 
 
+# ------------------------------------------------------- replica helpers --
+
+def max_over_ranks(t: float, dist=None, device="cpu") -> float:
+    """The slowest rank's time: the job finishes when every replica has."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return t
+    import torch
+    tt = torch.tensor([t], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def replica_throughput(flops_per_rank_step: float, steps: int, world: int,
+                       t_max: float) -> float:
+    """Whole-job TFLOP/s of ``world`` independent replicas: all ranks' work
+    over the max-over-ranks time (weak scaling: per-rank work is fixed)."""
+    return world * flops_per_rank_step * steps / t_max / 1e12
+
+
 # ---------------------------------------------------------------- clocks --
 
 class Clocks:
@@ -287,12 +306,7 @@ def main():
             fn()
         e.record()
         barrier()
-        t = s.elapsed_time(e) / 1e3
-        if dist is not None:
-            tt = torch.tensor([t], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            t = float(tt.item())
-        return t
+        return max_over_ranks(s.elapsed_time(e) / 1e3, dist, dev)
 
     flops, attn_flops = layer_flops(w, args.pass_)
     nchunks = w.Hq // ch
@@ -312,7 +326,7 @@ def main():
         t = timed(step, args.steps)
     clocks = clk.summary()
     durs = kt.durations_ms()
-    value = world * flops * args.steps / t / 1e12
+    value = replica_throughput(flops, args.steps, world, t)
 
     # ---- end to end: pinned host x -> device, layer, out -> pinned host
     x_host = inp["x"].cpu().pin_memory()
@@ -326,7 +340,7 @@ def main():
     for _ in range(2):
         e2e_step()
     t_e2e = timed(e2e_step, max(1, args.steps // 2))
-    e2e_value = world * flops * max(1, args.steps // 2) / t_e2e / 1e12
+    e2e_value = replica_throughput(flops, max(1, args.steps // 2), world, t_e2e)
 
     # ---- roofline of the attention kernels (algorithmic FLOPs per launch over
     # the live CUDA-event launch time)

@@ -60,6 +60,8 @@ def lib():
         L.upipe_attn_bwd.argtypes = ([ctypes.POINTER(Shape)] + [P] * 17 +
                                      [ctypes.c_size_t, P])
         L.upipe_attn_bwd.restype = ctypes.c_int
+        L.upipe_selftest_wait_timeout.argtypes = [ctypes.c_int, P]
+        L.upipe_selftest_wait_timeout.restype = ctypes.c_int
         L.upipe_last_error.argtypes = []
         L.upipe_last_error.restype = ctypes.c_int
         L.upipe_profile_attach.argtypes = [ctypes.c_int, P, P, ctypes.c_int]
@@ -157,6 +159,12 @@ class KernelTimer:
     def durations_ms(self):
         torch.cuda.synchronize()
         return [s.elapsed_time(e) for s, e in zip(self.starts[:self.count], self.ends[:self.count])]
+
+
+def selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    """Enqueue the bounded-wait self-test kernel (its waits expire)."""
+    _check(lib().upipe_selftest_wait_timeout(int(limit_us), _stream(stream)),
+           "upipe_selftest_wait_timeout")
 
 
 def last_error() -> int:

@@ -17,7 +17,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libupipe.so")
-SOURCES = ["upipe.cu", "gemm.cu", "attn_fwd.cu", "attn_bwd.cu", "elementwise.cu", "noalloc.cu"]
+SOURCES = ["upipe.cu", "gemm.cu", "attn_fwd.cu", "attn_bwd.cu", "elementwise.cu", "noalloc.cu",
+           "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

@@ -151,4 +151,7 @@ cudaError_t launch_qk_bwd(const QkBwdArgs& a, cudaStream_t stream);
 cudaError_t launch_f32_to_bf16x2(const float* in, int ld_in, bf16* hi, bf16* lo, int ld_out,
                                  long long S, int cols, cudaStream_t stream);
 
+// One-CTA kernel whose waits expire after limit_ns (failure-detection test).
+cudaError_t launch_selftest_wait(int* err, unsigned long long limit_ns, cudaStream_t stream);
+
 }  // namespace upipe

@@ -59,8 +59,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Wait until the phase with the given parity of ``bar`` has completed.
 // Gives up after kWaitLimitNs or as soon as another role has raised *abort;
 // a timeout is recorded in *err (first error wins) and raises *abort.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err,
-                                          volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, int* err,
+                                              volatile int* abort, unsigned long long limit_ns) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
@@ -68,13 +68,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
     if (mbar_try_wait(a, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         atomicCAS(err, 0, kErrDeviceTimeout);
         *abort = 1;
         return false;
       }
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err,
+                                          volatile int* abort) {
+  return mbar_wait_for(bar, parity, err, abort, kWaitLimitNs);
 }
 
 // Teardown wait after an abort: bounded by time only.

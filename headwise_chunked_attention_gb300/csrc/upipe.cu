@@ -621,6 +621,15 @@ extern "C" void upipe_profile_attach(int kernel, void* const* start_events,
 
 extern "C" int upipe_profile_count(void) { return g_prof.count; }
 
+extern "C" int upipe_selftest_wait_timeout(int limit_us, void* stream) {
+  if (limit_us <= 0 || limit_us > 1000000) return UPIPE_ERR_INVALID_ARG;
+  DeviceState* ds = nullptr;
+  UPIPE_TRY(device_state(&ds));
+  UPIPE_CUDA(launch_selftest_wait(ds->err, (unsigned long long)limit_us * 1000ull,
+                                  static_cast<cudaStream_t>(stream)));
+  return UPIPE_OK;
+}
+
 extern "C" int upipe_last_error(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return UPIPE_ERR_CUDA;
   int v = 0;

@@ -153,6 +153,15 @@ void upipe_profile_attach(int kernel, void* const* start_events, void* const* en
                           int capacity);
 int upipe_profile_count(void);
 
+/* Failure-detection self-test (no counterpart on the pages).  Enqueues a
+ * one-CTA kernel whose device-side waits can never be satisfied and expire
+ * after limit_us microseconds (1 .. 1e6), exactly as a stuck wait inside the
+ * layer kernels would: the kernel records UPIPE_ERR_DEVICE_TIMEOUT in the
+ * device error word and returns, without faulting.  The next
+ * upipe_last_error() reports it; the context stays usable.
+ * Returns UPIPE_OK once enqueued, UPIPE_ERR_INVALID_ARG for a bad limit. */
+int upipe_selftest_wait_timeout(int limit_us, void* stream);
+
 /* Synchronises the current device, then returns and clears the device error
  * word (UPIPE_OK or UPIPE_ERR_DEVICE_TIMEOUT), or UPIPE_ERR_CUDA if the
  * device reports a CUDA error. */
