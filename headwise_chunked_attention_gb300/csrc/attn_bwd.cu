@@ -79,10 +79,6 @@ struct BwdCfg {
   static constexpr uint32_t SMEM_BYTES = BAR_OFF + 256;
 };
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 }  // namespace
 
 template <int D>

@@ -18,7 +18,10 @@
 // Epilogues (what the attention layer needs around the attention kernel):
 //   EPI_PROJ        Q/K/V projection of one head chunk: optional per-head
 //                   RMSNorm (Qwen3 geometry), RoPE, bf16 store to workspace;
-//   EPI_F32         Wo-slice partial result: out (+)= O_c Wo_c^T in fp32;
+//   EPI_F32         Wo-slice partial result: out (+)= O_c Wo_c^T in fp32,
+//                   staged per warp in shared memory and written by TMA store
+//                   (first chunk) or TMA reduce-add (later chunks: the
+//                   read-modify-write runs in L2, the SM never reads out);
 //   EPI_DO          dO_c = dOut Wo_c with D = rowsum(dO * O) per head;
 //   EPI_F32_ATOMIC  split-K weight gradients, reduced with red.global.add.
 #include <algorithm>
@@ -35,13 +38,18 @@ constexpr int BK = 64;                      // one 128-byte swizzle atom of bf16
 constexpr int kThreads = 192;
 constexpr uint32_t A_STAGE_BYTES = BM * BK * 2;  // 16 KB
 
+constexpr int kEpiBufs = 2;                       // staging buffers per epilogue warp
+constexpr uint32_t EPI_BUF_BYTES = 32 * 32 * 4;   // [32 rows][32 cols] fp32
+
 template <int BN>
 struct GemmCfg {
   static constexpr uint32_t B_STAGE_BYTES = BN * BK * 2;
   static constexpr uint32_t STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
   static constexpr int STAGES = (BN == 256) ? 4 : 6;
   static constexpr uint32_t TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
-  static constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*bars*/;
+  static constexpr uint32_t EPI_OFF = STAGES * STAGE_BYTES;
+  static constexpr uint32_t BAR_OFF = EPI_OFF + 4 * kEpiBufs * EPI_BUF_BYTES;
+  static constexpr uint32_t SMEM_BYTES = BAR_OFF + 1024 /*align*/ + 256 /*bars*/;
 };
 
 struct TileCoord {
@@ -124,14 +132,15 @@ template <int BN, bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap0,
                 const __grid_constant__ CUtensorMap bmap1,
-                const __grid_constant__ CUtensorMap bmap2, const GemmArgs g, const EpiParams ep,
+                const __grid_constant__ CUtensorMap bmap2,
+                const __grid_constant__ CUtensorMap cmap, const GemmArgs g, const EpiParams ep,
                 int* __restrict__ err) {
   using Cfg = GemmCfg<BN>;
   constexpr int STAGES = Cfg::STAGES;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * Cfg::STAGE_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::BAR_OFF);
   uint64_t* empty = full + STAGES;
   uint64_t* acc_full = empty + STAGES;
   uint64_t* acc_empty = acc_full + 2;
@@ -268,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     int it = 0;
+    uint32_t epi_round = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
       const TileCoord tc = tile_coord(t, num_m, num_n, kb_total, ksplit);
       const int acc = it & 1;
@@ -337,6 +347,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (live) ep.D[(long long)head * g.M + m] = dot;
+      } else if constexpr (EPI == EPI_F32) {
+        // [32 rows x 32 cols] fp32 blocks of this warp's rows, 128-byte
+        // swizzled in shared memory, then one TMA store / reduce-add each
+        uint8_t* bufs = smem + Cfg::EPI_OFF + quarter * kEpiBufs * EPI_BUF_BYTES;
+        const bool any_live = (tc.m0 + quarter * 32 < g.M) && (tc.kb1 > tc.kb0);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c, ++epi_round) {
+          uint32_t r[32];
+          tmem_ld32(tbase + c * 32, r);
+          tmem_ld_wait(r);
+          if (any_live) {
+            uint8_t* buf = bufs + (epi_round % kEpiBufs) * EPI_BUF_BYTES;
+            if (lane == 0) bulk_wait_read<kEpiBufs - 1>();  // buf's previous copy has read it
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              *reinterpret_cast<uint4*>(buf + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+                  make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              if (ep.beta) tma_reduce_add_2d(&cmap, buf, n0 + 32 * c, tc.m0 + quarter * 32);
+              else tma_store_2d(&cmap, buf, n0 + 32 * c, tc.m0 + quarter * 32);
+              bulk_commit();
+            }
+          }
+        }
       } else {
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
@@ -345,29 +382,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait(r);
           if (live) {
             float* cp = ep.C + m * ep.ldc + n0 + c * 32;
-            if constexpr (EPI == EPI_F32) {
 #pragma unroll
-              for (int i = 0; i < 32; i += 4) {
-                float4 w = make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
-                                       __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
-                if (ep.beta) {
-                  const float4 o = *reinterpret_cast<const float4*>(cp + i);
-                  w.x += o.x; w.y += o.y; w.z += o.z; w.w += o.w;
-                }
-                *reinterpret_cast<float4*>(cp + i) = w;
-              }
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; i += 4)
-                red_add_v4_f32(cp + i, __uint_as_float(r[i]), __uint_as_float(r[i + 1]),
-                               __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
-            }
+            for (int i = 0; i < 32; i += 4)
+              red_add_v4_f32(cp + i, __uint_as_float(r[i]), __uint_as_float(r[i + 1]),
+                             __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
           }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
+    }
+    if constexpr (EPI == EPI_F32) {
+      if (lane == 0) bulk_wait_all();
+      __syncwarp();
     }
   }
 
@@ -393,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int BN, bool A_MN, bool B_MN, int EPI>
 static cudaError_t launch_t(const CUtensorMap& amap, const CUtensorMap* bmaps, int nb,
                             const GemmArgs& g, const EpiParams& ep, int* err, int num_sms,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, const CUtensorMap* cmap) {
   using Cfg = GemmCfg<BN>;
   auto kfn = gemm_kernel<BN, A_MN, B_MN, EPI>;
   static bool attr_set = false;
@@ -408,18 +436,20 @@ static cudaError_t launch_t(const CUtensorMap& amap, const CUtensorMap* bmaps, i
   const int grid = (int)std::max(1LL, std::min<long long>(tiles, num_sms));
   const CUtensorMap& b1 = nb > 1 ? bmaps[1] : bmaps[0];
   const CUtensorMap& b2 = nb > 2 ? bmaps[2] : bmaps[0];
-  kfn<<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(amap, bmaps[0], b1, b2, g, ep, err);
+  if (EPI == EPI_F32 && !cmap) return cudaErrorInvalidValue;
+  const CUtensorMap& cm = cmap ? *cmap : bmaps[0];
+  kfn<<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(amap, bmaps[0], b1, b2, cm, g, ep, err);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gemm(int bn, bool a_mn, bool b_mn, EpiKind epi, const CUtensorMap& amap,
                         const CUtensorMap* bmaps, int nb, const GemmArgs& g, const EpiParams& ep,
-                        int* err, int num_sms, cudaStream_t stream) {
+                        int* err, int num_sms, cudaStream_t stream, const CUtensorMap* cmap) {
   if (g.M <= 0 || g.N <= 0) return cudaSuccess;
   if (g.N % bn != 0) return cudaErrorInvalidValue;
 #define UPIPE_GEMM_CASE(BN_, AMN, BMN, E)                                              \
   if (bn == BN_ && a_mn == AMN && b_mn == BMN && epi == E)                             \
-    return launch_t<BN_, AMN, BMN, E>(amap, bmaps, nb, g, ep, err, num_sms, stream);
+    return launch_t<BN_, AMN, BMN, E>(amap, bmaps, nb, g, ep, err, num_sms, stream, cmap);
   // projections (one head per tile: BN = d)
   UPIPE_GEMM_CASE(64, false, false, EPI_PROJ)
   UPIPE_GEMM_CASE(128, false, false, EPI_PROJ)

@@ -62,7 +62,7 @@ struct EpiParams {
   // EPI_F32 / EPI_F32_ATOMIC
   float* C;
   long long ldc;
-  int beta;
+  int beta;          // EPI_F32: 0 store, 1 add (both through the C tensor map)
   // EPI_DO
   bf16* dO;
   int ld_do;
@@ -79,9 +79,12 @@ struct GemmArgs {
 
 // a_mn / b_mn: operand stored MN-major (A as [K, M] row-major, B as [K, N]).
 // bmaps: 1..3 maps for B (EPI_PROJ may use one per segment).
+// cmap: for EPI_F32, an fp32 tensor map over C with box 32 x 32 (128-byte
+// swizzle); the epilogue stores (beta 0) or reduce-adds (beta 1) through it.
 cudaError_t launch_gemm(int bn, bool a_mn, bool b_mn, EpiKind epi, const CUtensorMap& amap,
                         const CUtensorMap* bmaps, int nbmaps, const GemmArgs& g,
-                        const EpiParams& ep, int* err, int num_sms, cudaStream_t stream);
+                        const EpiParams& ep, int* err, int num_sms, cudaStream_t stream,
+                        const CUtensorMap* cmap = nullptr);
 
 // ------------------------------------------------------------- attention --
 

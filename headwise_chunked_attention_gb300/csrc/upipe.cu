@@ -349,8 +349,9 @@ extern "C" int upipe_attn_fwd(const upipe_shape_t* shape, const upipe_bf16* x_,
   float* flush = L.flush == (size_t)-1 ? nullptr : at<float>(workspace, L.flush);
   UPIPE_CUDA(launch_rope_table(rhi, rlo, g.S, g.d, shape->rope_theta, st));
 
-  CUtensorMap xmap;
+  CUtensorMap xmap, outmap;
   UPIPE_MAP(&xmap, x, g.S, g.hidden, g.hidden, 128, 64);
+  if (!make_tmap_f32(&outmap, out, g.S, g.hidden, g.hidden, 32, 32)) return UPIPE_ERR_CUDA;
   const int out_bn = (g.hidden % 256 == 0) ? 256 : 128;
   for (int c = 0; c < g.nchunks; ++c) {
     const int h0 = c * g.ch;
@@ -374,7 +375,7 @@ extern "C" int upipe_attn_fwd(const upipe_shape_t* shape, const upipe_bf16* x_,
     ep.beta = c > 0;
     GemmArgs ga{(int)g.S, g.hidden, g.ch * g.d, 1, g.d};
     UPIPE_CUDA(launch_gemm(out_bn, false, false, EPI_F32, om, &wom, 1, ga, ep, ds->err,
-                           ds->num_sms, st));
+                           ds->num_sms, st, &outmap));
   }
   return UPIPE_OK;
 }
@@ -442,7 +443,8 @@ extern "C" int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x_,
     UPIPE_CUDA(cudaMemsetAsync(dk_norm_w, 0, sizeof(float) * d, st));
   }
 
-  CUtensorMap xmap, x_mn, dout_k, dout_mn;
+  CUtensorMap xmap, x_mn, dout_k, dout_mn, dxmap;
+  if (!make_tmap_f32(&dxmap, dx, g.S, g.hidden, g.hidden, 32, 32)) return UPIPE_ERR_CUDA;
   UPIPE_MAP(&xmap, x, g.S, g.hidden, g.hidden, 128, 64);       // A, K-major
   UPIPE_MAP(&x_mn, x, g.S, g.hidden, g.hidden, 64, 64);        // B of dW = dA^T x (MN-major)
   UPIPE_MAP(&dout_k, dout, g.S, g.hidden, g.hidden, 128, 64);  // A of dO = dout Wo_c
@@ -462,7 +464,7 @@ extern "C" int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x_,
     ep.beta = dx_started ? 1 : 0;
     GemmArgs ga{(int)g.S, g.hidden, ncols, 1, d};
     UPIPE_CUDA(launch_gemm(dx_bn, false, true, EPI_F32, am, &bm, 1, ga, ep, ds->err,
-                           ds->num_sms, st));
+                           ds->num_sms, st, &dxmap));
     dx_started = true;
     return UPIPE_OK;
   };
