@@ -26,8 +26,8 @@
 //   warp 13      TMA producer: K, V once, then Q_u, dO_u through 3 stages
 //   warps 14-15  idle (they complete warpgroup 3 for register reallocation)
 // Registers are moved with setmaxnreg from warpgroups 2 and 3 to the two
-// softmax warpgroups: 168 + 168 + 104 + 40 per thread, x 128 threads each =
-// 61440 of the 65536 the block is launched with (512 threads x 128).
+// softmax warpgroups: 168 + 168 + 104 + 72 per thread, x 128 threads each =
+// 65536, the registers the block is launched with (512 threads x 128).
 // TMEM (512 columns), slot s in {0, 1} at column 128 s:
 //   [+0, +64)   S^T_u = K Q_u^T (fp32); then P^T_u (bf16, +0..31) and
 //               dS^T_u (bf16, +32..63), A operands of the dV / dK MMAs
@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
 
   const int wgroup = warp >> 2;
   if (wgroup == 3) {
-  setmaxnreg_dec<40>();
+  setmaxnreg_dec<72>();
   if (warp == kWarpTma) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {

@@ -16,6 +16,10 @@
 //   warps 4-7   softmax + epilogue of tile 1
 //   warp 8      TMEM owner and tcgen05.mma issuer
 //   warp 9      TMA producer (Q once, then K_j, V_j through a 4-slot ring)
+//   warps 10-11 idle (they complete warpgroup 2 for register reallocation)
+// setmaxnreg gives the softmax warpgroups 216 registers a thread and
+// warpgroup 2 72: 2 x 128 x 216 + 128 x 72 = 64512 = 384 threads x 168, the
+// registers the block is launched with.
 // TMEM (512 columns): S_0 | S_1 | O_0 | O_1.  P_t (bf16) is written over the
 // first half of S_t and fed to the PV MMA straight from TMEM.
 // Softmax runs in base 2 with a lazily updated row max: O and l are rescaled
@@ -38,7 +42,7 @@ namespace upipe {
 
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
 constexpr int kSlots = 4;
 
 __device__ __forceinline__ uint32_t sm_id() {
@@ -91,8 +95,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kvh = (a.h0 + head) / a.group - a.kv0;
   const int q0 = qb * 256;
   const int n_kv = 2 * qb + 2;  // KV tiles of query tile 1; tile 0 has n_kv - 1
-  const uint32_t smid = sm_id();
-  const bool flushing = a.flush != nullptr && smid < (uint32_t)kFlushSlots;
+  // folding of long rows (see above): only when the scratch exists, the rows
+  // are long enough, and this SM id has a slot
+  const bool folding = a.flush != nullptr && n_kv > kFlushTiles && sm_id() < (uint32_t)kFlushSlots;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -123,6 +128,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  if (warp >= 8) {
+  setmaxnreg_dec<72>();
   if (warp == 9) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -183,11 +190,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t o_tmem = tmem + Cfg::O_COL + t * D;
             const uint32_t p_tmem = tmem + 128 * t;
+            const uint32_t acc0 =
+                ((j - 1 == 0) || (folding && (j - 1) % kFlushTiles == 0)) ? 0u : 1u;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               const uint64_t bd = sdesc_sw128(v_addr + k * 2048, Cfg::BLOCK_BYTES, 1024);
-              const bool fresh = (j - 1 == 0) || (flushing && (j - 1) % kFlushTiles == 0);
-              mma_ts_w(o_tmem, p_tmem + k * 8, bd, IDESC_O, (!fresh || k > 0) ? 1u : 0u);
+              mma_ts_w(o_tmem, p_tmem + k * 8, bd, IDESC_O, k > 0 ? 1u : acc0);
             }
             if (t == 1) mma_commit_w(&slot_empty[vslot]);
             if (j - 1 == nt - 1) mma_commit_w(&o_done[t]);
@@ -209,8 +217,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+  }
   } else {
     // --------------------------------------------------- softmax (tile t)
+    setmaxnreg_inc<216>();
     const int t = warp >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
@@ -222,9 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = a.scale_log2;
     float m_run = -INFINITY;
     float l_run = 0.f;
-    bool have_acc = false;  // a folded part of O exists in acc_row
-    float m_acc = 0.f;      // row max the folded part is expressed in
-    float* acc_row = flushing ? a.flush + ((size_t)smid * 256 + 128 * t + r) * D : nullptr;
+    float m_acc = -INFINITY;  // row max of the folded part of O (-inf: nothing folded)
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
       // warp-uniform: the tcgen05.ld/st below are warp-collective
@@ -281,9 +289,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st32(s_tmem + 32 * h, pk);
       }
       l_run += sum;
-      if (flushing && j > 0 && j % kFlushTiles == 0) {
+      if (folding && j > 0 && j % kFlushTiles == 0) {
         // O in TMEM holds PV(0 .. j-1) since the last fold, in units of m_run
+        const bool have_acc = m_acc != -INFINITY;
         const float keep = have_acc ? ex2(m_acc - m_run) : 0.f;
+        float* acc_row = a.flush + ((size_t)sm_id() * 256 + 128 * t + r) * D;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t rr[32];
@@ -302,7 +312,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<float4*>(ap + i) = v;
           }
         }
-        have_acc = true;
         m_acc = m_run;
       }
       tmem_st_wait();
@@ -316,7 +325,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv_l = 1.f / l_run;
       const bool live = qpos < a.S;
+      const bool have_acc = m_acc != -INFINITY;
       const float keep = have_acc ? ex2(m_acc - m_run) : 0.f;
+      const float* acc_row =
+          have_acc ? a.flush + ((size_t)sm_id() * 256 + 128 * t + r) * D : nullptr;
       bf16* op = a.O + (long long)qpos * a.ldo + head * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
