@@ -12,8 +12,8 @@ What the method computes, and where it is stated
   liquidgold.cc): the heads a GPU owns are split into chunks that are run one
   after another; per chunk the heads are (re)computed, their attention is
   computed over the whole sequence and the partial result is stored, while the
-  buffers are reused.  The article's own editor's note calls it "not new
-  math": chunking changes memory, not the result.  So the oracle has no
+  buffers are reused.  The article's editor's note says the method brings no
+  new mathematics: chunking changes memory, not the result.  So the oracle has no
   chunking at all; it computes the layer by its plain definition, head by head,
   and chunk invariance is a property the tests check.
 * The Q&A of the talk (aipmzone.com article, Q&A; transcript) names the query,
