@@ -240,22 +240,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       float s[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(s_tmem + 32 * c, rr);
+      {
+        uint32_t rr[128];
+        tmem_ld128(s_tmem, rr);
         tmem_ld_wait(rr);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(rr[i]);
+        for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(rr[i]);
       }
       if (j == nt - 1) {
 #pragma unroll
         for (int c = 0; c < 128; ++c)
           if (c > r) s[c] = -INFINITY;
       }
-      float mx = s[0];
+      // row max: four independent three-input chains (depth 16, not 127)
+      float mq[4];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+      for (int k = 0; k < 4; ++k) mq[k] = fmaxf(s[2 * k], s[2 * k + 1]);
+#pragma unroll
+      for (int c = 8; c < 128; c += 8)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mq[k] = fmax3(mq[k], s[c + 2 * k], s[c + 2 * k + 1]);
+      const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
       const float m_new = fmaxf(m_run, mx * sl2);
       const bool need = m_new > m_run + kRescaleThreshold;
       if (__any_sync(0xffffffffu, need) && j > 0) {
@@ -275,20 +280,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         l_run *= ex2(m_run - m_new);
         m_run = m_new;
       }
-      float sum = 0.f;
+      // p = 2^(s * scale_log2 - m): pairs through one packed FMA each; the
+      // row sum in four packed partial sums (depth 16)
+      const float2 sc2 = make_float2(sl2, sl2);
+      const float2 nm2 = make_float2(-m_run, -m_run);
+      float2 ps[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                      make_float2(0.f, 0.f)};
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2(fmaf(s[64 * h + 2 * i], sl2, -m_run));
-          const float p1 = ex2(fmaf(s[64 * h + 2 * i + 1], sl2, -m_run));
-          sum += p0 + p1;
-          pk[i] = pack_bf16(p0, p1);
+          float2 x = ffma2(make_float2(s[64 * h + 2 * i], s[64 * h + 2 * i + 1]), sc2, nm2);
+          x.x = ex2(x.x);
+          x.y = ex2(x.y);
+          ps[i & 3] = fadd2(ps[i & 3], x);
+          pk[i] = pack_bf16(x.x, x.y);
         }
         tmem_st32(s_tmem + 32 * h, pk);
       }
-      l_run += sum;
+      const float2 s01 = fadd2(ps[0], ps[1]);
+      const float2 s23 = fadd2(ps[2], ps[3]);
+      l_run += (s01.x + s23.x) + (s01.y + s23.y);
       if (folding && j > 0 && j % kFlushTiles == 0) {
         // O in TMEM holds PV(0 .. j-1) since the last fold, in units of m_run
         const bool have_acc = m_acc != -INFINITY;
