@@ -252,6 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
     const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
     const uint32_t slot = tmem + lane_off + 128 * wg;
     const float sl2 = a.scale * 1.4426950408889634f;
+    const float2 sl2x2 = make_float2(sl2, sl2);
     const float* lse_g = a.lse + (long long)head * a.lse_stride;
     const float* D_g = a.D + (long long)head * S;
     // lse/D of the current sub-tile, shared by the warpgroup and double-buffered
@@ -277,8 +278,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
         const bool live = k0 + u * BQ + 32 * m + lane < S;  // queries past S: P = 0
-        ld_w[32 * m + lane] = live ? nl[m] * 1.4426950408889634f : INFINITY;
-        ld_w[BQ + 32 * m + lane] = live ? nd[m] : 0.f;
+        // stored negated, as the packed FMA / add below take them
+        ld_w[32 * m + lane] = live ? -nl[m] * 1.4426950408889634f : -INFINITY;
+        ld_w[BQ + 32 * m + lane] = live ? -nd[m] : 0.f;
       }
       __syncwarp();
       if (u + 2 < n_u) fetch(u + 2);
@@ -302,11 +304,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
           tmem_ld_wait(rr);
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
-            const float4 l4 = lse4[(32 * h + i) / 4];
-            p[i] = ex2(fmaf(__uint_as_float(rr[i]), sl2, -l4.x));
-            p[i + 1] = ex2(fmaf(__uint_as_float(rr[i + 1]), sl2, -l4.y));
-            p[i + 2] = ex2(fmaf(__uint_as_float(rr[i + 2]), sl2, -l4.z));
-            p[i + 3] = ex2(fmaf(__uint_as_float(rr[i + 3]), sl2, -l4.w));
+            const float4 l4 = lse4[(32 * h + i) / 4];  // -lse (log2 units)
+            const float2 x0 = ffma2(make_float2(__uint_as_float(rr[i]), __uint_as_float(rr[i + 1])),
+                                    sl2x2, make_float2(l4.x, l4.y));
+            const float2 x1 = ffma2(make_float2(__uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3])),
+                                    sl2x2, make_float2(l4.z, l4.w));
+            p[i] = ex2(x0.x);
+            p[i + 1] = ex2(x0.y);
+            p[i + 2] = ex2(x1.x);
+            p[i + 3] = ex2(x1.y);
           }
         }
         if (h == 1) tmem_st16(slot + 32, ds0);  // S^T fully read now
@@ -327,11 +333,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
           tmem_ld_wait(rr);
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
-            const float4 d4 = dd4[(32 * h + i) / 4];
-            pk[i / 2] = pack_bf16(p[i] * (__uint_as_float(rr[i]) - d4.x),
-                                  p[i + 1] * (__uint_as_float(rr[i + 1]) - d4.y));
-            pk[i / 2 + 1] = pack_bf16(p[i + 2] * (__uint_as_float(rr[i + 2]) - d4.z),
-                                      p[i + 3] * (__uint_as_float(rr[i + 3]) - d4.w));
+            const float4 d4 = dd4[(32 * h + i) / 4];  // -D
+            const float2 g0 = fmul2(make_float2(p[i], p[i + 1]),
+                                    fadd2(make_float2(__uint_as_float(rr[i]), __uint_as_float(rr[i + 1])),
+                                          make_float2(d4.x, d4.y)));
+            const float2 g1 = fmul2(make_float2(p[i + 2], p[i + 3]),
+                                    fadd2(make_float2(__uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3])),
+                                          make_float2(d4.z, d4.w)));
+            pk[i / 2] = pack_bf16(g0.x, g0.y);
+            pk[i / 2 + 1] = pack_bf16(g1.x, g1.y);
           }
           if (h == 0) {
 #pragma unroll

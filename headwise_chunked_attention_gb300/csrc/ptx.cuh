@@ -379,6 +379,18 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   return r;
 }
 
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
 __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
   float2 r;
   asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
