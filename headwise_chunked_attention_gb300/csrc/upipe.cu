@@ -38,6 +38,9 @@ struct DeviceState {
   bool ready = false;
   int num_sms = 0;
   int* err = nullptr;
+  // highest-priority stream on which the forward runs each chunk's Wo-slice
+  // accumulate beside the next chunk's attention (nullptr: not available)
+  cudaStream_t side = nullptr;
 };
 
 // measurement hook (upipe_profile_attach)
@@ -74,6 +77,12 @@ int device_state(DeviceState** out) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return UPIPE_ERR_CUDA;
     s.err = static_cast<int*>(p);
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
+        cudaStreamCreateWithPriority(&s.side, cudaStreamNonBlocking, greatest) != cudaSuccess) {
+      s.side = nullptr;
+      cudaGetLastError();
+    }
     s.ready = true;
   }
   *out = &s;
@@ -240,6 +249,29 @@ T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
 }
 
+// Events of one forward call's fork/join with the side stream.  Destroying an
+// event whose record is still pending is allowed: CUDA frees it on completion.
+struct Events {
+  cudaEvent_t proj = nullptr, out[2] = {nullptr, nullptr};
+  cudaError_t create() {
+    for (cudaEvent_t* e : {&proj, &out[0], &out[1]}) {
+      const cudaError_t r = cudaEventCreateWithFlags(e, cudaEventDisableTiming);
+      if (r != cudaSuccess) return r;
+    }
+    return cudaSuccess;
+  }
+  ~Events() {
+    for (cudaEvent_t e : {proj, out[0], out[1]})
+      if (e) cudaEventDestroy(e);
+  }
+};
+
+// SMs given to a Wo-slice accumulate that runs beside an attention launch: it
+// is bound by HBM (a read-modify-write of the fp32 layer output), which a
+// fifth of the SMs can nearly saturate, and the rest keep the tensor cores of
+// the attention busy.
+inline int side_sms(int num_sms) { return std::max(8, num_sms / 5); }
+
 // Fused projection of one chunk: Q heads [h0, h0+ch) and, when the chunk
 // starts a new KV group, K and V heads [kv0, kv0+kvc).  Each 128-row x d
 // output tile is one head, so a head's values never depend on chunk_heads.
@@ -353,17 +385,22 @@ extern "C" int upipe_attn_fwd(const upipe_shape_t* shape, const upipe_bf16* x_,
   UPIPE_MAP(&xmap, x, g.S, g.hidden, g.hidden, 128, 64);
   if (!make_tmap_f32(&outmap, out, g.S, g.hidden, g.hidden, 32, 32)) return UPIPE_ERR_CUDA;
   const int out_bn = (g.hidden % 256 == 0) ? 256 : 128;
-  for (int c = 0; c < g.nchunks; ++c) {
+
+  // Chunk c projects Q into buffer c % 2 and the attention writes O over it in
+  // place (each Q tile is read only by the CTA that writes the same O rows, and
+  // before it writes them).  With more than one chunk, the Wo-slice accumulate
+  // of chunk c - 1 runs on the side stream with a few SMs, after the projection
+  // of chunk c and beside its attention; the projection of chunk c + 1 waits
+  // for it, since it overwrites that buffer.  The last accumulate runs on the
+  // caller's stream with every SM, after the side stream's work.
+  bf16* QO[2] = {Q, Ows};
+  const bool overlap = g.nchunks > 1 && ds->side != nullptr;
+  Events ev;
+  if (overlap) UPIPE_CUDA(ev.create());
+  auto out_gemm = [&](int c, cudaStream_t s, int sms) -> int {
     const int h0 = c * g.ch;
-    const int kv0 = h0 / g.g;
-    const bool new_group = (g.ch >= g.g) || (h0 % g.g == 0);
-    UPIPE_TRY(project_chunk(g, ds, st, xmap, Wq, Wk, Wv, q_norm_w, k_norm_w, shape->norm_eps, h0,
-                            kv0, new_group, Q, K, V, rhi, rlo, nullptr, nullptr, nullptr,
-                            nullptr));
-    bf16* O = dbg ? dbg + (size_t)h0 * g.d : Ows;
+    const bf16* O = dbg ? dbg + (size_t)h0 * g.d : QO[c & 1];
     const int ldo = dbg ? g.Hq * g.d : g.ch * g.d;
-    UPIPE_TRY(attention_chunk(g, ds, st, Q, K, V, h0, kv0, O, ldo, lse + (size_t)h0 * g.S,
-                              flush));
     // out (+)= O_c Wo[:, h0*d : (h0+ch)*d]^T  (the chunk's partial result)
     CUtensorMap om, wom;
     UPIPE_MAP(&om, O, g.S, (uint64_t)g.ch * g.d, ldo, 128, 64);
@@ -374,9 +411,32 @@ extern "C" int upipe_attn_fwd(const upipe_shape_t* shape, const upipe_bf16* x_,
     ep.ldc = g.hidden;
     ep.beta = c > 0;
     GemmArgs ga{(int)g.S, g.hidden, g.ch * g.d, 1, g.d};
-    UPIPE_CUDA(launch_gemm(out_bn, false, false, EPI_F32, om, &wom, 1, ga, ep, ds->err,
-                           ds->num_sms, st, &outmap));
+    UPIPE_CUDA(launch_gemm(out_bn, false, false, EPI_F32, om, &wom, 1, ga, ep, ds->err, sms, s,
+                           &outmap));
+    return UPIPE_OK;
+  };
+  for (int c = 0; c < g.nchunks; ++c) {
+    const int h0 = c * g.ch;
+    const int kv0 = h0 / g.g;
+    const bool new_group = (g.ch >= g.g) || (h0 % g.g == 0);
+    bf16* Qc = QO[c & 1];
+    if (overlap && c >= 2) UPIPE_CUDA(cudaStreamWaitEvent(st, ev.out[c & 1], 0));
+    UPIPE_TRY(project_chunk(g, ds, st, xmap, Wq, Wk, Wv, q_norm_w, k_norm_w, shape->norm_eps, h0,
+                            kv0, new_group, Qc, K, V, rhi, rlo, nullptr, nullptr, nullptr,
+                            nullptr));
+    if (overlap && c >= 1) {
+      UPIPE_CUDA(cudaEventRecord(ev.proj, st));
+      UPIPE_CUDA(cudaStreamWaitEvent(ds->side, ev.proj, 0));
+      UPIPE_TRY(out_gemm(c - 1, ds->side, side_sms(ds->num_sms)));
+      UPIPE_CUDA(cudaEventRecord(ev.out[(c - 1) & 1], ds->side));
+    }
+    bf16* O = dbg ? dbg + (size_t)h0 * g.d : Qc;
+    const int ldo = dbg ? g.Hq * g.d : g.ch * g.d;
+    UPIPE_TRY(attention_chunk(g, ds, st, Qc, K, V, h0, kv0, O, ldo, lse + (size_t)h0 * g.S,
+                              flush));
   }
+  if (overlap) UPIPE_CUDA(cudaStreamWaitEvent(st, ev.out[(g.nchunks - 2) & 1], 0));
+  UPIPE_TRY(out_gemm(g.nchunks - 1, st, ds->num_sms));
   return UPIPE_OK;
 }
 

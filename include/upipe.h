@@ -25,10 +25,15 @@
  *  - Pointers named x, W*, out, lse, d*, workspace are DEVICE pointers of the
  *    current CUDA device; every buffer must be 16-byte aligned.
  *  - ``stream`` is a cudaStream_t (NULL = legacy default stream).  Calls only
- *    enqueue work on it and return; nothing is synchronised.  Two calls in
- *    flight at once must not share a workspace.
+ *    enqueue work and return; nothing is synchronised.  The forward may fork
+ *    part of its work onto a library-owned high-priority stream of the device
+ *    and joins it back with events before it returns, so its work is ordered
+ *    like one launch sequence on ``stream``.  Two calls in flight at once
+ *    must not share a workspace.
  *  - Ownership: the caller owns every buffer.  The library allocates no device
- *    or host memory of its own; all temporaries live in ``workspace``.
+ *    or host memory of its own (it creates only the one stream per device named
+ *    above and three events per forward call); all temporaries live in
+ *    ``workspace``.
  *  - Errors: every argument is validated on the host before the first launch;
  *    a failed check returns a code and launches nothing.  A device-side wait
  *    that exceeds its time limit is reported by upipe_last_error().
@@ -78,9 +83,9 @@ enum {
  * The bytes are affine in chunk_heads: the per-chunk Q/O (and backward) parts
  * scale with chunk_heads, the K/V part is one KV group (or chunk_heads/(Hq/Hkv)
  * groups when a chunk spans several), plus a RoPE table of
- * ((S >> 10) + 1 + 1024) * d/2 float2 entries.  "The next chunk reuses the
- * buffers the previous chunk allocated" (memeeeeeex.com, "Untied Ulysses
- * (UPipe)"): this one allocation is that buffer. */
+ * ((S >> 10) + 1 + 1024) * d/2 float2 entries.  Every chunk runs in these same
+ * buffers, which is how UPipe saves memory (memeeeeeex.com, "Untied Ulysses
+ * (UPipe)": the chunks reuse one set of buffers). */
 size_t upipe_workspace_bytes(const upipe_shape_t* shape, int mode);
 
 /* Forward of the layer, chunk by chunk (the UPipe loop).
