@@ -56,6 +56,14 @@ struct TileCoord {
   int m0, n0, kb0, kb1;
 };
 
+// Every tensor map of one launch, passed as one __grid_constant__ parameter
+// (TMA reads a map straight from parameter space).
+struct GemmMaps {
+  CUtensorMap a[kMaxASegs];
+  CUtensorMap b[kMaxBMaps];
+  CUtensorMap c;
+};
+
 __device__ __forceinline__ TileCoord tile_coord(int t, int num_m, int num_n, int kb_total,
                                                 int ksplit) {
   const int per_split = num_m * num_n;
@@ -130,10 +138,7 @@ __device__ __forceinline__ void epi_proj_row(const EpiParams& ep, const ProjSeg&
 
 template <int BN, bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap0,
-                const __grid_constant__ CUtensorMap bmap1,
-                const __grid_constant__ CUtensorMap bmap2,
-                const __grid_constant__ CUtensorMap cmap, const GemmArgs g, const EpiParams ep,
+    gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g, const EpiParams ep,
                 int* __restrict__ err) {
   using Cfg = GemmCfg<BN>;
   constexpr int STAGES = Cfg::STAGES;
@@ -153,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int num_m = (g.M + BM - 1) / BM;
   const int num_n = g.N / BN;
-  const int kb_total = (g.K + BK - 1) / BK;
+  const int kb_total = g.nkseg > 0 ? g.kseg_end[g.nkseg - 1] : (g.K + BK - 1) / BK;
   const int ksplit = g.ksplit > 0 ? g.ksplit : 1;
   const int num_tiles = num_m * num_n * ksplit;
 
@@ -171,11 +176,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&amap);
-    prefetch_tmap(&bmap0);
+    prefetch_tmap(&maps.a[0]);
+    prefetch_tmap(&maps.b[0]);
     if (EPI == EPI_PROJ) {
-      prefetch_tmap(&bmap1);
-      prefetch_tmap(&bmap2);
+      prefetch_tmap(&maps.b[1]);
+      prefetch_tmap(&maps.b[2]);
+    }
+    for (int s = 1; s < g.nkseg; ++s) {
+      prefetch_tmap(&maps.a[g.kseg_a[s]]);
+      prefetch_tmap(&maps.b[g.kseg_b[s]]);
     }
   }
   if (warp == 1) {
@@ -197,25 +206,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
         const TileCoord tc = tile_coord(t, num_m, num_n, kb_total, ksplit);
         const int n0 = tc.n0 * BN;
-        const CUtensorMap* bm = &bmap0;
+        const CUtensorMap* am = &maps.a[0];
+        const CUtensorMap* bm = &maps.b[0];
         int brow = n0;
         if (EPI == EPI_PROJ) {
           int s = 0;
           while (s + 1 < ep.nseg && n0 >= ep.seg[s].n_end) ++s;
-          bm = ep.seg[s].bmap == 0 ? &bmap0 : (ep.seg[s].bmap == 1 ? &bmap1 : &bmap2);
+          bm = &maps.b[ep.seg[s].bmap];
           brow = ep.seg[s].b_row0 + (n0 - ep.seg[s].n_begin);
         }
+        // K segment holding block kb (always segment 0 without K segments)
+        int ks = 0, ks_kb0 = 0;
         for (int kb = tc.kb0; kb < tc.kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, err, abort_flag)) { ok = false; break; }
           uint8_t* sa = smem + stage * Cfg::STAGE_BYTES;
           uint8_t* sb = sa + A_STAGE_BYTES;
           mbar_expect_tx(&full[stage], Cfg::STAGE_BYTES);
-          const int k0 = kb * BK;
+          if (g.nkseg > 0) {
+            while (kb >= g.kseg_end[ks]) ks_kb0 = g.kseg_end[ks++];
+            am = &maps.a[g.kseg_a[ks]];
+            bm = &maps.b[g.kseg_b[ks]];
+          }
+          const int k0 = (kb - ks_kb0) * BK;
           if (!A_MN) {
-            tma_load_2d(sa, &amap, &full[stage], k0, tc.m0);
+            tma_load_2d(sa, am, &full[stage], k0, tc.m0);
           } else {
-            tma_load_2d(sa, &amap, &full[stage], tc.m0, k0);
-            tma_load_2d(sa + 8192, &amap, &full[stage], tc.m0 + 64, k0);
+            tma_load_2d(sa, am, &full[stage], tc.m0, k0);
+            tma_load_2d(sa + 8192, am, &full[stage], tc.m0 + 64, k0);
           }
           if (!B_MN) {
             tma_load_2d(sb, bm, &full[stage], k0, brow);
@@ -368,8 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              if (ep.beta) tma_reduce_add_2d(&cmap, buf, n0 + 32 * c, tc.m0 + quarter * 32);
-              else tma_store_2d(&cmap, buf, n0 + 32 * c, tc.m0 + quarter * 32);
+              if (ep.beta) tma_reduce_add_2d(&maps.c, buf, n0 + 32 * c, tc.m0 + quarter * 32);
+              else tma_store_2d(&maps.c, buf, n0 + 32 * c, tc.m0 + quarter * 32);
               bulk_commit();
             }
           }
@@ -419,9 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------ host --
 
 template <int BN, bool A_MN, bool B_MN, int EPI>
-static cudaError_t launch_t(const CUtensorMap& amap, const CUtensorMap* bmaps, int nb,
-                            const GemmArgs& g, const EpiParams& ep, int* err, int num_sms,
-                            cudaStream_t stream, const CUtensorMap* cmap) {
+static cudaError_t launch_t(const GemmMaps& maps, const GemmArgs& g, const EpiParams& ep,
+                            int* err, int num_sms, cudaStream_t stream) {
   using Cfg = GemmCfg<BN>;
   auto kfn = gemm_kernel<BN, A_MN, B_MN, EPI>;
   static bool attr_set = false;
@@ -434,22 +450,30 @@ static cudaError_t launch_t(const CUtensorMap& amap, const CUtensorMap* bmaps, i
   const int num_m = (g.M + BM - 1) / BM;
   const long long tiles = (long long)num_m * (g.N / BN) * std::max(1, g.ksplit);
   const int grid = (int)std::max(1LL, std::min<long long>(tiles, num_sms));
-  const CUtensorMap& b1 = nb > 1 ? bmaps[1] : bmaps[0];
-  const CUtensorMap& b2 = nb > 2 ? bmaps[2] : bmaps[0];
-  if (EPI == EPI_F32 && !cmap) return cudaErrorInvalidValue;
-  const CUtensorMap& cm = cmap ? *cmap : bmaps[0];
-  kfn<<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(amap, bmaps[0], b1, b2, cm, g, ep, err);
+  kfn<<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(maps, g, ep, err);
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemm(int bn, bool a_mn, bool b_mn, EpiKind epi, const CUtensorMap& amap,
-                        const CUtensorMap* bmaps, int nb, const GemmArgs& g, const EpiParams& ep,
-                        int* err, int num_sms, cudaStream_t stream, const CUtensorMap* cmap) {
+cudaError_t launch_gemm(int bn, bool a_mn, bool b_mn, EpiKind epi, const CUtensorMap* amaps,
+                        int na, const CUtensorMap* bmaps, int nb, const GemmArgs& g,
+                        const EpiParams& ep, int* err, int num_sms, cudaStream_t stream,
+                        const CUtensorMap* cmap) {
   if (g.M <= 0 || g.N <= 0) return cudaSuccess;
   if (g.N % bn != 0) return cudaErrorInvalidValue;
+  if (na < 1 || na > kMaxASegs || nb < 1 || nb > kMaxBMaps) return cudaErrorInvalidValue;
+  if (epi == EPI_F32 && !cmap) return cudaErrorInvalidValue;
+  if (g.nkseg < 0 || g.nkseg > kMaxASegs) return cudaErrorInvalidValue;
+  for (int s = 0; s < g.nkseg; ++s)
+    if (g.kseg_a[s] < 0 || g.kseg_a[s] >= na || g.kseg_b[s] < 0 || g.kseg_b[s] >= nb ||
+        g.kseg_end[s] <= (s ? g.kseg_end[s - 1] : 0))
+      return cudaErrorInvalidValue;
+  GemmMaps maps;
+  for (int i = 0; i < kMaxASegs; ++i) maps.a[i] = amaps[i < na ? i : 0];
+  for (int i = 0; i < kMaxBMaps; ++i) maps.b[i] = bmaps[i < nb ? i : 0];
+  maps.c = cmap ? *cmap : bmaps[0];
 #define UPIPE_GEMM_CASE(BN_, AMN, BMN, E)                                              \
   if (bn == BN_ && a_mn == AMN && b_mn == BMN && epi == E)                             \
-    return launch_t<BN_, AMN, BMN, E>(amap, bmaps, nb, g, ep, err, num_sms, stream, cmap);
+    return launch_t<BN_, AMN, BMN, E>(maps, g, ep, err, num_sms, stream);
   // projections (one head per tile: BN = d)
   UPIPE_GEMM_CASE(64, false, false, EPI_PROJ)
   UPIPE_GEMM_CASE(128, false, false, EPI_PROJ)

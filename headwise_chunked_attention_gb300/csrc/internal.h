@@ -71,18 +71,31 @@ struct EpiParams {
   float* D;  // [heads][M]
 };
 
+constexpr int kMaxASegs = 6;  // A tensor maps of one GEMM
+constexpr int kMaxBMaps = 3;  // B tensor maps of one GEMM
+
 struct GemmArgs {
   int M, N, K;      // C[M, N] = sum_k A[m, k] * B[n, k]
   int ksplit;       // number of K partitions (EPI_F32_ATOMIC only)
   int head_dim;     // d (EPI_PROJ / EPI_DO)
+  // K segments (nkseg > 0): the K range is a concatenation of nkseg runs of
+  // 64-wide K blocks; run s ends at block kseg_end[s] (exclusive), reads A from
+  // A map kseg_a[s] and B from B map kseg_b[s], each from K coordinate 0.  So
+  // C = sum_s A_s B_s^T in one accumulator.  K is then 64 * kseg_end[nkseg-1].
+  int nkseg;
+  int kseg_end[kMaxASegs];
+  int kseg_a[kMaxASegs];
+  int kseg_b[kMaxASegs];
 };
 
 // a_mn / b_mn: operand stored MN-major (A as [K, M] row-major, B as [K, N]).
-// bmaps: 1..3 maps for B (EPI_PROJ may use one per segment).
+// amaps: 1..kMaxASegs maps for A (more than one only with K segments).
+// bmaps: 1..kMaxBMaps maps for B (EPI_PROJ may use one per segment, K
+// segments one per run).
 // cmap: for EPI_F32, an fp32 tensor map over C with box 32 x 32 (128-byte
 // swizzle); the epilogue stores (beta 0) or reduce-adds (beta 1) through it.
-cudaError_t launch_gemm(int bn, bool a_mn, bool b_mn, EpiKind epi, const CUtensorMap& amap,
-                        const CUtensorMap* bmaps, int nbmaps, const GemmArgs& g,
+cudaError_t launch_gemm(int bn, bool a_mn, bool b_mn, EpiKind epi, const CUtensorMap* amaps,
+                        int namaps, const CUtensorMap* bmaps, int nbmaps, const GemmArgs& g,
                         const EpiParams& ep, int* err, int num_sms, cudaStream_t stream,
                         const CUtensorMap* cmap = nullptr);
 

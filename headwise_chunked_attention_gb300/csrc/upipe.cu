@@ -303,7 +303,7 @@ int project_chunk(const Geo& g, const DeviceState* ds, cudaStream_t st, const CU
   }
   ep.nseg = ns;
   GemmArgs ga{(int)g.S, n, g.hidden, 1, d};
-  UPIPE_CUDA(launch_gemm(d, false, false, EPI_PROJ, xmap, bm, new_group ? 3 : 1, ga, ep, ds->err,
+  UPIPE_CUDA(launch_gemm(d, false, false, EPI_PROJ, &xmap, 1, bm, new_group ? 3 : 1, ga, ep, ds->err,
                          ds->num_sms, st));
   return UPIPE_OK;
 }
@@ -411,7 +411,7 @@ extern "C" int upipe_attn_fwd(const upipe_shape_t* shape, const upipe_bf16* x_,
     ep.ldc = g.hidden;
     ep.beta = c > 0;
     GemmArgs ga{(int)g.S, g.hidden, g.ch * g.d, 1, g.d};
-    UPIPE_CUDA(launch_gemm(out_bn, false, false, EPI_F32, om, &wom, 1, ga, ep, ds->err, sms, s,
+    UPIPE_CUDA(launch_gemm(out_bn, false, false, EPI_F32, &om, 1, &wom, 1, ga, ep, ds->err, sms, s,
                            &outmap));
     return UPIPE_OK;
   };
@@ -513,17 +513,42 @@ extern "C" int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x_,
   const int ksplit_w = std::max(1, std::min(64, (int)((S + 8191) / 8192)));
   bool dx_started = false;
 
-  auto dx_gemm = [&](const bf16* dA, int ncols, int ld_a, const bf16* W) -> int {
-    // dx (+)= dA[S, ncols] W[ncols rows, hidden]
-    CUtensorMap am, bm;
-    UPIPE_MAP(&am, dA, g.S, (uint64_t)ncols, (uint64_t)ld_a, 128, 64);
-    UPIPE_MAP(&bm, W, (uint64_t)ncols, g.hidden, g.hidden, 64, 64);
+  // dx (+)= sum_s dA_s W_s: one GEMM whose K range runs through the chunk's
+  // projection-output gradients (each as a bf16 hi and lo half) in turn, so
+  // that dx is read and written once per chunk.  W_s is the weight slice
+  // [ncols_s rows, hidden] that produced dA_s [S, ncols_s].
+  struct DxSeg {
+    const bf16* dA;
+    int ncols;
+    const bf16* W;
+  };
+  auto dx_gemm = [&](const DxSeg* segs, int nseg) -> int {
+    CUtensorMap am[kMaxASegs], bm[kMaxBMaps];
+    GemmArgs ga{(int)g.S, g.hidden, 0, 1, d};
+    ga.nkseg = nseg;
+    const bf16* bw[kMaxBMaps] = {};  // weight slice behind each B map
+    int nb = 0, kb = 0;
+    for (int s = 0; s < nseg; ++s) {
+      UPIPE_MAP(&am[s], segs[s].dA, g.S, (uint64_t)segs[s].ncols, (uint64_t)segs[s].ncols, 128,
+                64);
+      int b = 0;
+      while (b < nb && bw[b] != segs[s].W) ++b;
+      if (b == nb) {
+        if (nb == kMaxBMaps) return UPIPE_ERR_INVALID_ARG;
+        UPIPE_MAP(&bm[nb], segs[s].W, (uint64_t)segs[s].ncols, g.hidden, g.hidden, 64, 64);
+        bw[nb++] = segs[s].W;
+      }
+      kb += segs[s].ncols / 64;
+      ga.kseg_end[s] = kb;
+      ga.kseg_a[s] = s;
+      ga.kseg_b[s] = b;
+    }
+    ga.K = kb * 64;
     EpiParams ep{};
     ep.C = dx;
     ep.ldc = g.hidden;
     ep.beta = dx_started ? 1 : 0;
-    GemmArgs ga{(int)g.S, g.hidden, ncols, 1, d};
-    UPIPE_CUDA(launch_gemm(dx_bn, false, true, EPI_F32, am, &bm, 1, ga, ep, ds->err,
+    UPIPE_CUDA(launch_gemm(dx_bn, false, true, EPI_F32, am, nseg, bm, nb, ga, ep, ds->err,
                            ds->num_sms, st, &dxmap));
     dx_started = true;
     return UPIPE_OK;
@@ -536,7 +561,7 @@ extern "C" int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x_,
     ep.C = dW;
     ep.ldc = g.hidden;
     GemmArgs ga{ncols, g.hidden, (int)g.S, ksplit_w, d};
-    UPIPE_CUDA(launch_gemm(128, true, true, EPI_F32_ATOMIC, am, &x_mn, 1, ga, ep, ds->err,
+    UPIPE_CUDA(launch_gemm(128, true, true, EPI_F32_ATOMIC, &am, 1, &x_mn, 1, ga, ep, ds->err,
                            ds->num_sms, st));
     return UPIPE_OK;
   };
@@ -566,7 +591,7 @@ extern "C" int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x_,
       ep.ld_o = g.ch * d;
       ep.D = Dv;
       GemmArgs ga{(int)g.S, g.ch * d, g.hidden, 1, d};
-      UPIPE_CUDA(launch_gemm(d, false, true, EPI_DO, dout_k, &wom, 1, ga, ep, ds->err,
+      UPIPE_CUDA(launch_gemm(d, false, true, EPI_DO, &dout_k, 1, &wom, 1, ga, ep, ds->err,
                              ds->num_sms, st));
       CUtensorMap om;
       UPIPE_MAP(&om, Ows, g.S, (uint64_t)g.ch * d, (uint64_t)g.ch * d, 64, 64);
@@ -575,7 +600,7 @@ extern "C" int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x_,
       ep2.ldc = (long long)g.Hq * d;
       GemmArgs gb{g.hidden, g.ch * d, (int)g.S, ksplit_w, d};
       const int bn = (g.ch * d) % 128 == 0 ? 128 : 64;
-      UPIPE_CUDA(launch_gemm(bn, true, true, EPI_F32_ATOMIC, dout_mn, &om, 1, gb, ep2, ds->err,
+      UPIPE_CUDA(launch_gemm(bn, true, true, EPI_F32_ATOMIC, &dout_mn, 1, &om, 1, gb, ep2, ds->err,
                              ds->num_sms, st));
     }
     // 3. attention backward: dQ_c (fresh), dK/dV (accumulated over the group)
@@ -632,11 +657,12 @@ extern "C" int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x_,
       q.rope_hi = rhi;
       q.rope_lo = rlo;
       UPIPE_CUDA(launch_qk_bwd(q, st));
-      for (bf16* part : {dO, Ows}) {
-        UPIPE_TRY(dx_gemm(part, g.ch * d, g.ch * d, Wq + (size_t)h0 * d * g.hidden));
+      for (bf16* part : {dO, Ows})
         UPIPE_TRY(dw_gemm(part, g.ch * d, g.ch * d, dWq + (size_t)h0 * d * g.hidden));
-      }
     }
+    const bf16* Wq_c = Wq + (size_t)h0 * d * g.hidden;
+    DxSeg dxs[kMaxASegs] = {{dO, g.ch * d, Wq_c}, {Ows, g.ch * d, Wq_c}};
+    int ndx = 2;
     // 5. at the group's last chunk: dK -> dA_k (hi over K, lo beside it),
     //    dV -> hi over V and lo beside it
     if (last_of_group) {
@@ -659,15 +685,19 @@ extern "C" int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x_,
       q.rope_lo = rlo;
       UPIPE_CUDA(launch_qk_bwd(q, st));
       UPIPE_CUDA(launch_f32_to_bf16x2(dV, g.kvc * d, V, dVlo, g.kvc * d, g.S, g.kvc * d, st));
+      const bf16* Wk_g = Wk + (size_t)kv0 * d * g.hidden;
+      const bf16* Wv_g = Wv + (size_t)kv0 * d * g.hidden;
       for (int part = 0; part < 2; ++part) {
         const bf16* gk = part ? dKlo : K;
         const bf16* gv = part ? dVlo : V;
-        UPIPE_TRY(dx_gemm(gk, g.kvc * d, g.kvc * d, Wk + (size_t)kv0 * d * g.hidden));
-        UPIPE_TRY(dx_gemm(gv, g.kvc * d, g.kvc * d, Wv + (size_t)kv0 * d * g.hidden));
         UPIPE_TRY(dw_gemm(gk, g.kvc * d, g.kvc * d, dWk + (size_t)kv0 * d * g.hidden));
         UPIPE_TRY(dw_gemm(gv, g.kvc * d, g.kvc * d, dWv + (size_t)kv0 * d * g.hidden));
+        dxs[ndx++] = {gk, g.kvc * d, Wk_g};
+        dxs[ndx++] = {gv, g.kvc * d, Wv_g};
       }
     }
+    // 6. dx (+)= the chunk's Q part (and the group's K and V parts)
+    UPIPE_TRY(dx_gemm(dxs, ndx));
   }
   return UPIPE_OK;
 }
