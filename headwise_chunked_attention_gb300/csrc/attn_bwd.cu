@@ -28,11 +28,16 @@
 // Registers are moved with setmaxnreg from warpgroups 2 and 3 to the two
 // softmax warpgroups: 168 + 168 + 104 + 72 per thread, x 128 threads each =
 // 65536, the registers the block is launched with (512 threads x 128).
-// TMEM (512 columns), slot s in {0, 1} at column 128 s:
-//   [+0, +64)   S^T_u = K Q_u^T (fp32); then P^T_u (bf16, +0..31) and
-//               dS^T_u (bf16, +32..63), A operands of the dV / dK MMAs
-//   [+64,+128)  dP^T_u = V dO_u^T (fp32); then dQ^T_u = K^T dS^T_u (fp32)
+// TMEM (512 columns), slot s in {0, 1} at column 128 s, two 64-column blocks
+// per slot; for sub-tile u, with b = (u >> 1) & 1:
+//   block b     S^T_u = K Q_u^T (fp32); then P^T_u (bf16, +0..31) and
+//               dS^T_u (bf16, +32..63), A operands of the dV / dK MMAs; then
+//               dQ^T_u = K^T dS^T_u (fp32)
+//   block 1-b   dP^T_u = V dO_u^T (fp32)
 //   [256, 256+d) dV accumulator      [384, 384+d) dK accumulator
+// The blocks swap roles on every use of a slot: S^T of sub-tile u + 2 goes
+// into the block of dP^T_u (dead once its softmax has run) and is computed
+// while the epilogue still reads dQ^T_u; only dP^T_{u+2} waits for that read.
 // dS^T_u is also written to shared memory (one 128-byte swizzled row per key)
 // where it is the MN-major B operand of dQ^T = K^T dS^T.  MMAs issued by one
 // thread complete in order, which makes the reuse of the TMEM slots safe.
@@ -191,36 +196,41 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
       bool ok = mbar_wait_warp(kv_full, 0, err, abort_flag);
       for (int u = 0; u <= n_u && ok; ++u) {
         if (u < n_u) {
-          const int s = u & 1, st = u % NST;
+          const int s = u & 1, st = u % NST, p = (u >> 1) & 1;
           if (!mbar_wait_warp(&q_full[st], (u / NST) & 1, err, abort_flag)) break;
-          if (u >= 2 && !mbar_wait_warp(&dq_free[s], ((u - 2) >> 1) & 1, err, abort_flag)) break;
           tc_fence_after();
           const uint32_t qb = smem_u32(smem + Cfg::ST_OFF + st * Cfg::ST_BYTES);
           const uint32_t dob = qb + Cfg::Q_TILE;
           const uint32_t slot = tmem + 128 * s;
+          // S^T into the block that held dP^T of sub-tile u - 2 (read by its
+          // softmax before its dV / dK MMAs were issued)
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t ko = (k / 4) * Cfg::KV_BLOCK + (k % 4) * 32;
             const uint32_t qo = (k / 4) * Cfg::Q_BLOCK + (k % 4) * 32;
-            mma_ss_w(slot, sdesc_sw128(kb + ko, 16, 1024), sdesc_sw128(qb + qo, 16, 1024), ID_S,
-                   k > 0);
+            mma_ss_w(slot + 64 * p, sdesc_sw128(kb + ko, 16, 1024),
+                     sdesc_sw128(qb + qo, 16, 1024), ID_S, k > 0);
           }
+          // dP^T into the block of dQ^T of sub-tile u - 2: wait for its
+          // read-out, which overlaps the S^T MMAs above
+          if (u >= 2 && !mbar_wait_warp(&dq_free[s], ((u - 2) >> 1) & 1, err, abort_flag)) break;
+          tc_fence_after();
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t ko = (k / 4) * Cfg::KV_BLOCK + (k % 4) * 32;
             const uint32_t qo = (k / 4) * Cfg::Q_BLOCK + (k % 4) * 32;
-            mma_ss_w(slot + 64, sdesc_sw128(vb + ko, 16, 1024), sdesc_sw128(dob + qo, 16, 1024),
-                   ID_S, k > 0);
+            mma_ss_w(slot + 64 * (1 - p), sdesc_sw128(vb + ko, 16, 1024),
+                     sdesc_sw128(dob + qo, 16, 1024), ID_S, k > 0);
           }
           mma_commit_w(&s_full[s]);
         }
         if (u >= 1) {
-          const int v = u - 1, sv = v & 1, stv = v % NST;
+          const int v = u - 1, sv = v & 1, stv = v % NST, pv = (v >> 1) & 1;
           if (!mbar_wait_warp(&p_ready[sv], (v >> 1) & 1, err, abort_flag)) break;
           tc_fence_after();
           const uint32_t qb = smem_u32(smem + Cfg::ST_OFF + stv * Cfg::ST_BYTES);
           const uint32_t dob = qb + Cfg::Q_TILE;
-          const uint32_t slot = tmem + 128 * sv;
+          const uint32_t slot = tmem + 128 * sv + 64 * pv;  // P^T | dS^T, then dQ^T
           const uint32_t dsb = smem_u32(smem + Cfg::DS_OFF + sv * Cfg::DS_BYTES);
           // dV += P^T dO ; dK += dS^T Q   (k over the sub-tile's 64 queries)
 #pragma unroll
@@ -231,10 +241,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
             mma_ts_w(tmem + 384, slot + 32 + k * 8,
                    sdesc_sw128(qb + k * 2048, Cfg::Q_BLOCK, 1024), ID_ACC, acc);
           }
-          // dQ^T = K^T dS^T  (k over the 128 keys; both operands MN-major)
+          // dQ^T = K^T dS^T  (k over the 128 keys; both operands MN-major),
+          // over P^T / dS^T: the dV / dK MMAs above read them first
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            mma_ss_w(slot + 64, sdesc_sw128(kb + k * 2048, Cfg::KV_BLOCK, 1024),
+            mma_ss_w(slot, sdesc_sw128(kb + k * 2048, Cfg::KV_BLOCK, 1024),
                    sdesc_sw128(dsb + k * 2048, Cfg::Q_BLOCK, 1024), ID_DQ, k > 0);
           mma_commit_w(&dq_full[sv]);
           mma_commit_w(&q_empty[stv]);
@@ -291,6 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
       const float4* dd4 = reinterpret_cast<const float4*>(ld_w + BQ);
       const int mask_from = r - u * BQ;  // columns c < mask_from hold key > query: masked
       uint8_t* row = ds_rows;
+      // the slot's two 64-column blocks swap roles on every use of the slot
+      const uint32_t sblk = slot + 64 * ph, pblk = slot + 64 * (ph ^ 1);
       // two halves of 32 queries: P^T, then dS^T = P^T (dP^T - D).  dS^T goes
       // over the second half of S^T, so the first half's dS^T is stored to
       // TMEM only after the second half of S^T has been read.
@@ -300,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
         float p[32];
         {
           uint32_t rr[32];
-          tmem_ld32(slot + 32 * h, rr);
+          tmem_ld32(sblk + 32 * h, rr);
           tmem_ld_wait(rr);
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
@@ -315,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
             p[i + 3] = ex2(x1.y);
           }
         }
-        if (h == 1) tmem_st16(slot + 32, ds0);  // S^T fully read now
+        if (h == 1) tmem_st16(sblk + 32, ds0);  // S^T fully read now
         if (mask_from > 32 * h) {  // only the two sub-tiles on the diagonal
 #pragma unroll
           for (int i = 0; i < 32; ++i)
@@ -325,11 +338,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(p[2 * i], p[2 * i + 1]);
-          tmem_st16(slot + 16 * h, pk);
+          tmem_st16(sblk + 16 * h, pk);
         }
         {
           uint32_t rr[32], pk[16];
-          tmem_ld32(slot + 64 + 32 * h, rr);
+          tmem_ld32(pblk + 32 * h, rr);
           tmem_ld_wait(rr);
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
@@ -347,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
 #pragma unroll
             for (int i = 0; i < 16; ++i) ds0[i] = pk[i];
           } else {
-            tmem_st16(slot + 48, pk);
+            tmem_st16(sblk + 48, pk);
           }
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
@@ -379,9 +392,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
       if (!ok) break;
       tc_fence_after();
       uint32_t lo[32], hi[32];
-      tmem_ld32(tmem + lane_off + 128 * s + 64, lo);
+      const uint32_t dqb = tmem + lane_off + 128 * s + 64 * ((u >> 1) & 1);
+      tmem_ld32(dqb, lo);
       tmem_ld_wait(lo);
-      tmem_ld32(tmem + lane_off + 128 * s + 96, hi);
+      tmem_ld32(dqb + 32, hi);
       tmem_ld_wait(hi);
       tc_fence_before();
       __syncwarp();
