@@ -377,6 +377,30 @@ def main():
             t_b = timed(step, max(1, args.steps // 2))
         roof_bwd = roofline("attn_bwd_kernel", kb.durations_ms(), 10.0, t_b, max(1, args.steps // 2))
 
+    # ---- the saved-O backward: the forward keeps every head's attention
+    # output and the backward reuses it instead of recomputing the attention
+    saved_o = None
+    if mode:
+        o_all = torch.empty(w.S, w.Hq * w.d, dtype=torch.bfloat16, device=dev)
+
+        def step_saved_o():
+            u.attn_fwd(shape, inp["x"], inp["Wq"], inp["Wk"], inp["Wv"], inp["Wo"], out, lse,
+                       ws, inp.get("q_gamma"), inp.get("k_gamma"), o_all)
+            u.attn_bwd(shape, inp["x"], inp["Wq"], inp["Wk"], inp["Wv"], inp["Wo"], inp["dout"],
+                       lse, grads["dx"], grads["dWq"], grads["dWk"], grads["dWv"],
+                       grads["dWo"], ws, inp.get("q_gamma"), inp.get("k_gamma"),
+                       grads["dqg"], grads["dkg"], attn_o=o_all)
+
+        step_saved_o()
+        k = max(1, args.steps // 2)
+        ts = timed(step_saved_o, k)
+        saved_o = {"tflops": round(replica_throughput(flops, k, world, ts), 2),
+                   "ms_per_step": round(1e3 * ts / k, 3), "steps": k,
+                   "extra_bytes": int(o_all.numel() * 2),
+                   "note": "forward keeps the [S, Hq*d] bf16 attention output; the backward "
+                           "skips the per-chunk attention recompute"}
+        del o_all
+
     # ---- chunk sweep: throughput and workspace against chunk_heads
     sweep = []
     if not args.no_sweep:
@@ -416,6 +440,7 @@ def main():
         "peak_workspace_gb": round(peak_ws / 1e9, 4),
         "workspace_gb_planned": round(u.workspace_bytes(shape, mode) / 1e9, 4),
         "chunk_sweep": sweep,
+        "saved_o_backward": saved_o,
         "roofline": roof_bwd if roof_bwd else roof_fwd,
         "roofline_attn_fwd": roof_fwd,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",

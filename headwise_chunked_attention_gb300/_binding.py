@@ -60,6 +60,9 @@ def lib():
         L.upipe_attn_bwd.argtypes = ([ctypes.POINTER(Shape)] + [P] * 17 +
                                      [ctypes.c_size_t, P])
         L.upipe_attn_bwd.restype = ctypes.c_int
+        L.upipe_attn_bwd_saved_o.argtypes = ([ctypes.POINTER(Shape)] + [P] * 18 +
+                                             [ctypes.c_size_t, P])
+        L.upipe_attn_bwd_saved_o.restype = ctypes.c_int
         L.upipe_selftest_wait_timeout.argtypes = [ctypes.c_int, P]
         L.upipe_selftest_wait_timeout.restype = ctypes.c_int
         L.upipe_last_error.argtypes = []
@@ -102,9 +105,10 @@ def _check(rc: int, where: str):
 
 
 def attn_fwd(shape: Shape, x, Wq, Wk, Wv, Wo, out, lse, workspace,
-             q_norm_w=None, k_norm_w=None, attn_o_debug=None, stream=None):
+             q_norm_w=None, k_norm_w=None, attn_o=None, stream=None):
     """upipe_attn_fwd on torch tensors (bf16 inputs, fp32 out/lse, uint8
-    workspace); enqueues on ``stream`` (default: current stream)."""
+    workspace); enqueues on ``stream`` (default: current stream).  ``attn_o``
+    ([S, Hq*d] bf16 or None) receives every head's attention output."""
     bf = torch.bfloat16
     rc = lib().upipe_attn_fwd(
         ctypes.byref(shape), _ptr(x, bf, "x"), _ptr(Wq, bf, "Wq"), _ptr(Wk, bf, "Wk"),
@@ -112,24 +116,32 @@ def attn_fwd(shape: Shape, x, Wq, Wk, Wv, Wo, out, lse, workspace,
         _ptr(k_norm_w, torch.float32, "k_norm_w"), _ptr(out, torch.float32, "out"),
         _ptr(lse, torch.float32, "lse"), _ptr(workspace, None, "workspace"),
         workspace.numel() * workspace.element_size(),
-        _ptr(attn_o_debug, bf, "attn_o_debug"), _stream(stream))
+        _ptr(attn_o, bf, "attn_o"), _stream(stream))
     _check(rc, "upipe_attn_fwd")
 
 
 def attn_bwd(shape: Shape, x, Wq, Wk, Wv, Wo, dout, lse, dx, dWq, dWk, dWv, dWo,
              workspace, q_norm_w=None, k_norm_w=None, dq_norm_w=None,
-             dk_norm_w=None, stream=None):
-    """upipe_attn_bwd on torch tensors."""
+             dk_norm_w=None, attn_o=None, stream=None):
+    """upipe_attn_bwd on torch tensors; with ``attn_o`` (the forward's
+    attention output) upipe_attn_bwd_saved_o, which skips the recompute of
+    the attention forward."""
     bf, f = torch.bfloat16, torch.float32
-    rc = lib().upipe_attn_bwd(
-        ctypes.byref(shape), _ptr(x, bf, "x"), _ptr(Wq, bf, "Wq"), _ptr(Wk, bf, "Wk"),
-        _ptr(Wv, bf, "Wv"), _ptr(Wo, bf, "Wo"), _ptr(q_norm_w, f, "q_norm_w"),
-        _ptr(k_norm_w, f, "k_norm_w"), _ptr(dout, bf, "dout"), _ptr(lse, f, "lse"),
+    head = [ctypes.byref(shape), _ptr(x, bf, "x"), _ptr(Wq, bf, "Wq"), _ptr(Wk, bf, "Wk"),
+            _ptr(Wv, bf, "Wv"), _ptr(Wo, bf, "Wo"), _ptr(q_norm_w, f, "q_norm_w"),
+            _ptr(k_norm_w, f, "k_norm_w"), _ptr(dout, bf, "dout"), _ptr(lse, f, "lse")]
+    if attn_o is not None:
+        fn, where = lib().upipe_attn_bwd_saved_o, "upipe_attn_bwd_saved_o"
+        head.append(_ptr(attn_o, bf, "attn_o"))
+    else:
+        fn, where = lib().upipe_attn_bwd, "upipe_attn_bwd"
+    rc = fn(
+        *head,
         _ptr(dx, f, "dx"), _ptr(dWq, f, "dWq"), _ptr(dWk, f, "dWk"), _ptr(dWv, f, "dWv"),
         _ptr(dWo, f, "dWo"), _ptr(dq_norm_w, f, "dq_norm_w"), _ptr(dk_norm_w, f, "dk_norm_w"),
         _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
         _stream(stream))
-    _check(rc, "upipe_attn_bwd")
+    _check(rc, where)
 
 
 class KernelTimer:

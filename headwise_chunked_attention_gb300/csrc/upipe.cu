@@ -351,7 +351,7 @@ extern "C" int upipe_attn_fwd(const upipe_shape_t* shape, const upipe_bf16* x_,
                               const upipe_bf16* Wq_, const upipe_bf16* Wk_, const upipe_bf16* Wv_,
                               const upipe_bf16* Wo_, const float* q_norm_w, const float* k_norm_w,
                               float* out, float* lse, void* workspace, size_t ws_bytes,
-                              upipe_bf16* attn_o_debug, void* stream) {
+                              upipe_bf16* attn_o, void* stream) {
   Geo g;
   UPIPE_TRY(check_shape(shape, &g));
   const bf16* x = reinterpret_cast<const bf16*>(x_);
@@ -359,10 +359,10 @@ extern "C" int upipe_attn_fwd(const upipe_shape_t* shape, const upipe_bf16* x_,
   const bf16* Wk = reinterpret_cast<const bf16*>(Wk_);
   const bf16* Wv = reinterpret_cast<const bf16*>(Wv_);
   const bf16* Wo = reinterpret_cast<const bf16*>(Wo_);
-  bf16* dbg = reinterpret_cast<bf16*>(attn_o_debug);
+  bf16* o_all = reinterpret_cast<bf16*>(attn_o);
   if (!x || !Wq || !Wk || !Wv || !Wo || !out || !lse || !workspace) return UPIPE_ERR_INVALID_ARG;
   for (const void* p : {(const void*)x, (const void*)Wq, (const void*)Wk, (const void*)Wv,
-                        (const void*)Wo, (const void*)out, (const void*)lse, (const void*)dbg,
+                        (const void*)Wo, (const void*)out, (const void*)lse, (const void*)o_all,
                         (const void*)q_norm_w, (const void*)k_norm_w})
     if (p && !aligned16(p)) return UPIPE_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return UPIPE_ERR_INVALID_ARG;
@@ -399,8 +399,8 @@ extern "C" int upipe_attn_fwd(const upipe_shape_t* shape, const upipe_bf16* x_,
   if (overlap) UPIPE_CUDA(ev.create());
   auto out_gemm = [&](int c, cudaStream_t s, int sms) -> int {
     const int h0 = c * g.ch;
-    const bf16* O = dbg ? dbg + (size_t)h0 * g.d : QO[c & 1];
-    const int ldo = dbg ? g.Hq * g.d : g.ch * g.d;
+    const bf16* O = o_all ? o_all + (size_t)h0 * g.d : QO[c & 1];
+    const int ldo = o_all ? g.Hq * g.d : g.ch * g.d;
     // out (+)= O_c Wo[:, h0*d : (h0+ch)*d]^T  (the chunk's partial result)
     CUtensorMap om, wom;
     UPIPE_MAP(&om, O, g.S, (uint64_t)g.ch * g.d, ldo, 128, 64);
@@ -430,8 +430,8 @@ extern "C" int upipe_attn_fwd(const upipe_shape_t* shape, const upipe_bf16* x_,
       UPIPE_TRY(out_gemm(c - 1, ds->side, side_sms(ds->num_sms)));
       UPIPE_CUDA(cudaEventRecord(ev.out[(c - 1) & 1], ds->side));
     }
-    bf16* O = dbg ? dbg + (size_t)h0 * g.d : Qc;
-    const int ldo = dbg ? g.Hq * g.d : g.ch * g.d;
+    bf16* O = o_all ? o_all + (size_t)h0 * g.d : Qc;
+    const int ldo = o_all ? g.Hq * g.d : g.ch * g.d;
     UPIPE_TRY(attention_chunk(g, ds, st, Qc, K, V, h0, kv0, O, ldo, lse + (size_t)h0 * g.S,
                               flush));
   }
@@ -440,14 +440,20 @@ extern "C" int upipe_attn_fwd(const upipe_shape_t* shape, const upipe_bf16* x_,
   return UPIPE_OK;
 }
 
-extern "C" int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x_,
-                              const upipe_bf16* Wq_, const upipe_bf16* Wk_, const upipe_bf16* Wv_,
-                              const upipe_bf16* Wo_, const float* q_norm_w, const float* k_norm_w,
-                              const upipe_bf16* dout_, const float* lse, float* dx, float* dWq,
-                              float* dWk, float* dWv, float* dWo, float* dq_norm_w,
-                              float* dk_norm_w, void* workspace, size_t ws_bytes, void* stream) {
+// The backward of both entry points.  o_saved: nullptr (recompute each
+// chunk's attention output in the workspace) or the forward's per-head
+// attention output [S, Hq*d] bf16.
+static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
+                         const upipe_bf16* Wq_, const upipe_bf16* Wk_, const upipe_bf16* Wv_,
+                         const upipe_bf16* Wo_, const float* q_norm_w, const float* k_norm_w,
+                         const upipe_bf16* dout_, const float* lse, const upipe_bf16* o_saved_,
+                         float* dx, float* dWq, float* dWk, float* dWv, float* dWo,
+                         float* dq_norm_w, float* dk_norm_w, void* workspace, size_t ws_bytes,
+                         void* stream) {
   Geo g;
   UPIPE_TRY(check_shape(shape, &g));
+  const bf16* o_saved = reinterpret_cast<const bf16*>(o_saved_);
+  if (o_saved && !aligned16(o_saved)) return UPIPE_ERR_INVALID_ARG;
   const bf16* x = reinterpret_cast<const bf16*>(x_);
   const bf16* Wq = reinterpret_cast<const bf16*>(Wq_);
   const bf16* Wk = reinterpret_cast<const bf16*>(Wk_);
@@ -578,7 +584,12 @@ extern "C" int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x_,
       UPIPE_CUDA(cudaMemsetAsync(dK, 0, sizeof(float) * S * g.kvc * d, st));
       UPIPE_CUDA(cudaMemsetAsync(dV, 0, sizeof(float) * S * g.kvc * d, st));
     }
-    UPIPE_TRY(attention_chunk(g, ds, st, Q, K, V, h0, kv0, Ows, g.ch * d, nullptr, flush));
+    // the chunk's attention output: recomputed into the workspace, or the
+    // forward's saved copy
+    const bf16* Oc = o_saved ? o_saved + (size_t)h0 * d : Ows;
+    const int ldo = o_saved ? g.Hq * d : g.ch * d;
+    if (!o_saved)
+      UPIPE_TRY(attention_chunk(g, ds, st, Q, K, V, h0, kv0, Ows, g.ch * d, nullptr, flush));
     // 2. dO_c = dout Wo_c, D = rowsum(dO * O); dWo_c = dout^T O_c
     {
       CUtensorMap wom;
@@ -587,14 +598,14 @@ extern "C" int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x_,
       EpiParams ep{};
       ep.dO = dO;
       ep.ld_do = g.ch * d;
-      ep.O = Ows;
-      ep.ld_o = g.ch * d;
+      ep.O = Oc;
+      ep.ld_o = ldo;
       ep.D = Dv;
       GemmArgs ga{(int)g.S, g.ch * d, g.hidden, 1, d};
       UPIPE_CUDA(launch_gemm(d, false, true, EPI_DO, &dout_k, 1, &wom, 1, ga, ep, ds->err,
                              ds->num_sms, st));
       CUtensorMap om;
-      UPIPE_MAP(&om, Ows, g.S, (uint64_t)g.ch * d, (uint64_t)g.ch * d, 64, 64);
+      UPIPE_MAP(&om, Oc, g.S, (uint64_t)g.ch * d, (uint64_t)ldo, 64, 64);
       EpiParams ep2{};
       ep2.C = dWo + (size_t)h0 * d;
       ep2.ldc = (long long)g.Hq * d;
@@ -700,6 +711,29 @@ extern "C" int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x_,
     UPIPE_TRY(dx_gemm(dxs, ndx));
   }
   return UPIPE_OK;
+}
+
+extern "C" int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x,
+                              const upipe_bf16* Wq, const upipe_bf16* Wk, const upipe_bf16* Wv,
+                              const upipe_bf16* Wo, const float* q_norm_w, const float* k_norm_w,
+                              const upipe_bf16* dout, const float* lse, float* dx, float* dWq,
+                              float* dWk, float* dWv, float* dWo, float* dq_norm_w,
+                              float* dk_norm_w, void* workspace, size_t ws_bytes, void* stream) {
+  return attn_bwd_impl(shape, x, Wq, Wk, Wv, Wo, q_norm_w, k_norm_w, dout, lse, nullptr, dx, dWq,
+                       dWk, dWv, dWo, dq_norm_w, dk_norm_w, workspace, ws_bytes, stream);
+}
+
+extern "C" int upipe_attn_bwd_saved_o(const upipe_shape_t* shape, const upipe_bf16* x,
+                                      const upipe_bf16* Wq, const upipe_bf16* Wk,
+                                      const upipe_bf16* Wv, const upipe_bf16* Wo,
+                                      const float* q_norm_w, const float* k_norm_w,
+                                      const upipe_bf16* dout, const float* lse,
+                                      const upipe_bf16* attn_o, float* dx, float* dWq, float* dWk,
+                                      float* dWv, float* dWo, float* dq_norm_w, float* dk_norm_w,
+                                      void* workspace, size_t ws_bytes, void* stream) {
+  if (!attn_o) return UPIPE_ERR_INVALID_ARG;
+  return attn_bwd_impl(shape, x, Wq, Wk, Wv, Wo, q_norm_w, k_norm_w, dout, lse, attn_o, dx, dWq,
+                       dWk, dWv, dWo, dq_norm_w, dk_norm_w, workspace, ws_bytes, stream);
 }
 
 extern "C" void upipe_profile_attach(int kernel, void* const* start_events,

@@ -92,15 +92,17 @@ size_t upipe_workspace_bytes(const upipe_shape_t* shape, int mode);
  *   out   [S, hidden] fp32, overwritten (the first chunk stores, later chunks
  *         add their Wo-slice partial results)
  *   lse   [Hq, S] fp32 natural-log log-sum-exp of each head's scaled scores
- *   attn_o_debug  NULL, or [S, Hq*d] bf16: receives every head's attention
- *         output o_h at columns h*d (for chunk-invariance checks)
+ *   attn_o  NULL, or [S, Hq*d] bf16: receives every head's attention output
+ *         o_h at columns h*d.  Keep it for upipe_attn_bwd_saved_o (the
+ *         backward then skips recomputing the attention forward), or use it
+ *         to check that o_h does not depend on chunk_heads.
  *   workspace / ws_bytes: device buffer of at least
  *         upipe_workspace_bytes(shape, 0) bytes, 256-byte aligned
  * Returns UPIPE_OK or an error code (nothing launched on error). */
 int upipe_attn_fwd(const upipe_shape_t* shape, const upipe_bf16* x, const upipe_bf16* Wq,
                    const upipe_bf16* Wk, const upipe_bf16* Wv, const upipe_bf16* Wo,
                    const float* q_norm_w, const float* k_norm_w, float* out, float* lse,
-                   void* workspace, size_t ws_bytes, upipe_bf16* attn_o_debug, void* stream);
+                   void* workspace, size_t ws_bytes, upipe_bf16* attn_o, void* stream);
 
 /* Backward of the layer for L = sum(out * dout), chunk by chunk, recomputing
  * each chunk's Q/K/V and attention output in the reused workspace (activation
@@ -120,13 +122,33 @@ int upipe_attn_bwd(const upipe_shape_t* shape, const upipe_bf16* x, const upipe_
                    float* dq_norm_w, float* dk_norm_w, void* workspace, size_t ws_bytes,
                    void* stream);
 
+/* The same backward, with the attention output saved by the forward instead
+ * of recomputed.  upipe_attn_bwd recomputes every chunk's attention forward
+ * (4*d FLOPs per causal pair and head, about 30% of the backward's work) so
+ * that only the chunk-sized workspace holds activations; a caller that can
+ * keep the full attention output of the layer (S * Hq * d bf16, e.g. 1 GiB for
+ * 4 heads of d = 128 over 1M tokens) passes it here and saves that work.
+ * This is the memory / throughput trade of the chunk-size choice
+ * (memeeeeeex.com "Results": larger chunks use more memory and run slightly
+ * faster), taken one step further.
+ *   attn_o  [S, Hq*d] bf16, as written by upipe_attn_fwd(..., attn_o, ...) on
+ *           the same inputs (required: NULL is UPIPE_ERR_INVALID_ARG)
+ * Every other argument, the workspace size and the results are those of
+ * upipe_attn_bwd. */
+int upipe_attn_bwd_saved_o(const upipe_shape_t* shape, const upipe_bf16* x, const upipe_bf16* Wq,
+                           const upipe_bf16* Wk, const upipe_bf16* Wv, const upipe_bf16* Wo,
+                           const float* q_norm_w, const float* k_norm_w, const upipe_bf16* dout,
+                           const float* lse, const upipe_bf16* attn_o, float* dx, float* dWq,
+                           float* dWk, float* dWv, float* dWo, float* dq_norm_w,
+                           float* dk_norm_w, void* workspace, size_t ws_bytes, void* stream);
+
 /* Forward for callers that cannot allocate device memory: code running where
  * cudaMalloc is not allowed or not wanted (inside a graph-building or
  * real-time section, under an external allocator that forbids extra device
  * allocations, or in a plugin that only receives its inputs' and outputs'
  * pointers).  The paper has no counterpart; this is a convenience of the
  * library.  Same arguments and results as upipe_attn_fwd minus the workspace
- * and attn_o_debug: the workspace is a static device array of
+ * and attn_o: the workspace is a static device array of
  * UPIPE_STATIC_SCRATCH_BYTES (64 MiB) compiled into the library, which every
  * GPU that loads the library holds until the process exits.
  *  - Shapes whose upipe_workspace_bytes(shape, 0) exceeds

@@ -111,3 +111,18 @@ def test_binding_marshals_error_codes(u):
     x = torch.zeros(4, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         u.attn_fwd(u.Shape.of(w, 2), x, x, x, x, x, x, x, x)   # CPU tensors refused
+
+
+def test_saved_o_backward_validates_before_any_launch(u):
+    # upipe_attn_bwd_saved_o requires the forward's attention output and
+    # validates it, like every other argument, before the first launch
+    L = u.lib()
+    w = WORKLOADS["tiny-s2048"]
+    sh = u.Shape.of(w, 2)
+    p = [0x100000 + 0x1000 * i for i in range(20)]
+    args = lambda o: (ctypes.byref(sh), *p[:5], None, None, p[5], p[6], o,
+                      *p[7:12], None, None, p[12], 1 << 40, None)
+    assert L.upipe_attn_bwd_saved_o(*args(None)) == 1       # NULL attn_o
+    assert L.upipe_attn_bwd_saved_o(*args(p[13] + 8)) == 1  # misaligned attn_o
+    bad = u.Shape.of(w, 3)                                   # 3 does not divide Hq
+    assert L.upipe_attn_bwd_saved_o(ctypes.byref(bad), *args(p[13])[1:]) == 1

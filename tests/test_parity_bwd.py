@@ -1,5 +1,7 @@
 """GPU backward parity: upipe_attn_bwd (chunked, recomputing Q/K/V and the
-attention output per chunk) against the float64 chain-rule oracle."""
+attention output per chunk) and upipe_attn_bwd_saved_o (the forward's saved
+attention output instead of its recompute) against the float64 chain-rule
+oracle."""
 import numpy as np
 import pytest
 import torch
@@ -11,7 +13,7 @@ from tests._util import f64, assert_close
 pytestmark = pytest.mark.gpu
 
 
-def run_fwd_bwd(w, ch, inp):
+def run_fwd_bwd(w, ch, inp, saved_o=False):
     import headwise_chunked_attention_gb300 as u
     dev = "cuda"
     t = {k: v.to(dev) for k, v in inp.items()}
@@ -19,8 +21,11 @@ def run_fwd_bwd(w, ch, inp):
     out = torch.empty(w.S, w.hidden, device=dev)
     lse = torch.empty(w.Hq, w.S, device=dev)
     ws = torch.empty(u.workspace_bytes(sh, 1), dtype=torch.uint8, device=dev)
+    o = torch.empty(w.S, w.Hq * w.d, dtype=torch.bfloat16, device=dev) if saved_o else None
     u.attn_fwd(sh, t["x"], t["Wq"], t["Wk"], t["Wv"], t["Wo"], out, lse, ws,
-               t.get("q_gamma"), t.get("k_gamma"))
+               t.get("q_gamma"), t.get("k_gamma"), o)
+    if saved_o:   # the backward must not depend on what the forward left in ws
+        ws.fill_(0xFF)
     g = {n: torch.full(t[src].shape, float("nan"), device=dev)
          for n, src in [("dx", "x"), ("dWq", "Wq"), ("dWk", "Wk"), ("dWv", "Wv"),
                         ("dWo", "Wo")]}
@@ -28,7 +33,7 @@ def run_fwd_bwd(w, ch, inp):
     dkg = torch.full((w.d,), float("nan"), device=dev) if w.qk_norm else None
     u.attn_bwd(sh, t["x"], t["Wq"], t["Wk"], t["Wv"], t["Wo"], t["dout"], lse,
                g["dx"], g["dWq"], g["dWk"], g["dWv"], g["dWo"], ws,
-               t.get("q_gamma"), t.get("k_gamma"), dqg, dkg)
+               t.get("q_gamma"), t.get("k_gamma"), dqg, dkg, attn_o=o)
     torch.cuda.synchronize()
     assert u.last_error() == 0
     g["dq_gamma"], g["dk_gamma"] = dqg, dkg
@@ -65,3 +70,24 @@ def test_backward_matches_oracle(w, chs):
         if w.qk_norm:
             for name in ("dq_gamma", "dk_gamma"):
                 assert_close(f64(g[name]), ref[name], f"{name} ch={ch}")
+
+
+@pytest.mark.parametrize("w,chs", [CASES[1], CASES[2]],
+                         ids=lambda c: getattr(c, "name", str(c)))
+def test_backward_with_saved_attention_output(w, chs):
+    # the saved-O backward computes the same gradients: against the oracle
+    # with the same bound, and against the recomputing backward (whose
+    # recomputed O equals the forward's bit for bit; only the order of fp32
+    # reductions differs) to within a much tighter bound
+    inp = make_inputs(w, seed=0, with_grad=True, norm_gains="random")
+    ref = oracle_bwd(w, inp)
+    for ch in chs:
+        g = run_fwd_bwd(w, ch, inp, saved_o=True)
+        r = run_fwd_bwd(w, ch, inp)
+        names = ["dx", "dWq", "dWk", "dWv", "dWo"] + (["dq_gamma", "dk_gamma"]
+                                                      if w.qk_norm else [])
+        for name in names:
+            assert_close(f64(g[name]), ref[name], f"saved-O {name} ch={ch}")
+            a, b = f64(g[name]), f64(r[name])
+            scale = np.sqrt(np.mean(b ** 2)) + 1e-30
+            assert np.max(np.abs(a - b)) / scale < 1e-4, f"saved-O vs recompute {name} ch={ch}"
