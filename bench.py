@@ -337,19 +337,70 @@ def main():
         t_events = timed(step, args.steps)
     durs = kt.durations_ms()
 
-    # ---- end to end: pinned host x -> device, layer, out -> pinned host
-    x_host = inp["x"].cpu().pin_memory()
-    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    # ---- end to end through the public API with host buffers: every step
+    # uploads its inputs (x; and dout for the backward) from pinned host
+    # memory and downloads its result (out; dx for the backward).  Steps are
+    # pipelined: step i+1's upload and step i-1's download run on two copy
+    # streams while step i computes, on double-buffered device copies when
+    # the device has room for them (else one set, and the copies serialise).
+    in_names = ["x"] + (["dout"] if mode else [])
+    res0 = grads["dx"] if mode else out
+    hosts = {n: inp[n].cpu().pin_memory() for n in in_names}
+    res_host = torch.empty(res0.shape, dtype=res0.dtype).pin_memory()
+    extra = sum(inp[n].numel() * inp[n].element_size() for n in in_names) + \
+        res0.numel() * res0.element_size()
+    nbuf = 2 if extra + (8 << 30) < torch.cuda.mem_get_info(dev)[0] else 1
+    dbufs = [{n: inp[n] for n in in_names}] + \
+        [{n: torch.empty_like(inp[n]) for n in in_names} for _ in range(nbuf - 1)]
+    rbufs = [res0] + [torch.empty_like(res0) for _ in range(nbuf - 1)]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = {k: [torch.cuda.Event() for _ in range(nbuf)] for k in ("in", "done", "out")}
 
-    def e2e_step():
-        inp["x"].copy_(x_host, non_blocking=True)
-        step()
-        out_host.copy_(out, non_blocking=True)
+    def step_io(b):
+        db, rb = dbufs[b], rbufs[b]
+        o_ = rb if not mode else out
+        u.attn_fwd(shape, db["x"], inp["Wq"], inp["Wk"], inp["Wv"], inp["Wo"], o_, lse, ws,
+                   inp.get("q_gamma"), inp.get("k_gamma"))
+        if mode:
+            u.attn_bwd(shape, db["x"], inp["Wq"], inp["Wk"], inp["Wv"], inp["Wo"], db["dout"],
+                       lse, rb, grads["dWq"], grads["dWk"], grads["dWv"], grads["dWo"], ws,
+                       inp.get("q_gamma"), inp.get("k_gamma"), grads["dqg"], grads["dkg"])
 
-    for _ in range(2):
-        e2e_step()
-    t_e2e = timed(e2e_step, max(1, args.steps // 2))
-    e2e_value = replica_throughput(flops, max(1, args.steps // 2), world, t_e2e)
+    def e2e_run(k):
+        main = torch.cuda.current_stream(dev)
+        s_in.wait_stream(main)
+        s_out.wait_stream(main)
+
+        def upload(i):
+            b = i % nbuf
+            with torch.cuda.stream(s_in):
+                if i >= nbuf:
+                    s_in.wait_event(ev["done"][b])   # step i - nbuf is done with it
+                for n in in_names:
+                    dbufs[b][n].copy_(hosts[n], non_blocking=True)
+                ev["in"][b].record(s_in)
+
+        upload(0)
+        for i in range(k):
+            b = i % nbuf
+            if i + 1 < k:
+                upload(i + 1)
+            main.wait_event(ev["in"][b])
+            if i >= nbuf:
+                main.wait_event(ev["out"][b])        # its result has been downloaded
+            step_io(b)
+            ev["done"][b].record(main)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev["done"][b])
+                res_host.copy_(rbufs[b], non_blocking=True)
+                ev["out"][b].record(s_out)
+        main.wait_stream(s_out)
+
+    e2e_run(2)
+    k_e2e = max(2, args.steps)
+    t_e2e = timed(lambda: e2e_run(k_e2e), 1)
+    e2e_value = replica_throughput(flops, k_e2e, world, t_e2e)
+    del dbufs, rbufs
 
     # ---- roofline of the attention kernels (algorithmic FLOPs per launch over
     # the live CUDA-event launch time)
@@ -444,8 +495,10 @@ def main():
         "roofline": roof_bwd if roof_bwd else roof_fwd,
         "roofline_attn_fwd": roof_fwd,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": int(x_host.numel() * 2),
-                "d2h_bytes_per_step": int(out_host.numel() * 4)},
+                "h2d_bytes_per_step": int(sum(h.numel() * h.element_size()
+                                              for h in hosts.values())),
+                "d2h_bytes_per_step": int(res_host.numel() * res_host.element_size()),
+                "steps": k_e2e, "pipelined_buffers": nbuf},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
