@@ -123,7 +123,25 @@ class Clocks:
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+        # nvidia-smi takes a moment to start: wait for its first sample, and
+        # keep only the samples taken after this point (the timed region)
+        self.skip = 0
+        if self.proc is not None:
+            t0 = time.time()
+            while time.time() - t0 < 5 and self.proc.poll() is None:
+                n = self._nlines()
+                if n > 0:
+                    self.skip = n
+                    break
+                time.sleep(0.02)
         return self
+
+    def _nlines(self):
+        self.f.flush()
+        try:
+            return sum(1 for l in open(self.f.name) if l.strip())
+        except OSError:
+            return 0
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -139,6 +157,8 @@ class Clocks:
         self.f.flush()
         rows = [l.split(",") for l in open(self.f.name).read().strip().splitlines() if l]
         os.unlink(self.f.name)
+        if len(rows) > self.skip:
+            rows = rows[self.skip:]
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
@@ -160,10 +180,13 @@ class Clocks:
 
 # ---------------------------------------------------------------- oracle --
 
-def oracle_sample(w, inp, rows_per_head=64, groups=1):
+def oracle_sample(w, inp, rows_per_head=64, groups=1, target_s=None):
     """Time the float64 oracle on a bounded sample of the workload: the full
-    K/V projection of ``groups`` kv heads plus ``rows_per_head`` sampled query
-    rows of each of their query heads.  Returns (TFLOP/s, seconds, flops)."""
+    K/V projection of ``groups`` kv heads plus sampled query rows of each of
+    their query heads (attention over all earlier keys).  Without
+    ``target_s``: ``rows_per_head`` rows.  With it: seeded-shuffled batches of
+    256 rows until ``target_s`` seconds of CPU work have been spent (at most
+    16384 rows).  Returns (TFLOP/s, seconds, flops, rows per head)."""
     import numpy as np
     import torch
 
@@ -172,21 +195,34 @@ def oracle_sample(w, inp, rows_per_head=64, groups=1):
     a = {k: v.to("cpu", torch.float64).numpy() for k, v in inp.items() if k != "x"}
     xb = inp["x"]
     x_src = lambda lo, hi: xb[lo:hi].to("cpu", torch.float64).numpy()
-    rows = np.asarray(sample_rows(w.S, rows_per_head))
     g = w.Hq // w.Hkv
     t0 = time.perf_counter()
     flops = 0.0
+    kv = []
     for kvh in range(groups):
-        K, V = O.project_kv(x_src, a["Wk"], a["Wv"], w, kvh, w.S, a.get("k_gamma"))
+        kv.append(O.project_kv(x_src, a["Wk"], a["Wv"], w, kvh, w.S, a.get("k_gamma")))
         flops += 2 * 2.0 * w.S * w.hidden * w.d
+    if target_s is None:
+        rows_all, batch = np.asarray(sample_rows(w.S, rows_per_head)), None
+    else:
+        rows_all = np.random.default_rng(0).permutation(
+            np.asarray(sample_rows(w.S, min(w.S, 16384))))
+        batch = 256
+    done = 0
+    for b0 in range(0, len(rows_all), batch or len(rows_all)):
+        rows = np.sort(rows_all[b0:b0 + (batch or len(rows_all))])
         xq = np.concatenate([x_src(int(r), int(r) + 1) for r in rows])
-        for h in range(kvh * g, (kvh + 1) * g):
-            q = O.attention_layer._qk_post(xq @ a["Wq"][h * w.d:(h + 1) * w.d].T, rows, w,
-                                           a.get("q_gamma"), None)
-            O.causal_attention(q, K, V, rows)
-            flops += 2.0 * len(rows) * w.hidden * w.d + 4.0 * w.d * float(np.sum(rows + 1))
+        for kvh, (K, V) in enumerate(kv):
+            for h in range(kvh * g, (kvh + 1) * g):
+                q = O.attention_layer._qk_post(xq @ a["Wq"][h * w.d:(h + 1) * w.d].T, rows, w,
+                                               a.get("q_gamma"), None)
+                O.causal_attention(q, K, V, rows)
+                flops += 2.0 * len(rows) * w.hidden * w.d + 4.0 * w.d * float(np.sum(rows + 1))
+        done += len(rows)
+        if target_s is not None and time.perf_counter() - t0 >= target_s:
+            break
     dt = time.perf_counter() - t0
-    return flops / dt / 1e12, dt, flops
+    return flops / dt / 1e12, dt, flops, done
 
 
 def cores():
@@ -212,7 +248,7 @@ def run_reference(args, w, ch):
         make_inputs(w, seed=0, device="cuda")
     times, tf = [], []
     for i in range(args.warmup + args.steps):
-        v, dt, fl = oracle_sample(w, inp)
+        v, dt, fl, _ = oracle_sample(w, inp)
         if i >= args.warmup:
             times.append(dt)
             tf.append(v)
@@ -234,7 +270,7 @@ def run_reference(args, w, ch):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
@@ -504,13 +540,14 @@ def main():
     }
     if world == 1 and not args.no_cpu:
         groups = min(w.Hkv, 4)
-        v, dt, fl = oracle_sample(w, {k: v for k, v in inp.items()}, rows_per_head=256,
-                                  groups=groups)
+        v, dt, fl, nrows = oracle_sample(w, {k: v for k, v in inp.items()}, groups=groups,
+                                         target_s=12.0)
         line["cpu_baseline"] = {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores(),
                                 "kind": "oracle", "seconds": round(dt, 2),
                                 "sample": f"float64 oracle: full K/V projection of {groups} kv "
-                                          "head(s) + 256 sampled query rows of each of their "
-                                          "query heads (attention over all earlier keys)"}
+                                          f"head(s) + {nrows} seeded random query rows of each "
+                                          "of their query heads (attention over all earlier "
+                                          "keys), batches of 256 rows until 12 s of CPU work"}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/upipe.h"
+
 namespace upipe {
 
 using bf16 = __nv_bfloat16;
@@ -166,6 +168,13 @@ cudaError_t launch_qk_bwd(const QkBwdArgs& a, cudaStream_t stream);
 // [S, ld_out] each, for ``cols`` columns: hi + lo carries ~16 significant bits.
 cudaError_t launch_f32_to_bf16x2(const float* in, int ld_in, bf16* hi, bf16* lo, int ld_out,
                                  long long S, int cols, cudaStream_t stream);
+
+// upipe_attn_fwd with every launch on the caller's stream: no side stream,
+// no events (the static-scratch entry point, which must create nothing).
+int attn_fwd_unforked(const upipe_shape_t* shape, const upipe_bf16* x, const upipe_bf16* Wq,
+                      const upipe_bf16* Wk, const upipe_bf16* Wv, const upipe_bf16* Wo,
+                      const float* q_norm_w, const float* k_norm_w, float* out, float* lse,
+                      void* workspace, size_t ws_bytes, void* stream);
 
 // One-CTA kernel whose waits expire after limit_ns (failure-detection test).
 cudaError_t launch_selftest_wait(int* err, unsigned long long limit_ns, cudaStream_t stream);

@@ -1,12 +1,14 @@
 // upipe_attn_fwd_noalloc: the layer forward for callers that cannot allocate
 // device memory (see include/upipe.h).  Its workspace is one file-scope
-// static __device__ array of UPIPE_STATIC_SCRATCH_BYTES; the existing forward
-// entry point runs on it unchanged.
+// static __device__ array of UPIPE_STATIC_SCRATCH_BYTES; the layer forward
+// runs on it with every launch on the caller's stream (it creates no events
+// and uses no side stream).
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "../../include/upipe.h"
+#include "internal.h"
 
 namespace {
 
@@ -42,14 +44,14 @@ extern "C" int upipe_attn_fwd_noalloc(const upipe_shape_t* shape, const upipe_bf
                                       float* lse, void* stream) {
   const size_t need = upipe_workspace_bytes(shape, 0);
   if (need == 0)  // invalid or unsupported shape: report its own code, launch nothing
-    return upipe_attn_fwd(shape, x, Wq, Wk, Wv, Wo, q_norm_w, k_norm_w, out, lse, nullptr, 0,
-                          nullptr, stream);
+    return upipe::attn_fwd_unforked(shape, x, Wq, Wk, Wv, Wo, q_norm_w, k_norm_w, out, lse,
+                                    nullptr, 0, stream);
   if (need > (size_t)UPIPE_STATIC_SCRATCH_BYTES) return UPIPE_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;
   const int rc = static_scratch(&scratch);
   if (rc != UPIPE_OK) return rc;
   // Nothing in the scratch has to start at zero: every byte the forward reads
   // is written earlier in the same call.
-  return upipe_attn_fwd(shape, x, Wq, Wk, Wv, Wo, q_norm_w, k_norm_w, out, lse, scratch,
-                        (size_t)UPIPE_STATIC_SCRATCH_BYTES, nullptr, stream);
+  return upipe::attn_fwd_unforked(shape, x, Wq, Wk, Wv, Wo, q_norm_w, k_norm_w, out, lse, scratch,
+                                  (size_t)UPIPE_STATIC_SCRATCH_BYTES, stream);
 }

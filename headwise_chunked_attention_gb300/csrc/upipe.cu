@@ -39,7 +39,9 @@ struct DeviceState {
   int num_sms = 0;
   int* err = nullptr;
   // highest-priority stream on which the forward runs each chunk's Wo-slice
-  // accumulate beside the next chunk's attention (nullptr: not available)
+  // accumulate beside the next chunk's attention; created by the first
+  // forward that forks (nullptr: not yet, or not available)
+  bool side_tried = false;
   cudaStream_t side = nullptr;
 };
 
@@ -77,16 +79,26 @@ int device_state(DeviceState** out) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return UPIPE_ERR_CUDA;
     s.err = static_cast<int*>(p);
-    int least = 0, greatest = 0;
-    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
-        cudaStreamCreateWithPriority(&s.side, cudaStreamNonBlocking, greatest) != cudaSuccess) {
-      s.side = nullptr;
-      cudaGetLastError();
-    }
     s.ready = true;
   }
   *out = &s;
   return UPIPE_OK;
+}
+
+// The side stream of the current device (set up by device_state), created on
+// first use; nullptr if it cannot be created (the forward then runs serially).
+cudaStream_t side_stream(DeviceState* s) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!s->side_tried) {
+    s->side_tried = true;
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
+        cudaStreamCreateWithPriority(&s->side, cudaStreamNonBlocking, greatest) != cudaSuccess) {
+      s->side = nullptr;
+      cudaGetLastError();
+    }
+  }
+  return s->side;
 }
 
 // ---------------------------------------------------------- tensor maps --
@@ -347,11 +359,15 @@ extern "C" size_t upipe_workspace_bytes(const upipe_shape_t* shape, int mode) {
   return plan(g, mode).total;
 }
 
-extern "C" int upipe_attn_fwd(const upipe_shape_t* shape, const upipe_bf16* x_,
-                              const upipe_bf16* Wq_, const upipe_bf16* Wk_, const upipe_bf16* Wv_,
-                              const upipe_bf16* Wo_, const float* q_norm_w, const float* k_norm_w,
-                              float* out, float* lse, void* workspace, size_t ws_bytes,
-                              upipe_bf16* attn_o, void* stream) {
+// The forward of both entry points.  fork: run each chunk's Wo-slice
+// accumulate on the device's side stream beside the next chunk's attention
+// (three events per call); false keeps every launch on the caller's stream
+// and creates nothing.
+static int attn_fwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
+                         const upipe_bf16* Wq_, const upipe_bf16* Wk_, const upipe_bf16* Wv_,
+                         const upipe_bf16* Wo_, const float* q_norm_w, const float* k_norm_w,
+                         float* out, float* lse, void* workspace, size_t ws_bytes,
+                         upipe_bf16* attn_o, void* stream, bool fork) {
   Geo g;
   UPIPE_TRY(check_shape(shape, &g));
   const bf16* x = reinterpret_cast<const bf16*>(x_);
@@ -392,9 +408,12 @@ extern "C" int upipe_attn_fwd(const upipe_shape_t* shape, const upipe_bf16* x_,
   // of chunk c - 1 runs on the side stream with a few SMs, after the projection
   // of chunk c and beside its attention; the projection of chunk c + 1 waits
   // for it, since it overwrites that buffer.  The last accumulate runs on the
-  // caller's stream with every SM, after the side stream's work.
+  // caller's stream with every SM, after the side stream's work.  Without the
+  // side stream each accumulate follows its chunk's attention on the caller's
+  // stream.
   bf16* QO[2] = {Q, Ows};
-  const bool overlap = g.nchunks > 1 && ds->side != nullptr;
+  cudaStream_t side = (fork && g.nchunks > 1) ? side_stream(ds) : nullptr;
+  const bool overlap = side != nullptr;
   Events ev;
   if (overlap) UPIPE_CUDA(ev.create());
   auto out_gemm = [&](int c, cudaStream_t s, int sms) -> int {
@@ -426,19 +445,39 @@ extern "C" int upipe_attn_fwd(const upipe_shape_t* shape, const upipe_bf16* x_,
                             nullptr));
     if (overlap && c >= 1) {
       UPIPE_CUDA(cudaEventRecord(ev.proj, st));
-      UPIPE_CUDA(cudaStreamWaitEvent(ds->side, ev.proj, 0));
-      UPIPE_TRY(out_gemm(c - 1, ds->side, side_sms(ds->num_sms)));
-      UPIPE_CUDA(cudaEventRecord(ev.out[(c - 1) & 1], ds->side));
+      UPIPE_CUDA(cudaStreamWaitEvent(side, ev.proj, 0));
+      UPIPE_TRY(out_gemm(c - 1, side, side_sms(ds->num_sms)));
+      UPIPE_CUDA(cudaEventRecord(ev.out[(c - 1) & 1], side));
     }
     bf16* O = o_all ? o_all + (size_t)h0 * g.d : Qc;
     const int ldo = o_all ? g.Hq * g.d : g.ch * g.d;
     UPIPE_TRY(attention_chunk(g, ds, st, Qc, K, V, h0, kv0, O, ldo, lse + (size_t)h0 * g.S,
                               flush));
+    if (!overlap && c + 1 < g.nchunks) UPIPE_TRY(out_gemm(c, st, ds->num_sms));
   }
   if (overlap) UPIPE_CUDA(cudaStreamWaitEvent(st, ev.out[(g.nchunks - 2) & 1], 0));
   UPIPE_TRY(out_gemm(g.nchunks - 1, st, ds->num_sms));
   return UPIPE_OK;
 }
+
+extern "C" int upipe_attn_fwd(const upipe_shape_t* shape, const upipe_bf16* x,
+                              const upipe_bf16* Wq, const upipe_bf16* Wk, const upipe_bf16* Wv,
+                              const upipe_bf16* Wo, const float* q_norm_w, const float* k_norm_w,
+                              float* out, float* lse, void* workspace, size_t ws_bytes,
+                              upipe_bf16* attn_o, void* stream) {
+  return attn_fwd_impl(shape, x, Wq, Wk, Wv, Wo, q_norm_w, k_norm_w, out, lse, workspace,
+                       ws_bytes, attn_o, stream, true);
+}
+
+namespace upipe {
+int attn_fwd_unforked(const upipe_shape_t* shape, const upipe_bf16* x, const upipe_bf16* Wq,
+                      const upipe_bf16* Wk, const upipe_bf16* Wv, const upipe_bf16* Wo,
+                      const float* q_norm_w, const float* k_norm_w, float* out, float* lse,
+                      void* workspace, size_t ws_bytes, void* stream) {
+  return attn_fwd_impl(shape, x, Wq, Wk, Wv, Wo, q_norm_w, k_norm_w, out, lse, workspace,
+                       ws_bytes, nullptr, stream, false);
+}
+}  // namespace upipe
 
 // The backward of both entry points.  o_saved: nullptr (recompute each
 // chunk's attention output in the workspace) or the forward's per-head

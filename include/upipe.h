@@ -25,14 +25,15 @@
  *  - Pointers named x, W*, out, lse, d*, workspace are DEVICE pointers of the
  *    current CUDA device; every buffer must be 16-byte aligned.
  *  - ``stream`` is a cudaStream_t (NULL = legacy default stream).  Calls only
- *    enqueue work and return; nothing is synchronised.  The forward may fork
- *    part of its work onto a library-owned high-priority stream of the device
- *    and joins it back with events before it returns, so its work is ordered
- *    like one launch sequence on ``stream``.  Two calls in flight at once
- *    must not share a workspace.
+ *    enqueue work and return; nothing is synchronised.  With more than one
+ *    chunk, upipe_attn_fwd forks part of its work onto a library-owned
+ *    high-priority stream of the device (created by the first such call) and
+ *    joins it back with events before it returns, so its work is ordered like
+ *    one launch sequence on ``stream``.  Two calls in flight at once must not
+ *    share a workspace.
  *  - Ownership: the caller owns every buffer.  The library allocates no device
- *    or host memory of its own (it creates only the one stream per device named
- *    above and three events per forward call); all temporaries live in
+ *    or host memory of its own (upipe_attn_fwd creates only the one stream per
+ *    device named above and three events per call); all temporaries live in
  *    ``workspace``.
  *  - Errors: every argument is validated on the host before the first launch;
  *    a failed check returns a code and launches nothing.  A device-side wait
@@ -157,6 +158,8 @@ int upipe_attn_bwd_saved_o(const upipe_shape_t* shape, const upipe_bf16* x, cons
  *  - The first call on each device looks up the array's device address (with
  *    that device current); make that first call before any stream capture.
  *  - Allocates nothing: no cudaMalloc/cudaFree or allocating library call.
+ *    Unlike upipe_attn_fwd it keeps every launch on ``stream``: it uses no
+ *    side stream and creates no events.
  *  - Every call shares the one array and leaves its contents behind; nothing
  *    in it needs to start at zero.  Calls that overlap on the GPU (different
  *    streams, or host threads racing) race on the array: serialise them. */
