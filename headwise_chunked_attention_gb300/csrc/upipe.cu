@@ -278,6 +278,30 @@ struct Events {
   }
 };
 
+// Split-K partitions of a weight-gradient GEMM (K = S tokens, M x N output in
+// 128 x bn tiles): about one partition per 8192 tokens (at most 64), moved
+// within a factor of two of that to the count whose tiles fill the last wave
+// of SMs best (ties: the count nearest the base), keeping >= 1024 tokens per
+// partition.
+int wgrad_splits(int64_t S, int M, int N, int bn, int sms) {
+  const long long mn = (long long)((M + 127) / 128) * (N / bn);
+  const int base = (int)std::max<int64_t>(1, std::min<int64_t>(64, (S + 8191) / 8192));
+  int best = base;
+  double best_eff = -1.0;
+  for (int k = std::max(1, base / 2); k <= std::min(64, 2 * base); ++k) {
+    if (k > 1 && S / k < 1024) continue;
+    const long long tiles = mn * k;
+    const long long waves = (tiles + sms - 1) / sms;
+    const double eff = (double)tiles / (double)(waves * sms);
+    if (eff > best_eff + 1e-9 ||
+        (eff > best_eff - 1e-9 && std::abs(k - base) < std::abs(best - base))) {
+      best = k;
+      best_eff = eff;
+    }
+  }
+  return best;
+}
+
 // SMs given to a Wo-slice accumulate that runs beside an attention launch: it
 // is bound by HBM (a read-modify-write of the fp32 layer output), which a
 // fifth of the SMs can nearly saturate, and the rest keep the tensor cores of
@@ -555,7 +579,6 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
   UPIPE_MAP(&dout_k, dout, g.S, g.hidden, g.hidden, 128, 64);  // A of dO = dout Wo_c
   UPIPE_MAP(&dout_mn, dout, g.S, g.hidden, g.hidden, 64, 64);  // A of dWo = dout^T O
   const int dx_bn = (g.hidden % 256 == 0) ? 256 : 128;
-  const int ksplit_w = std::max(1, std::min(64, (int)((S + 8191) / 8192)));
   bool dx_started = false;
 
   // dx (+)= sum_s dA_s W_s: one GEMM whose K range runs through the chunk's
@@ -605,7 +628,8 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
     EpiParams ep{};
     ep.C = dW;
     ep.ldc = g.hidden;
-    GemmArgs ga{ncols, g.hidden, (int)g.S, ksplit_w, d};
+    GemmArgs ga{ncols, g.hidden, (int)g.S, wgrad_splits(g.S, ncols, g.hidden, 128, ds->num_sms),
+                d};
     UPIPE_CUDA(launch_gemm(128, true, true, EPI_F32_ATOMIC, &am, 1, &x_mn, 1, ga, ep, ds->err,
                            ds->num_sms, st));
     return UPIPE_OK;
@@ -648,8 +672,9 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
       EpiParams ep2{};
       ep2.C = dWo + (size_t)h0 * d;
       ep2.ldc = (long long)g.Hq * d;
-      GemmArgs gb{g.hidden, g.ch * d, (int)g.S, ksplit_w, d};
       const int bn = (g.ch * d) % 128 == 0 ? 128 : 64;
+      GemmArgs gb{g.hidden, g.ch * d, (int)g.S,
+                  wgrad_splits(g.S, g.hidden, g.ch * d, bn, ds->num_sms), d};
       UPIPE_CUDA(launch_gemm(bn, true, true, EPI_F32_ATOMIC, &dout_mn, 1, &om, 1, gb, ep2, ds->err,
                              ds->num_sms, st));
     }
