@@ -19,9 +19,11 @@ namespace upipe {
 // so the angle is split: pos = hi + lo with hi = pos & ~1023, lo = pos & 1023;
 // hi[b][i] = (cos, sin)(b * 1024 * w_i), lo[p][i] = (cos, sin)(p * w_i), both
 // evaluated in float64 and rounded once; the consumer combines them with one
-// complex multiplication (error ~1e-7).
-__global__ void rope_table_kernel(float2* __restrict__ hi, float2* __restrict__ lo, long long nhi,
-                                  int half, double theta) {
+// complex multiplication (error ~1e-7).  lo is also written transposed,
+// lo_t[i][p], for consumers whose threads walk positions (one row each).
+__global__ void rope_table_kernel(float2* __restrict__ hi, float2* __restrict__ lo,
+                                  float2* __restrict__ lo_t, long long nhi, int half,
+                                  double theta) {
   const long long total = (nhi + 1024) * half;
   for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
        t += (long long)gridDim.x * blockDim.x) {
@@ -40,16 +42,17 @@ __global__ void rope_table_kernel(float2* __restrict__ hi, float2* __restrict__ 
     double s, c;
     sincos(ang, &s, &c);
     *dst = make_float2((float)c, (float)s);
+    if (row >= nhi) lo_t[(long long)i * 1024 + (row - nhi)] = make_float2((float)c, (float)s);
   }
 }
 
-cudaError_t launch_rope_table(float2* hi, float2* lo, long long S, int d, double theta,
-                              cudaStream_t stream) {
+cudaError_t launch_rope_table(float2* hi, float2* lo, float2* lo_t, long long S, int d,
+                              double theta, cudaStream_t stream) {
   const long long nhi = (S >> 10) + 1;
   const long long total = (nhi + 1024) * (d / 2);
   const int threads = 256;
   const int blocks = (int)std::min<long long>((total + threads - 1) / threads, 4096);
-  rope_table_kernel<<<blocks, threads, 0, stream>>>(hi, lo, nhi, d / 2, theta);
+  rope_table_kernel<<<blocks, threads, 0, stream>>>(hi, lo, lo_t, nhi, d / 2, theta);
   return cudaGetLastError();
 }
 

@@ -81,11 +81,13 @@ __device__ __forceinline__ TileCoord tile_coord(int t, int num_m, int num_n, int
 // ---- epilogue helpers -------------------------------------------------
 
 // cos/sin of pos * w_i from the two-level table: angle = hi part + lo part.
+// The lo part comes from the transposed table, so that the warp's threads
+// (consecutive rows) read consecutive entries.
 __device__ __forceinline__ void rope_cs(const float2* __restrict__ hi,
-                                        const float2* __restrict__ lo, long long pos, int half,
+                                        const float2* __restrict__ lo_t, long long pos, int half,
                                         int i, float& c, float& s) {
   const float2 a = __ldg(hi + (pos >> 10) * half + i);
-  const float2 b = __ldg(lo + (pos & 1023) * half + i);
+  const float2 b = __ldg(lo_t + (long long)i * 1024 + (pos & 1023));
   c = a.x * b.x - a.y * b.y;
   s = a.y * b.x + a.x * b.y;
 }
@@ -116,7 +118,7 @@ __device__ __forceinline__ void epi_proj_row(const EpiParams& ep, const ProjSeg&
 #pragma unroll
     for (int i = 0; i < H; ++i) {
       float c, s;
-      rope_cs(ep.rope_hi, ep.rope_lo, m, H, i, c, s);
+      rope_cs(ep.rope_hi, ep.rope_lo_t, m, H, i, c, s);
       const float a = v[i], b = v[i + H];
       v[i] = a * c - b * s;
       v[i + H] = b * c + a * s;

@@ -59,7 +59,7 @@ struct EpiParams {
   ProjSeg seg[3];
   int nseg;
   const float2* rope_hi;  // [(S >> 10) + 1][d/2] (cos, sin) of (pos & ~1023) * w_i
-  const float2* rope_lo;  // [1024][d/2]          (cos, sin) of (pos & 1023) * w_i
+  const float2* rope_lo_t;  // [d/2][1024]        (cos, sin) of (pos & 1023) * w_i
   float eps;
   // EPI_F32 / EPI_F32_ATOMIC
   float* C;
@@ -143,8 +143,9 @@ cudaError_t launch_attn_bwd(const AttnBwdArgs& a, int* err, cudaStream_t stream)
 
 // ---------------------------------------------------------- elementwise --
 
-cudaError_t launch_rope_table(float2* hi, float2* lo, long long S, int d, double theta,
-                              cudaStream_t stream);
+// hi [(S >> 10) + 1][d/2], lo [1024][d/2] and lo_t [d/2][1024] (lo transposed)
+cudaError_t launch_rope_table(float2* hi, float2* lo, float2* lo_t, long long S, int d,
+                              double theta, cudaStream_t stream);
 
 // Backward of (RMSNorm ->) RoPE for one block of heads: g (fp32, gradient of
 // the rotated values) -> bf16 gradient of the projection output; optionally

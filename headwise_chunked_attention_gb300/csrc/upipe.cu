@@ -192,7 +192,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // ----------------------------------------------------------- workspace --
 
 struct Layout {
-  size_t rope_hi, rope_lo, q, k, v, o, flush;     // forward
+  size_t rope_hi, rope_lo, rope_lo_t, q, k, v, o, flush;     // forward
   size_t dO, D, dq, dk, dv, dklo, dvlo, yq, rq, yk, rk;  // backward
   size_t total;
 };
@@ -208,6 +208,7 @@ Layout plan(const Geo& g, int mode) {
   const size_t S = (size_t)g.S, d = (size_t)g.d, ch = (size_t)g.ch, kvc = (size_t)g.kvc;
   L.rope_hi = take((((size_t)g.S >> 10) + 1) * (d / 2) * sizeof(float2));
   L.rope_lo = take(1024 * (d / 2) * sizeof(float2));
+  L.rope_lo_t = take(1024 * (d / 2) * sizeof(float2));
   L.q = take(S * ch * d * 2);
   L.k = take(S * kvc * d * 2);
   L.v = take(S * kvc * d * 2);
@@ -314,13 +315,13 @@ inline int side_sms(int num_sms) { return std::max(8, num_sms / 5); }
 int project_chunk(const Geo& g, const DeviceState* ds, cudaStream_t st, const CUtensorMap& xmap,
                   const bf16* Wq, const bf16* Wk, const bf16* Wv, const float* qgw,
                   const float* kgw, float eps, int h0, int kv0, bool new_group, bf16* Q, bf16* K,
-                  bf16* V, const float2* rhi, const float2* rlo, float* yq, float* rq, float* yk,
+                  bf16* V, const float2* rhi, const float2* rlo_t, float* yq, float* rq, float* yk,
                   float* rk) {
   const int d = g.d;
   CUtensorMap bm[3];
   EpiParams ep{};
   ep.rope_hi = rhi;
-  ep.rope_lo = rlo;
+  ep.rope_lo_t = rlo_t;
   ep.eps = eps;
   const int qk_mode = g.norm ? PROJ_NORM_ROPE : PROJ_ROPE;
   int n = 0, ns = 0;
@@ -414,12 +415,13 @@ static int attn_fwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
 
   float2* rhi = at<float2>(workspace, L.rope_hi);
   float2* rlo = at<float2>(workspace, L.rope_lo);
+  float2* rlo_t = at<float2>(workspace, L.rope_lo_t);
   bf16* Q = at<bf16>(workspace, L.q);
   bf16* K = at<bf16>(workspace, L.k);
   bf16* V = at<bf16>(workspace, L.v);
   bf16* Ows = at<bf16>(workspace, L.o);
   float* flush = L.flush == (size_t)-1 ? nullptr : at<float>(workspace, L.flush);
-  UPIPE_CUDA(launch_rope_table(rhi, rlo, g.S, g.d, shape->rope_theta, st));
+  UPIPE_CUDA(launch_rope_table(rhi, rlo, rlo_t, g.S, g.d, shape->rope_theta, st));
 
   CUtensorMap xmap, outmap;
   UPIPE_MAP(&xmap, x, g.S, g.hidden, g.hidden, 128, 64);
@@ -465,7 +467,7 @@ static int attn_fwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
     bf16* Qc = QO[c & 1];
     if (overlap && c >= 2) UPIPE_CUDA(cudaStreamWaitEvent(st, ev.out[c & 1], 0));
     UPIPE_TRY(project_chunk(g, ds, st, xmap, Wq, Wk, Wv, q_norm_w, k_norm_w, shape->norm_eps, h0,
-                            kv0, new_group, Qc, K, V, rhi, rlo, nullptr, nullptr, nullptr,
+                            kv0, new_group, Qc, K, V, rhi, rlo_t, nullptr, nullptr, nullptr,
                             nullptr));
     if (overlap && c >= 1) {
       UPIPE_CUDA(cudaEventRecord(ev.proj, st));
@@ -544,6 +546,7 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
 
   float2* rhi = at<float2>(workspace, L.rope_hi);
   float2* rlo = at<float2>(workspace, L.rope_lo);
+  float2* rlo_t = at<float2>(workspace, L.rope_lo_t);
   bf16* Q = at<bf16>(workspace, L.q);
   bf16* K = at<bf16>(workspace, L.k);
   bf16* V = at<bf16>(workspace, L.v);
@@ -561,7 +564,7 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
   float* yk = g.norm ? at<float>(workspace, L.yk) : nullptr;
   float* rk = g.norm ? at<float>(workspace, L.rk) : nullptr;
 
-  UPIPE_CUDA(launch_rope_table(rhi, rlo, g.S, d, shape->rope_theta, st));
+  UPIPE_CUDA(launch_rope_table(rhi, rlo, rlo_t, g.S, d, shape->rope_theta, st));
   // split-K weight gradients accumulate with reductions: start from zero
   UPIPE_CUDA(cudaMemsetAsync(dWq, 0, sizeof(float) * (size_t)g.Hq * d * g.hidden, st));
   UPIPE_CUDA(cudaMemsetAsync(dWk, 0, sizeof(float) * (size_t)g.Hkv * d * g.hidden, st));
@@ -642,7 +645,7 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
     const bool last_of_group = (g.ch >= g.g) || ((h0 + g.ch) % g.g == 0);
     // 1. recompute Q (and K, V) and the attention output of the chunk
     UPIPE_TRY(project_chunk(g, ds, st, xmap, Wq, Wk, Wv, q_norm_w, k_norm_w, shape->norm_eps, h0,
-                            kv0, new_group, Q, K, V, rhi, rlo, yq, rq, yk, rk));
+                            kv0, new_group, Q, K, V, rhi, rlo_t, yq, rq, yk, rk));
     if (new_group) {
       UPIPE_CUDA(cudaMemsetAsync(dK, 0, sizeof(float) * S * g.kvc * d, st));
       UPIPE_CUDA(cudaMemsetAsync(dV, 0, sizeof(float) * S * g.kvc * d, st));

@@ -83,8 +83,8 @@ enum {
  * (mode 1) for this shape, or 0 if the shape is invalid.  Pure host function.
  * The bytes are affine in chunk_heads: the per-chunk Q/O (and backward) parts
  * scale with chunk_heads, the K/V part is one KV group (or chunk_heads/(Hq/Hkv)
- * groups when a chunk spans several), plus a RoPE table of
- * ((S >> 10) + 1 + 1024) * d/2 float2 entries.  Every chunk runs in these same
+ * groups when a chunk spans several), plus RoPE tables of
+ * ((S >> 10) + 1 + 2 * 1024) * d/2 float2 entries.  Every chunk runs in these same
  * buffers, which is how UPipe saves memory (memeeeeeex.com, "Untied Ulysses
  * (UPipe)": the chunks reuse one set of buffers). */
 size_t upipe_workspace_bytes(const upipe_shape_t* shape, int mode);

@@ -48,7 +48,7 @@ def test_workspace_closed_form(u):
         for ch in w.chunk_heads:
             kvc = max(1, ch // g)
             S, d = w.S, w.d
-            expect = (al(((S >> 10) + 1) * (d // 2) * 8) + al(1024 * (d // 2) * 8)
+            expect = (al(((S >> 10) + 1) * (d // 2) * 8) + 2 * al(1024 * (d // 2) * 8)
                       + 2 * al(S * ch * d * 2) + 2 * al(S * kvc * d * 2))
             if S > 512 * 128:   # per-SM fp32 rows for folding long attention rows
                 expect += 256 * 256 * d * 4
