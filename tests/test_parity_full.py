@@ -59,8 +59,12 @@ def test_forward_sampled_rows_at_full_size(name):
         assert np.array_equal(got[ch][2], first), ch
 
 
-@pytest.mark.parametrize("name", ["llama3-8b-rank-s1m", "qwen3-32b-rank-s1m"])
-def test_backward_tail_rows_at_full_size(name):
+@pytest.mark.parametrize("name,saved_o", [("llama3-8b-rank-s1m", False),
+                                          ("qwen3-32b-rank-s1m", False),
+                                          ("llama3-8b-rank-s1m", True)])
+def test_backward_tail_rows_at_full_size(name, saved_o):
+    # saved_o: the backward takes the forward's attention output
+    # (upipe_attn_bwd_saved_o) instead of recomputing it chunk by chunk
     import headwise_chunked_attention_gb300 as u
     w = WORKLOADS[name]
     ch = w.chunk_heads[0]
@@ -69,8 +73,9 @@ def test_backward_tail_rows_at_full_size(name):
     out = torch.empty(w.S, w.hidden, device="cuda")
     lse = torch.empty(w.Hq, w.S, device="cuda")
     ws = torch.empty(u.workspace_bytes(sh, 1), dtype=torch.uint8, device="cuda")
+    o = torch.empty(w.S, w.Hq * w.d, device="cuda", dtype=torch.bfloat16) if saved_o else None
     u.attn_fwd(sh, t["x"], t["Wq"], t["Wk"], t["Wv"], t["Wo"], out, lse, ws,
-               t.get("q_gamma"), t.get("k_gamma"))
+               t.get("q_gamma"), t.get("k_gamma"), o)
     del out
     g = {n: torch.empty(t[s].shape, device="cuda") for n, s in
          [("dx", "x"), ("dWq", "Wq"), ("dWk", "Wk"), ("dWv", "Wv"), ("dWo", "Wo")]}
@@ -78,7 +83,7 @@ def test_backward_tail_rows_at_full_size(name):
     dkg = torch.empty(w.d, device="cuda") if w.qk_norm else None
     u.attn_bwd(sh, t["x"], t["Wq"], t["Wk"], t["Wv"], t["Wo"], t["dout"], lse, g["dx"],
                g["dWq"], g["dWk"], g["dWv"], g["dWo"], ws, t.get("q_gamma"), t.get("k_gamma"),
-               dqg, dkg)
+               dqg, dkg, attn_o=o)
     torch.cuda.synchronize()
     assert u.last_error() == 0
     n = N_ROWS
