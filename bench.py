@@ -510,9 +510,9 @@ def main():
     if mode:
         groups = w.Hkv if ch < w.Hq // w.Hkv else nchunks
         # per chunk: projection, attention, dO, dWo, attention backward, Q
-        # RoPE/RMSNorm backward, dWq hi and lo, one dx; per KV group: K
-        # RoPE/RMSNorm backward, dV split, dWk and dWv hi and lo
-        launches_per_step += 1 + 9 * nchunks + 6 * groups
+        # RoPE/RMSNorm backward, one dW and one dx GEMM; per KV group: K
+        # RoPE/RMSNorm backward, dV split
+        launches_per_step += 1 + 8 * nchunks + 2 * groups
 
     if rank != 0:
         if dist is not None:

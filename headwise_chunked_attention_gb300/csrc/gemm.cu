@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  const int num_m = (g.M + BM - 1) / BM;
+  const int num_m = g.nmseg > 0 ? g.mseg_t0[g.nmseg] : (g.M + BM - 1) / BM;
   const int num_n = g.N / BN;
   const int kb_total = g.nkseg > 0 ? g.kseg_end[g.nkseg - 1] : (g.K + BK - 1) / BK;
   const int ksplit = g.ksplit > 0 ? g.ksplit : 1;
@@ -188,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&maps.a[g.kseg_a[s]]);
       prefetch_tmap(&maps.b[g.kseg_b[s]]);
     }
+    for (int s = 1; s < g.nmseg; ++s) prefetch_tmap(&maps.a[g.mseg_a[s]]);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
@@ -211,6 +212,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap* am = &maps.a[0];
         const CUtensorMap* bm = &maps.b[0];
         int brow = n0;
+        int arow = tc.m0;  // first row of the A tile in its tensor map
+        if (g.nmseg > 0) {
+          const int mt = tc.m0 / BM;
+          int s = 0;
+          while (s + 1 < g.nmseg && mt >= g.mseg_t0[s + 1]) ++s;
+          am = &maps.a[g.mseg_a[s]];
+          arow = (mt - g.mseg_t0[s]) * BM;
+        }
         if (EPI == EPI_PROJ) {
           int s = 0;
           while (s + 1 < ep.nseg && n0 >= ep.seg[s].n_end) ++s;
@@ -231,10 +240,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int k0 = (kb - ks_kb0) * BK;
           if (!A_MN) {
-            tma_load_2d(sa, am, &full[stage], k0, tc.m0);
+            tma_load_2d(sa, am, &full[stage], k0, arow);
           } else {
-            tma_load_2d(sa, am, &full[stage], tc.m0, k0);
-            tma_load_2d(sa + 8192, am, &full[stage], tc.m0 + 64, k0);
+            tma_load_2d(sa, am, &full[stage], arow, k0);
+            tma_load_2d(sa + 8192, am, &full[stage], arow + 64, k0);
           }
           if (!B_MN) {
             tma_load_2d(sb, bm, &full[stage], k0, brow);
@@ -394,13 +403,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
+        float* crow;
+        bool row_live;
+        if (g.nmseg > 0) {  // the segment holding this row, and the row within it
+          const int mt = tc.m0 / BM;
+          int s = 0;
+          while (s + 1 < g.nmseg && mt >= g.mseg_t0[s + 1]) ++s;
+          const long long ml = m - (long long)g.mseg_t0[s] * BM;
+          row_live = (tc.kb1 > tc.kb0) && ml < g.mseg_rows[s];
+          crow = ep.mseg_c[s] + (row_live ? ml * ep.ldc : 0);
+        } else {
+          row_live = live;
+          crow = ep.C + (row_live ? m * ep.ldc : 0);
+        }
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t r[32];
           tmem_ld32(tbase + c * 32, r);
           tmem_ld_wait(r);
-          if (live) {
-            float* cp = ep.C + m * ep.ldc + n0 + c * 32;
+          if (row_live) {
+            float* cp = crow + n0 + c * 32;
 #pragma unroll
             for (int i = 0; i < 32; i += 4)
               red_add_v4_f32(cp + i, __uint_as_float(r[i]), __uint_as_float(r[i + 1]),
@@ -465,6 +487,13 @@ cudaError_t launch_gemm(int bn, bool a_mn, bool b_mn, EpiKind epi, const CUtenso
   if (na < 1 || na > kMaxASegs || nb < 1 || nb > kMaxBMaps) return cudaErrorInvalidValue;
   if (epi == EPI_F32 && !cmap) return cudaErrorInvalidValue;
   if (g.nkseg < 0 || g.nkseg > kMaxASegs) return cudaErrorInvalidValue;
+  if (g.nmseg < 0 || g.nmseg > kMaxASegs || (g.nmseg > 0 && epi != EPI_F32_ATOMIC))
+    return cudaErrorInvalidValue;
+  for (int s = 0; s < g.nmseg; ++s)
+    if (g.mseg_a[s] < 0 || g.mseg_a[s] >= na || g.mseg_t0[s + 1] <= g.mseg_t0[s] ||
+        g.mseg_rows[s] <= 0 || g.mseg_rows[s] > (g.mseg_t0[s + 1] - g.mseg_t0[s]) * BM ||
+        !ep.mseg_c[s])
+      return cudaErrorInvalidValue;
   for (int s = 0; s < g.nkseg; ++s)
     if (g.kseg_a[s] < 0 || g.kseg_a[s] >= na || g.kseg_b[s] < 0 || g.kseg_b[s] >= nb ||
         g.kseg_end[s] <= (s ? g.kseg_end[s - 1] : 0))

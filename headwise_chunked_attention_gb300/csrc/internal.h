@@ -65,6 +65,8 @@ struct EpiParams {
   float* C;
   long long ldc;
   int beta;          // EPI_F32: 0 store, 1 add (both through the C tensor map)
+  // EPI_F32_ATOMIC with M segments: output base of each segment (row 0)
+  float* mseg_c[6];
   // EPI_DO
   bf16* dO;
   int ld_do;
@@ -88,6 +90,14 @@ struct GemmArgs {
   int kseg_end[kMaxASegs];
   int kseg_a[kMaxASegs];
   int kseg_b[kMaxASegs];
+  // M segments (nmseg > 0, EPI_F32_ATOMIC): the M range is a concatenation of
+  // nmseg runs of 128-row tiles; run s covers tiles [mseg_t0[s], mseg_t0[s+1]),
+  // reads A from A map mseg_a[s] (rows from 0) and adds its mseg_rows[s] rows
+  // into EpiParams::mseg_c[s] (row stride ldc).  M is then 128 * mseg_t0[nmseg].
+  int nmseg;
+  int mseg_t0[kMaxASegs + 1];
+  int mseg_rows[kMaxASegs];
+  int mseg_a[kMaxASegs];
 };
 
 // a_mn / b_mn: operand stored MN-major (A as [K, M] row-major, B as [K, N]).

@@ -624,16 +624,34 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
     dx_started = true;
     return UPIPE_OK;
   };
-  auto dw_gemm = [&](const bf16* dA, int ncols, int ld_a, float* dW) -> int {
-    // dW[ncols, hidden] += dA^T x  (K = S, split and reduced)
-    CUtensorMap am;
-    UPIPE_MAP(&am, dA, g.S, (uint64_t)ncols, (uint64_t)ld_a, 64, 64);
+  // dW (+)= dA^T x for every part of the chunk in one split-K GEMM: the parts
+  // are M segments (one A map and one output each; a weight's hi and lo parts
+  // add into the same rows), so the chunk reads x once, not once per part.
+  struct DwSeg {
+    const bf16* dA;  // [S, ncols] bf16
+    int ncols;
+    float* dW;       // [ncols rows, hidden] fp32
+  };
+  auto dw_gemm = [&](const DwSeg* segs, int nseg) -> int {
+    CUtensorMap am[kMaxASegs];
+    GemmArgs ga{0, g.hidden, (int)g.S, 1, d};
     EpiParams ep{};
-    ep.C = dW;
     ep.ldc = g.hidden;
-    GemmArgs ga{ncols, g.hidden, (int)g.S, wgrad_splits(g.S, ncols, g.hidden, 128, ds->num_sms),
-                d};
-    UPIPE_CUDA(launch_gemm(128, true, true, EPI_F32_ATOMIC, &am, 1, &x_mn, 1, ga, ep, ds->err,
+    ga.nmseg = nseg;
+    int tiles = 0;
+    for (int s = 0; s < nseg; ++s) {
+      UPIPE_MAP(&am[s], segs[s].dA, g.S, (uint64_t)segs[s].ncols, (uint64_t)segs[s].ncols, 64,
+                64);
+      ga.mseg_t0[s] = tiles;
+      ga.mseg_rows[s] = segs[s].ncols;
+      ga.mseg_a[s] = s;
+      ep.mseg_c[s] = segs[s].dW;
+      tiles += (segs[s].ncols + 127) / 128;
+    }
+    ga.mseg_t0[nseg] = tiles;
+    ga.M = tiles * 128;
+    ga.ksplit = wgrad_splits(g.S, ga.M, g.hidden, 128, ds->num_sms);
+    UPIPE_CUDA(launch_gemm(128, true, true, EPI_F32_ATOMIC, am, nseg, &x_mn, 1, ga, ep, ds->err,
                            ds->num_sms, st));
     return UPIPE_OK;
   };
@@ -735,11 +753,11 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
       q.rope_hi = rhi;
       q.rope_lo = rlo;
       UPIPE_CUDA(launch_qk_bwd(q, st));
-      for (bf16* part : {dO, Ows})
-        UPIPE_TRY(dw_gemm(part, g.ch * d, g.ch * d, dWq + (size_t)h0 * d * g.hidden));
     }
     const bf16* Wq_c = Wq + (size_t)h0 * d * g.hidden;
     DxSeg dxs[kMaxASegs] = {{dO, g.ch * d, Wq_c}, {Ows, g.ch * d, Wq_c}};
+    float* dWq_c = dWq + (size_t)h0 * d * g.hidden;
+    DwSeg dws[kMaxASegs] = {{dO, g.ch * d, dWq_c}, {Ows, g.ch * d, dWq_c}};
     int ndx = 2;
     // 5. at the group's last chunk: dK -> dA_k (hi over K, lo beside it),
     //    dV -> hi over V and lo beside it
@@ -765,16 +783,20 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
       UPIPE_CUDA(launch_f32_to_bf16x2(dV, g.kvc * d, V, dVlo, g.kvc * d, g.S, g.kvc * d, st));
       const bf16* Wk_g = Wk + (size_t)kv0 * d * g.hidden;
       const bf16* Wv_g = Wv + (size_t)kv0 * d * g.hidden;
+      float* dWk_g = dWk + (size_t)kv0 * d * g.hidden;
+      float* dWv_g = dWv + (size_t)kv0 * d * g.hidden;
       for (int part = 0; part < 2; ++part) {
         const bf16* gk = part ? dKlo : K;
         const bf16* gv = part ? dVlo : V;
-        UPIPE_TRY(dw_gemm(gk, g.kvc * d, g.kvc * d, dWk + (size_t)kv0 * d * g.hidden));
-        UPIPE_TRY(dw_gemm(gv, g.kvc * d, g.kvc * d, dWv + (size_t)kv0 * d * g.hidden));
+        dws[ndx] = {gk, g.kvc * d, dWk_g};
         dxs[ndx++] = {gk, g.kvc * d, Wk_g};
+        dws[ndx] = {gv, g.kvc * d, dWv_g};
         dxs[ndx++] = {gv, g.kvc * d, Wv_g};
       }
     }
-    // 6. dx (+)= the chunk's Q part (and the group's K and V parts)
+    // 6. dWq (and the group's dWk, dWv) and dx (+)= the chunk's Q part (and
+    //    the group's K and V parts), each as one GEMM over all parts
+    UPIPE_TRY(dw_gemm(dws, ndx));
     UPIPE_TRY(dx_gemm(dxs, ndx));
   }
   return UPIPE_OK;
