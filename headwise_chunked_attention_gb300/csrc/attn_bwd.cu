@@ -471,14 +471,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
 template <int D>
 static cudaError_t launch_bwd_t(const AttnBwdArgs& a, int* err, cudaStream_t stream) {
   using Cfg = BwdCfg<D>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  const cudaError_t ea = smem_attr_once(attn_bwd_kernel<D>, (int)Cfg::SMEM_BYTES, attr_done);
+  if (ea != cudaSuccess) return ea;
   CUtensorMap qm, km, vm, dm, dqm;
   if (!make_tmap_f32(&dqm, a.dQ, a.S, (uint64_t)a.ld_dq, a.ld_dq, DQR, 32) ||
       !make_tmap_bf16(&qm, a.Q, a.S, (uint64_t)a.heads * D, a.ldq, BQ, 64) ||

@@ -392,14 +392,9 @@ static cudaError_t launch_fwd_t(const CUtensorMap& qmap, const CUtensorMap& kmap
                                 const CUtensorMap& vmap, const AttnFwdArgs& a, int* err,
                                 cudaStream_t stream) {
   using Cfg = FwdCfg<D>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  const cudaError_t ea = smem_attr_once(attn_fwd_kernel<D>, (int)Cfg::SMEM_BYTES, attr_done);
+  if (ea != cudaSuccess) return ea;
   const long long nqb = (a.S + 255) / 256;
   const long long grid = nqb * a.heads;
   attn_fwd_kernel<D><<<(unsigned)grid, kThreads, Cfg::SMEM_BYTES, stream>>>(qmap, kmap, vmap, a,

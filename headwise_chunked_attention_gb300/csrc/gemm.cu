@@ -464,13 +464,9 @@ static cudaError_t launch_t(const GemmMaps& maps, const GemmArgs& g, const EpiPa
                             int* err, int num_sms, cudaStream_t stream) {
   using Cfg = GemmCfg<BN>;
   auto kfn = gemm_kernel<BN, A_MN, B_MN, EPI>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  const cudaError_t ea = smem_attr_once(kfn, (int)Cfg::SMEM_BYTES, attr_done);
+  if (ea != cudaSuccess) return ea;
   const int num_m = (g.M + BM - 1) / BM;
   const long long tiles = (long long)num_m * (g.N / BN) * std::max(1, g.ksplit);
   const int grid = (int)std::max(1LL, std::min<long long>(tiles, num_sms));

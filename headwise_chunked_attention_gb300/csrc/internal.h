@@ -7,9 +7,26 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/upipe.h"
 
 namespace upipe {
+
+// Sets a kernel's dynamic shared memory limit once per device (thread-safe:
+// concurrent first calls both set it, which is harmless).  ``done`` is the
+// kernel's own bit mask of devices already set up.
+template <typename Kernel>
+cudaError_t smem_attr_once(Kernel* kernel, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 using bf16 = __nv_bfloat16;
 
