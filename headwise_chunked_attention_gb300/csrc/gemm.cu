@@ -514,6 +514,7 @@ cudaError_t launch_gemm(int bn, bool a_mn, bool b_mn, EpiKind epi, const CUtenso
   UPIPE_GEMM_CASE(128, false, true, EPI_F32)
   UPIPE_GEMM_CASE(256, false, true, EPI_F32)
   // weight gradients (K = S, split)
+  UPIPE_GEMM_CASE(256, true, true, EPI_F32_ATOMIC)
   UPIPE_GEMM_CASE(128, true, true, EPI_F32_ATOMIC)
   UPIPE_GEMM_CASE(64, true, true, EPI_F32_ATOMIC)
 #undef UPIPE_GEMM_CASE

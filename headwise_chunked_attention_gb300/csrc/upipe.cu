@@ -650,8 +650,11 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
     }
     ga.mseg_t0[nseg] = tiles;
     ga.M = tiles * 128;
-    ga.ksplit = wgrad_splits(g.S, ga.M, g.hidden, 128, ds->num_sms);
-    UPIPE_CUDA(launch_gemm(128, true, true, EPI_F32_ATOMIC, am, nseg, &x_mn, 1, ga, ep, ds->err,
+    // 256-wide tiles: two operands MN-major at BN = 128 bring 128 bytes into
+    // the SM per tensor-core cycle, more than the TMA path feeds
+    const int bn = (g.hidden % 256 == 0) ? 256 : 128;
+    ga.ksplit = wgrad_splits(g.S, ga.M, g.hidden, bn, ds->num_sms);
+    UPIPE_CUDA(launch_gemm(bn, true, true, EPI_F32_ATOMIC, am, nseg, &x_mn, 1, ga, ep, ds->err,
                            ds->num_sms, st));
     return UPIPE_OK;
   };
