@@ -41,12 +41,14 @@ constexpr uint32_t A_STAGE_BYTES = BM * BK * 2;  // 16 KB
 constexpr int kEpiBufs = 2;                       // staging buffers per epilogue warp
 constexpr uint32_t EPI_BUF_BYTES = 32 * 32 * 4;   // [32 rows][32 cols] fp32
 
-template <int BN>
+// MT: 128-row A tiles per output tile (MT = 2: two accumulators share each
+// B tile, halving the B bytes loaded and read per FLOP)
+template <int BN, int MT = 1>
 struct GemmCfg {
   static constexpr uint32_t B_STAGE_BYTES = BN * BK * 2;
-  static constexpr uint32_t STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-  static constexpr int STAGES = (BN == 256) ? 4 : 6;
-  static constexpr uint32_t TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
+  static constexpr uint32_t STAGE_BYTES = MT * A_STAGE_BYTES + B_STAGE_BYTES;
+  static constexpr int STAGES = (STAGE_BYTES > 32768) ? 4 : 6;
+  static constexpr uint32_t TMEM_COLS = (2 * MT * BN < 32) ? 32 : 2 * MT * BN;
   static constexpr uint32_t EPI_OFF = STAGES * STAGE_BYTES;
   static constexpr uint32_t BAR_OFF = EPI_OFF + 4 * kEpiBufs * EPI_BUF_BYTES;
   static constexpr uint32_t SMEM_BYTES = BAR_OFF + 1024 /*align*/ + 256 /*bars*/;
@@ -65,12 +67,12 @@ struct GemmMaps {
 };
 
 __device__ __forceinline__ TileCoord tile_coord(int t, int num_m, int num_n, int kb_total,
-                                                int ksplit) {
+                                                int ksplit, int tile_rows) {
   const int per_split = num_m * num_n;
   const int ks = t / per_split;
   const int r = t - ks * per_split;
   TileCoord c;
-  c.m0 = (r / num_n) * BM;
+  c.m0 = (r / num_n) * tile_rows;
   c.n0 = (r % num_n);
   const int kb_per = (kb_total + ksplit - 1) / ksplit;
   c.kb0 = ks * kb_per;
@@ -138,11 +140,11 @@ __device__ __forceinline__ void epi_proj_row(const EpiParams& ep, const ProjSeg&
 
 }  // namespace
 
-template <int BN, bool A_MN, bool B_MN, int EPI>
+template <int BN, bool A_MN, bool B_MN, int EPI, int MT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g, const EpiParams ep,
                 int* __restrict__ err) {
-  using Cfg = GemmCfg<BN>;
+  using Cfg = GemmCfg<BN, MT>;
   constexpr int STAGES = Cfg::STAGES;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -158,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  const int num_m = g.nmseg > 0 ? g.mseg_t0[g.nmseg] : (g.M + BM - 1) / BM;
+  const int num_m = g.nmseg > 0 ? g.mseg_t0[g.nmseg] : (g.M + BM * MT - 1) / (BM * MT);
   const int num_n = g.N / BN;
   const int kb_total = g.nkseg > 0 ? g.kseg_end[g.nkseg - 1] : (g.K + BK - 1) / BK;
   const int ksplit = g.ksplit > 0 ? g.ksplit : 1;
@@ -207,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t issued = 0, issued_phase = 0;  // per-stage bit masks
       bool ok = true;
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        const TileCoord tc = tile_coord(t, num_m, num_n, kb_total, ksplit);
+        const TileCoord tc = tile_coord(t, num_m, num_n, kb_total, ksplit, BM * MT);
         const int n0 = tc.n0 * BN;
         const CUtensorMap* am = &maps.a[0];
         const CUtensorMap* bm = &maps.b[0];
@@ -231,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = tc.kb0; kb < tc.kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, err, abort_flag)) { ok = false; break; }
           uint8_t* sa = smem + stage * Cfg::STAGE_BYTES;
-          uint8_t* sb = sa + A_STAGE_BYTES;
+          uint8_t* sb = sa + MT * A_STAGE_BYTES;
           mbar_expect_tx(&full[stage], Cfg::STAGE_BYTES);
           if (g.nkseg > 0) {
             while (kb >= g.kseg_end[ks]) ks_kb0 = g.kseg_end[ks++];
@@ -239,11 +241,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             bm = &maps.b[g.kseg_b[ks]];
           }
           const int k0 = (kb - ks_kb0) * BK;
-          if (!A_MN) {
-            tma_load_2d(sa, am, &full[stage], k0, arow);
-          } else {
-            tma_load_2d(sa, am, &full[stage], arow, k0);
-            tma_load_2d(sa + 8192, am, &full[stage], arow + 64, k0);
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            uint8_t* sam = sa + mt * A_STAGE_BYTES;
+            if (!A_MN) {
+              tma_load_2d(sam, am, &full[stage], k0, arow + BM * mt);
+            } else {
+              tma_load_2d(sam, am, &full[stage], arow + BM * mt, k0);
+              tma_load_2d(sam + 8192, am, &full[stage], arow + BM * mt + 64, k0);
+            }
           }
           if (!B_MN) {
             tma_load_2d(sb, bm, &full[stage], k0, brow);
@@ -272,25 +278,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++it) {
-        const TileCoord tc = tile_coord(t, num_m, num_n, kb_total, ksplit);
+        const TileCoord tc = tile_coord(t, num_m, num_n, kb_total, ksplit, BM * MT);
         const int acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
         if (!mbar_wait_warp(&acc_empty[acc], acc_phase ^ 1, err, abort_flag)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * BN;
+        const uint32_t d_tmem = tmem_base + acc * (MT * BN);
         for (int kb = tc.kb0; kb < tc.kb1; ++kb) {
           if (!mbar_wait_warp(&full[stage], phase, err, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * Cfg::STAGE_BYTES);
-          const uint32_t sb = sa + A_STAGE_BYTES;
+          const uint32_t sb = sa + MT * A_STAGE_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
-            uint64_t ad, bd;
-            if (!A_MN) ad = sdesc_sw128(sa + k * 32, 16, 1024);
-            else ad = sdesc_sw128(sa + k * 2048, 8192, 1024);
+            uint64_t bd;
             if (!B_MN) bd = sdesc_sw128(sb + k * 32, 16, 1024);
             else bd = sdesc_sw128(sb + k * 2048, 8192, 1024);
-            mma_ss_w(d_tmem, ad, bd, IDESC, (kb > tc.kb0 || k > 0) ? 1u : 0u);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+              const uint32_t sam = sa + mt * A_STAGE_BYTES;
+              uint64_t ad;
+              if (!A_MN) ad = sdesc_sw128(sam + k * 32, 16, 1024);
+              else ad = sdesc_sw128(sam + k * 2048, 8192, 1024);
+              mma_ss_w(d_tmem + mt * BN, ad, bd, IDESC, (kb > tc.kb0 || k > 0) ? 1u : 0u);
+            }
           }
           mma_commit_w(&empty[stage]);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -307,14 +318,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = 0;
     uint32_t epi_round = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
-      const TileCoord tc = tile_coord(t, num_m, num_n, kb_total, ksplit);
+      const TileCoord tc = tile_coord(t, num_m, num_n, kb_total, ksplit, BM * MT);
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
       // warp-uniform: the tcgen05.ld below is warp-collective
       if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[acc], acc_phase, err, abort_flag))) break;
       tc_fence_after();
-      const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(quarter * 32) << 16);
-      const long long m = (long long)tc.m0 + row;
+#pragma unroll 1
+      for (int mt = 0; mt < MT; ++mt) {
+      const int m0t = tc.m0 + BM * mt;  // first row of this 128-row part
+      const uint32_t tbase =
+          tmem_base + acc * (MT * BN) + mt * BN + ((uint32_t)(quarter * 32) << 16);
+      const long long m = (long long)m0t + row;
       const int n0 = tc.n0 * BN;
       const bool live = (m < g.M) && (tc.kb1 > tc.kb0);
 
@@ -379,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // [32 rows x 32 cols] fp32 blocks of this warp's rows, 128-byte
         // swizzled in shared memory, then one TMA store / reduce-add each
         uint8_t* bufs = smem + Cfg::EPI_OFF + quarter * kEpiBufs * EPI_BUF_BYTES;
-        const bool any_live = (tc.m0 + quarter * 32 < g.M) && (tc.kb1 > tc.kb0);
+        const bool any_live = (m0t + quarter * 32 < g.M) && (tc.kb1 > tc.kb0);
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c, ++epi_round) {
           uint32_t r[32];
@@ -396,8 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              if (ep.beta) tma_reduce_add_2d(&maps.c, buf, n0 + 32 * c, tc.m0 + quarter * 32);
-              else tma_store_2d(&maps.c, buf, n0 + 32 * c, tc.m0 + quarter * 32);
+              if (ep.beta) tma_reduce_add_2d(&maps.c, buf, n0 + 32 * c, m0t + quarter * 32);
+              else tma_store_2d(&maps.c, buf, n0 + 32 * c, m0t + quarter * 32);
               bulk_commit();
             }
           }
@@ -406,9 +421,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* crow;
         bool row_live;
         if (g.nmseg > 0) {  // the segment holding this row, and the row within it
-          const int mt = tc.m0 / BM;
+          const int mtile = m0t / BM;
           int s = 0;
-          while (s + 1 < g.nmseg && mt >= g.mseg_t0[s + 1]) ++s;
+          while (s + 1 < g.nmseg && mtile >= g.mseg_t0[s + 1]) ++s;
           const long long ml = m - (long long)g.mseg_t0[s] * BM;
           row_live = (tc.kb1 > tc.kb0) && ml < g.mseg_rows[s];
           crow = ep.mseg_c[s] + (row_live ? ml * ep.ldc : 0);
@@ -430,6 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      }  // mt
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
@@ -459,15 +475,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ host --
 
-template <int BN, bool A_MN, bool B_MN, int EPI>
+template <int BN, bool A_MN, bool B_MN, int EPI, int MT = 1>
 static cudaError_t launch_t(const GemmMaps& maps, const GemmArgs& g, const EpiParams& ep,
                             int* err, int num_sms, cudaStream_t stream) {
-  using Cfg = GemmCfg<BN>;
-  auto kfn = gemm_kernel<BN, A_MN, B_MN, EPI>;
+  using Cfg = GemmCfg<BN, MT>;
+  auto kfn = gemm_kernel<BN, A_MN, B_MN, EPI, MT>;
   static std::atomic<unsigned long long> attr_done{0};
   const cudaError_t ea = smem_attr_once(kfn, (int)Cfg::SMEM_BYTES, attr_done);
   if (ea != cudaSuccess) return ea;
-  const int num_m = (g.M + BM - 1) / BM;
+  if (MT > 1 && g.nmseg > 0) return cudaErrorInvalidValue;
+  const int num_m = g.nmseg > 0 ? g.mseg_t0[g.nmseg] : (g.M + BM * MT - 1) / (BM * MT);
   const long long tiles = (long long)num_m * (g.N / BN) * std::max(1, g.ksplit);
   const int grid = (int)std::max(1LL, std::min<long long>(tiles, num_sms));
   kfn<<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(maps, g, ep, err);
@@ -501,15 +518,18 @@ cudaError_t launch_gemm(int bn, bool a_mn, bool b_mn, EpiKind epi, const CUtenso
 #define UPIPE_GEMM_CASE(BN_, AMN, BMN, E)                                              \
   if (bn == BN_ && a_mn == AMN && b_mn == BMN && epi == E)                             \
     return launch_t<BN_, AMN, BMN, E>(maps, g, ep, err, num_sms, stream);
-  // projections (one head per tile: BN = d)
+  // projections (one head per tile: BN = d; at d = 128 each tile holds 256
+  // rows in two accumulators that share the weight tile)
   UPIPE_GEMM_CASE(64, false, false, EPI_PROJ)
-  UPIPE_GEMM_CASE(128, false, false, EPI_PROJ)
+  if (bn == 128 && !a_mn && !b_mn && epi == EPI_PROJ)
+    return launch_t<128, false, false, EPI_PROJ, 2>(maps, g, ep, err, num_sms, stream);
   // Wo-slice accumulate
   UPIPE_GEMM_CASE(128, false, false, EPI_F32)
   UPIPE_GEMM_CASE(256, false, false, EPI_F32)
-  // dO = dOut Wo_c (+ D)
+  // dO = dOut Wo_c (+ D); at d = 128 also 256 rows per tile
   UPIPE_GEMM_CASE(64, false, true, EPI_DO)
-  UPIPE_GEMM_CASE(128, false, true, EPI_DO)
+  if (bn == 128 && !a_mn && b_mn && epi == EPI_DO)
+    return launch_t<128, false, true, EPI_DO, 2>(maps, g, ep, err, num_sms, stream);
   // dX += dQKV W
   UPIPE_GEMM_CASE(128, false, true, EPI_F32)
   UPIPE_GEMM_CASE(256, false, true, EPI_F32)
