@@ -264,8 +264,13 @@ T* at(void* ws, size_t off) {
 
 // Events of one forward call's fork/join with the side stream.  Destroying an
 // event whose record is still pending is allowed: CUDA frees it on completion.
+// If the call leaves early (an error after work was forked), the destructor
+// still orders the caller's stream after everything enqueued on the side
+// stream, so the caller never sees the side stream's work outlive the call.
 struct Events {
   cudaEvent_t proj = nullptr, out[2] = {nullptr, nullptr};
+  cudaStream_t side = nullptr, caller = nullptr;  // set once work is forked
+  bool joined = false;
   cudaError_t create() {
     for (cudaEvent_t* e : {&proj, &out[0], &out[1]}) {
       const cudaError_t r = cudaEventCreateWithFlags(e, cudaEventDisableTiming);
@@ -274,6 +279,8 @@ struct Events {
     return cudaSuccess;
   }
   ~Events() {
+    if (side && !joined && proj && cudaEventRecord(proj, side) == cudaSuccess)
+      cudaStreamWaitEvent(caller, proj, 0);
     for (cudaEvent_t e : {proj, out[0], out[1]})
       if (e) cudaEventDestroy(e);
   }
@@ -441,7 +448,11 @@ static int attn_fwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
   cudaStream_t side = (fork && g.nchunks > 1) ? side_stream(ds) : nullptr;
   const bool overlap = side != nullptr;
   Events ev;
-  if (overlap) UPIPE_CUDA(ev.create());
+  if (overlap) {
+    UPIPE_CUDA(ev.create());
+    ev.side = side;
+    ev.caller = st;
+  }
   auto out_gemm = [&](int c, cudaStream_t s, int sms) -> int {
     const int h0 = c * g.ch;
     const bf16* O = o_all ? o_all + (size_t)h0 * g.d : QO[c & 1];
@@ -481,7 +492,10 @@ static int attn_fwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
                               flush));
     if (!overlap && c + 1 < g.nchunks) UPIPE_TRY(out_gemm(c, st, ds->num_sms));
   }
-  if (overlap) UPIPE_CUDA(cudaStreamWaitEvent(st, ev.out[(g.nchunks - 2) & 1], 0));
+  if (overlap) {
+    UPIPE_CUDA(cudaStreamWaitEvent(st, ev.out[(g.nchunks - 2) & 1], 0));
+    ev.joined = true;
+  }
   UPIPE_TRY(out_gemm(g.nchunks - 1, st, ds->num_sms));
   return UPIPE_OK;
 }
