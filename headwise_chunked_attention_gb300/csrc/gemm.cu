@@ -2,18 +2,24 @@
 //
 //   C[M, N] = sum_k A[m, k] * B[n, k]       (bf16 operands, fp32 in TMEM)
 //
-// One CTA per SM walks the output tiles (BM = 128 rows x BN columns) with a
+// One CTA per SM walks the output tiles (MT x 128 rows x BN columns) with a
 // static stride.  Warp roles:
-//   warp 0      TMA producer: 128-byte-swizzled 64-wide K slabs of A and B
-//               into a ring of shared-memory stages;
-//   warp 1      TMEM owner and MMA issuer: tcgen05.mma M=128, N=BN, K=16,
-//               accumulating into one of two TMEM accumulators, so that the
-//               epilogue of tile i overlaps the main loop of tile i+1;
+//   warp 0      TMA producer: 128-byte-swizzled 64-wide K slabs of A (MT
+//               128-row tiles) and B into a ring of shared-memory stages;
+//   warp 1      TMEM owner and MMA issuer: tcgen05.mma M=128, N=BN, K=16 per
+//               128-row part (MT = 2: two parts share each B slab, halving
+//               the B bytes loaded and read per FLOP), accumulating into one
+//               of two TMEM accumulator sets, so that the epilogue of tile i
+//               overlaps the main loop of tile i+1;
 //   warps 2..5  epilogue: tcgen05.ld of one accumulator row per thread,
 //               then the fused operation and the global store.
 // Operands may be K-major (row-major [M,K] / [N,K]) or MN-major ([K,M] /
 // [K,N]); the layout is chosen by the instruction descriptor's transpose bits
 // and the shared-memory descriptors, the data is never transposed.
+// K segments: the K range may run through several (A, B) tensor-map pairs
+// into one accumulator (dx += sum of a chunk's gradient parts times their
+// weight slices).  M segments: 128-row tile runs may each take their own A
+// map and output pointer (a chunk's split-K weight gradients in one launch).
 //
 // Epilogues (what the attention layer needs around the attention kernel):
 //   EPI_PROJ        Q/K/V projection of one head chunk: optional per-head
