@@ -476,6 +476,41 @@ def main():
             t_b = timed(step, max(1, args.steps // 2))
         roof_bwd = roofline("attn_bwd_kernel", kb.durations_ms(), 10.0, t_b, max(1, args.steps // 2))
 
+    # ---- the HBM-bound kernels: algorithmic bytes per layer call over their
+    # summed live launch time (hook kernels 2, 3, 4)
+    def hbm_kernel(name, kernel, bytes_per_call):
+        k = max(1, args.steps // 4)
+        kt_ = u.KernelTimer(kernel, k * (nchunks + w.Hkv + 1))
+        with kt_:
+            timed(step, k)
+        d_ = kt_.durations_ms()
+        if not d_:
+            return None
+        per_call = len(d_) // k
+        b = bytes_per_call(per_call)
+        ach = b / (sum(d_) / k / 1e3) / 1e9
+        return {"kernel": name, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm,
+                "unit": "GB/s", "frac": round(ach / hbm, 4), "launches_timed": len(d_),
+                "launches_per_call": per_call, "avg_launch_us": round(1e3 * sum(d_) / len(d_), 2),
+                "bytes_per_call": int(b)}
+
+    def wo_bytes(per_call):
+        # out (+)= O_c Wo_c^T: fp32 out read and written (written only for the
+        # first chunk), O_c and the Wo slice read once
+        first = 1 if per_call == nchunks else 0
+        rmw = (per_call - first) * 8 + first * 4
+        return per_call * 2 * (w.S + w.hidden) * ch * w.d + rmw * w.S * w.hidden
+
+    el = 12 if w.qk_norm else 8   # fp32 g (+ fp32 y-hat) read, bf16 hi + lo written
+    hbm_kernels = [hbm_kernel("gemm_kernel<F32> (Wo-slice accumulate on all SMs)", 2, wo_bytes)]
+    if mode:
+        hbm_kernels.append(hbm_kernel(
+            "qk_bwd_kernel (dQ and dK RoPE/RMSNorm backward)", 3,
+            lambda n: w.S * (w.Hq + w.Hkv) * (w.d * el + (4 if w.qk_norm else 0))))
+        hbm_kernels.append(hbm_kernel("f32_to_bf16x2_kernel (dV hi/lo split)", 4,
+                                      lambda n: w.S * w.Hkv * w.d * 8))
+    hbm_kernels = [h for h in hbm_kernels if h]
+
     # ---- the saved-O backward: the forward keeps every head's attention
     # output and the backward reuses it instead of recomputing the attention
     saved_o = None
@@ -542,6 +577,7 @@ def main():
         "saved_o_backward": saved_o,
         "roofline": roof_bwd if roof_bwd else roof_fwd,
         "roofline_attn_fwd": roof_fwd,
+        "hbm_kernels": hbm_kernels,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(sum(h.numel() * h.element_size()
                                               for h in hosts.values())),

@@ -57,77 +57,109 @@ cudaError_t launch_rope_table(float2* hi, float2* lo, float2* lo_t, long long S,
 }
 
 // ------------------------------------------------------ q/k post backward --
-// One warp per (row, head).  Lane l owns elements l + 32k, k < D/32, which
-// holds each RoPE pair (i, i + D/2) inside one lane.
+// D/8 lanes per (row, head) item, so a warp takes 32 / (D/8) items per pass.
+// Lane j of an item owns elements 4j..4j+3 and their RoPE partners
+// H+4j..H+4j+3 (H = D/2): every pair (i, i + H) stays inside one lane and each
+// access is one 16-byte load (fp32) or 8-byte store (bf16).
 //   dy = R^T g                       (RoPE transpose)
 //   norm mode, with yhat = a / r saved by the forward projection:
 //     dgamma += dy * yhat;  dyhat = dy * gamma;
 //     da = (dyhat - yhat * mean(dyhat * yhat)) * rstd
-template <int D>
+template <int D, bool NORM>
 __global__ void __launch_bounds__(256) qk_bwd_kernel(const QkBwdArgs a) {
-  constexpr int E = D / 32;
   constexpr int H = D / 2;
+  constexpr int LPR = D / 8;      // lanes per item
+  constexpr int IPW = 32 / LPR;   // items per warp pass
   __shared__ float sg[D];
   const int lane = threadIdx.x & 31;
   const int wib = threadIdx.x >> 5;
-  const bool norm = a.mode == PROJ_NORM_ROPE;
-  if (norm)
+  const int j = lane % LPR;
+  const int sub = lane / LPR;
+  constexpr bool norm = NORM;
+  if constexpr (norm) {
     for (int i = threadIdx.x; i < D; i += blockDim.x) sg[i] = 0.f;
-  __syncthreads();
-  float gam[E], dgam[E];
-#pragma unroll
-  for (int k = 0; k < E; ++k) {
-    gam[k] = (norm && a.gamma) ? a.gamma[lane + 32 * k] : 1.f;
-    dgam[k] = 0.f;
+    __syncthreads();
   }
+  // element k < 4 is column 4j + k, element 4 + k is column H + 4j + k
+  float gam[8], dgam[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    gam[k] = (norm && a.gamma) ? a.gamma[4 * j + k] : 1.f;
+    gam[4 + k] = (norm && a.gamma) ? a.gamma[H + 4 * j + k] : 1.f;
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) dgam[k] = 0.f;
   const long long items = a.S * a.heads;
-  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
-  for (long long it = blockIdx.x * (long long)(blockDim.x >> 5) + wib; it < items; it += warps) {
+  const long long step = (long long)gridDim.x * (blockDim.x >> 5) * IPW;
+  for (long long base = ((long long)blockIdx.x * (blockDim.x >> 5) + wib) * IPW; base < items;
+       base += step) {
+    // every lane runs the body (the norm mode reduces across the item's
+    // lanes); an item past the end recomputes the last one and stores nothing
+    const long long it0 = base + sub;
+    const bool live = it0 < items;
+    const long long it = live ? it0 : items - 1;
     const long long s = it / a.heads;
     const int h = (int)(it - s * a.heads);
-    const float* gp = a.g + s * a.ld_g + h * D;
-    float g[E], dy[E];
+    const float* gp = a.g + s * a.ld_g + h * D + 4 * j;
+    const float4 ga4 = *reinterpret_cast<const float4*>(gp);
+    const float4 gb4 = *reinterpret_cast<const float4*>(gp + H);
+    const float4* lo4 = reinterpret_cast<const float4*>(a.rope_lo + (s & 1023) * H + 4 * j);
+    const float4* hi4 = reinterpret_cast<const float4*>(a.rope_hi + (s >> 10) * H + 4 * j);
+    const float4 l01 = __ldg(lo4), l23 = __ldg(lo4 + 1);
+    const float4 h01 = __ldg(hi4), h23 = __ldg(hi4 + 1);
+    const float lc[4] = {l01.x, l01.z, l23.x, l23.z}, ls[4] = {l01.y, l01.w, l23.y, l23.w};
+    const float hc[4] = {h01.x, h01.z, h23.x, h23.z}, hs[4] = {h01.y, h01.w, h23.y, h23.w};
+    const float ga[4] = {ga4.x, ga4.y, ga4.z, ga4.w}, gb[4] = {gb4.x, gb4.y, gb4.z, gb4.w};
+    float dy[8];
 #pragma unroll
-    for (int k = 0; k < E; ++k) g[k] = gp[lane + 32 * k];
-#pragma unroll
-    for (int k = 0; k < E / 2; ++k) {
-      const int i = lane + 32 * k;  // first half index, partner i + H
-      const float2 lo = __ldg(a.rope_lo + (s & 1023) * H + i);
-      const float2 hi = __ldg(a.rope_hi + (s >> 10) * H + i);
-      const float c = hi.x * lo.x - hi.y * lo.y;
-      const float sn = hi.y * lo.x + hi.x * lo.y;
-      const float ga = g[k], gb = g[k + E / 2];
-      dy[k] = ga * c + gb * sn;
-      dy[k + E / 2] = gb * c - ga * sn;
+    for (int k = 0; k < 4; ++k) {
+      const float c = hc[k] * lc[k] - hs[k] * ls[k];
+      const float sn = hs[k] * lc[k] + hc[k] * ls[k];
+      dy[k] = ga[k] * c + gb[k] * sn;
+      dy[4 + k] = gb[k] * c - ga[k] * sn;
     }
-    bf16* op = a.out + s * a.ld_out + h * D;
-    bf16* lp = a.out_lo + s * a.ld_out + h * D;
-    if (norm) {
-      const float* yp = a.yhat + s * a.ld_yhat + h * D;
+    if constexpr (norm) {
+      const float* yp = a.yhat + s * a.ld_yhat + h * D + 4 * j;
+      const float4 ya4 = *reinterpret_cast<const float4*>(yp);
+      const float4 yb4 = *reinterpret_cast<const float4*>(yp + H);
+      const float yh[8] = {ya4.x, ya4.y, ya4.z, ya4.w, yb4.x, yb4.y, yb4.z, yb4.w};
       const float rs = a.rstd[(long long)h * a.S + s];
-      float yh[E], dot = 0.f;
+      float dot = 0.f;
 #pragma unroll
-      for (int k = 0; k < E; ++k) {
-        yh[k] = yp[lane + 32 * k];
-        dgam[k] = fmaf(dy[k], yh[k], dgam[k]);
+      for (int k = 0; k < 8; ++k) {
+        if (live) dgam[k] = fmaf(dy[k], yh[k], dgam[k]);
         dot = fmaf(dy[k] * gam[k], yh[k], dot);
       }
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+      for (int off = LPR / 2; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
       const float mean = dot * (1.0f / D);
 #pragma unroll
-      for (int k = 0; k < E; ++k) dy[k] = (dy[k] * gam[k] - yh[k] * mean) * rs;
+      for (int k = 0; k < 8; ++k) dy[k] = (dy[k] * gam[k] - yh[k] * mean) * rs;
     }
+    if (live) {
+      const long long o = s * a.ld_out + h * D + 4 * j;
 #pragma unroll
-    for (int k = 0; k < E; ++k) {
-      const bf16 hi = __float2bfloat16(dy[k]);
-      op[lane + 32 * k] = hi;
-      lp[lane + 32 * k] = __float2bfloat16(dy[k] - __bfloat162float(hi));
+      for (int half = 0; half < 2; ++half) {
+        const float* v = dy + 4 * half;
+        uint2 wh, wl;
+        wh.x = pack_bf16(v[0], v[1]);
+        wh.y = pack_bf16(v[2], v[3]);
+        const float2 h0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wh.x));
+        const float2 h1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wh.y));
+        wl.x = pack_bf16(v[0] - h0.x, v[1] - h0.y);
+        wl.y = pack_bf16(v[2] - h1.x, v[3] - h1.y);
+        *reinterpret_cast<uint2*>(a.out + o + half * H) = wh;
+        *reinterpret_cast<uint2*>(a.out_lo + o + half * H) = wl;
+      }
     }
   }
-  if (norm && a.dgamma) {
+  if constexpr (norm) {
+    if (!a.dgamma) return;
 #pragma unroll
-    for (int k = 0; k < E; ++k) atomicAdd(&sg[lane + 32 * k], dgam[k]);
+    for (int k = 0; k < 4; ++k) {
+      atomicAdd(&sg[4 * j + k], dgam[k]);
+      atomicAdd(&sg[H + 4 * j + k], dgam[4 + k]);
+    }
     __syncthreads();
     for (int i = threadIdx.x; i < D; i += blockDim.x) atomicAdd(a.dgamma + i, sg[i]);
   }
@@ -135,44 +167,69 @@ __global__ void __launch_bounds__(256) qk_bwd_kernel(const QkBwdArgs a) {
 
 cudaError_t launch_qk_bwd(const QkBwdArgs& a, cudaStream_t stream) {
   if (a.S <= 0 || a.heads <= 0) return cudaSuccess;
+  if (a.d != 128 && a.d != 64) return cudaErrorNotSupported;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long items = a.S * a.heads;
-  const int blocks = (int)std::min<long long>((items + 7) / 8, (long long)sms * 8);
-  if (a.d == 128) qk_bwd_kernel<128><<<blocks, 256, 0, stream>>>(a);
-  else if (a.d == 64) qk_bwd_kernel<64><<<blocks, 256, 0, stream>>>(a);
-  else return cudaErrorNotSupported;
+  const long long per_block = 8LL * (32 / (a.d / 8));   // 8 warps, 32 / (d/8) items each
+  const int blocks =
+      (int)std::min<long long>((items + per_block - 1) / per_block, (long long)sms * 8);
+  const bool norm = a.mode == PROJ_NORM_ROPE;
+  if (a.d == 128 && norm) qk_bwd_kernel<128, true><<<blocks, 256, 0, stream>>>(a);
+  else if (a.d == 128) qk_bwd_kernel<128, false><<<blocks, 256, 0, stream>>>(a);
+  else if (norm) qk_bwd_kernel<64, true><<<blocks, 256, 0, stream>>>(a);
+  else qk_bwd_kernel<64, false><<<blocks, 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
 // ---------------------------------------------------------- fp32->bf16x2 --
+// Each thread converts float4 groups t and t + stride per pass: both loads
+// are issued before either result is stored.
+__device__ __forceinline__ void split_store(const float4 v, bf16* hi, bf16* lo) {
+  uint2 wh, wl;
+  wh.x = pack_bf16(v.x, v.y);
+  wh.y = pack_bf16(v.z, v.w);
+  const float2 h0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wh.x));
+  const float2 h1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wh.y));
+  wl.x = pack_bf16(v.x - h0.x, v.y - h0.y);
+  wl.y = pack_bf16(v.z - h1.x, v.w - h1.y);
+  *reinterpret_cast<uint2*>(hi) = wh;
+  *reinterpret_cast<uint2*>(lo) = wl;
+}
+
 __global__ void f32_to_bf16x2_kernel(const float* __restrict__ in, int ld_in,
                                      bf16* __restrict__ hi, bf16* __restrict__ lo, int ld_out,
                                      long long S, int cols4) {
   const long long total = S * cols4;
+  const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
-       t += (long long)gridDim.x * blockDim.x) {
+       t += 2 * stride) {
+    const long long t2 = t + stride;
     const long long r = t / cols4;
     const int c = (int)(t - r * cols4) * 4;
     const float4 v = *reinterpret_cast<const float4*>(in + r * ld_in + c);
-    uint2 wh, wl;
-    wh.x = pack_bf16(v.x, v.y);
-    wh.y = pack_bf16(v.z, v.w);
-    const float2 h0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wh.x));
-    const float2 h1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wh.y));
-    wl.x = pack_bf16(v.x - h0.x, v.y - h0.y);
-    wl.y = pack_bf16(v.z - h1.x, v.w - h1.y);
-    *reinterpret_cast<uint2*>(hi + r * ld_out + c) = wh;
-    *reinterpret_cast<uint2*>(lo + r * ld_out + c) = wl;
+    long long r2 = 0;
+    int c2 = 0;
+    float4 v2 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t2 < total) {
+      r2 = t2 / cols4;
+      c2 = (int)(t2 - r2 * cols4) * 4;
+      v2 = *reinterpret_cast<const float4*>(in + r2 * ld_in + c2);
+    }
+    split_store(v, hi + r * ld_out + c, lo + r * ld_out + c);
+    if (t2 < total) split_store(v2, hi + r2 * ld_out + c2, lo + r2 * ld_out + c2);
   }
 }
 
 cudaError_t launch_f32_to_bf16x2(const float* in, int ld_in, bf16* hi, bf16* lo, int ld_out,
                                  long long S, int cols, cudaStream_t stream) {
   if (S <= 0 || cols <= 0) return cudaSuccess;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long total = S * (cols / 4);
-  const int blocks = (int)std::min<long long>((total + 255) / 256, 152 * 16);
+  const int blocks = (int)std::min<long long>((total + 511) / 512, (long long)sms * 8);
   f32_to_bf16x2_kernel<<<blocks, 256, 0, stream>>>(in, ld_in, hi, lo, ld_out, S, cols / 4);
   return cudaGetLastError();
 }

@@ -453,7 +453,9 @@ static int attn_fwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
     ev.side = side;
     ev.caller = st;
   }
-  auto out_gemm = [&](int c, cudaStream_t s, int sms) -> int {
+  // timed: the measurement hook's kernel 2 covers the accumulates that run on
+  // the call's stream with every SM, not the ones beside the next attention
+  auto out_gemm = [&](int c, cudaStream_t s, int sms, bool timed) -> int {
     const int h0 = c * g.ch;
     const bf16* O = o_all ? o_all + (size_t)h0 * g.d : QO[c & 1];
     const int ldo = o_all ? g.Hq * g.d : g.ch * g.d;
@@ -467,8 +469,10 @@ static int attn_fwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
     ep.ldc = g.hidden;
     ep.beta = c > 0;
     GemmArgs ga{(int)g.S, g.hidden, g.ch * g.d, 1, g.d};
+    if (timed) prof_begin(2, s);
     UPIPE_CUDA(launch_gemm(out_bn, false, false, EPI_F32, &om, 1, &wom, 1, ga, ep, ds->err, sms, s,
                            &outmap));
+    if (timed) prof_end(2, s);
     return UPIPE_OK;
   };
   for (int c = 0; c < g.nchunks; ++c) {
@@ -483,20 +487,20 @@ static int attn_fwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
     if (overlap && c >= 1) {
       UPIPE_CUDA(cudaEventRecord(ev.proj, st));
       UPIPE_CUDA(cudaStreamWaitEvent(side, ev.proj, 0));
-      UPIPE_TRY(out_gemm(c - 1, side, side_sms(ds->num_sms)));
+      UPIPE_TRY(out_gemm(c - 1, side, side_sms(ds->num_sms), false));
       UPIPE_CUDA(cudaEventRecord(ev.out[(c - 1) & 1], side));
     }
     bf16* O = o_all ? o_all + (size_t)h0 * g.d : Qc;
     const int ldo = o_all ? g.Hq * g.d : g.ch * g.d;
     UPIPE_TRY(attention_chunk(g, ds, st, Qc, K, V, h0, kv0, O, ldo, lse + (size_t)h0 * g.S,
                               flush));
-    if (!overlap && c + 1 < g.nchunks) UPIPE_TRY(out_gemm(c, st, ds->num_sms));
+    if (!overlap && c + 1 < g.nchunks) UPIPE_TRY(out_gemm(c, st, ds->num_sms, true));
   }
   if (overlap) {
     UPIPE_CUDA(cudaStreamWaitEvent(st, ev.out[(g.nchunks - 2) & 1], 0));
     ev.joined = true;
   }
-  UPIPE_TRY(out_gemm(g.nchunks - 1, st, ds->num_sms));
+  UPIPE_TRY(out_gemm(g.nchunks - 1, st, ds->num_sms, true));
   return UPIPE_OK;
 }
 
@@ -769,7 +773,9 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
       q.dgamma = dq_norm_w;
       q.rope_hi = rhi;
       q.rope_lo = rlo;
+      prof_begin(3, st);
       UPIPE_CUDA(launch_qk_bwd(q, st));
+      prof_end(3, st);
     }
     const bf16* Wq_c = Wq + (size_t)h0 * d * g.hidden;
     DxSeg dxs[kMaxASegs] = {{dO, g.ch * d, Wq_c}, {Ows, g.ch * d, Wq_c}};
@@ -796,8 +802,12 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
       q.dgamma = dk_norm_w;
       q.rope_hi = rhi;
       q.rope_lo = rlo;
+      prof_begin(3, st);
       UPIPE_CUDA(launch_qk_bwd(q, st));
+      prof_end(3, st);
+      prof_begin(4, st);
       UPIPE_CUDA(launch_f32_to_bf16x2(dV, g.kvc * d, V, dVlo, g.kvc * d, g.S, g.kvc * d, st));
+      prof_end(4, st);
       const bf16* Wk_g = Wk + (size_t)kv0 * d * g.hidden;
       const bf16* Wv_g = Wv + (size_t)kv0 * d * g.hidden;
       float* dWk_g = dWk + (size_t)kv0 * d * g.hidden;

@@ -8,7 +8,7 @@ import torch
 
 import oracle as O
 from workloads import WORKLOADS, Workload, make_inputs
-from tests._util import f64, assert_close
+from tests._util import f64, assert_close, GAIN_MAX_REL, GAIN_MEAN_REL
 
 pytestmark = pytest.mark.gpu
 
@@ -56,6 +56,9 @@ CASES = [
               chunk_heads=(1, 2, 4), rope_theta=1e6, qk_norm=True), (1, 4)),
     (Workload("d64-mha-s333", S=333, hidden=256, Hq=2, Hkv=2, d=64,
               chunk_heads=(1, 2), rope_theta=1e4), (1, 2)),
+    # d = 64 with the per-head RMSNorm; chunk_heads 4 spans two KV groups
+    (Workload("d64-qknorm-s389", S=389, hidden=256, Hq=4, Hkv=2, d=64,
+              chunk_heads=(1, 2, 4), rope_theta=1e6, qk_norm=True), (1, 4)),
 ]
 
 
@@ -69,7 +72,8 @@ def test_backward_matches_oracle(w, chs):
             assert_close(f64(g[name]), ref[name], f"{name} ch={ch}")
         if w.qk_norm:
             for name in ("dq_gamma", "dk_gamma"):
-                assert_close(f64(g[name]), ref[name], f"{name} ch={ch}")
+                assert_close(f64(g[name]), ref[name], f"{name} ch={ch}",
+                             GAIN_MAX_REL, GAIN_MEAN_REL)
 
 
 @pytest.mark.parametrize("w,chs", [CASES[1], CASES[2]],
@@ -87,7 +91,8 @@ def test_backward_with_saved_attention_output(w, chs):
         names = ["dx", "dWq", "dWk", "dWv", "dWo"] + (["dq_gamma", "dk_gamma"]
                                                       if w.qk_norm else [])
         for name in names:
-            assert_close(f64(g[name]), ref[name], f"saved-O {name} ch={ch}")
+            bound = (GAIN_MAX_REL, GAIN_MEAN_REL) if "gamma" in name else ()
+            assert_close(f64(g[name]), ref[name], f"saved-O {name} ch={ch}", *bound)
             a, b = f64(g[name]), f64(r[name])
             scale = np.sqrt(np.mean(b ** 2)) + 1e-30
             assert np.max(np.abs(a - b)) / scale < 1e-4, f"saved-O vs recompute {name} ch={ch}"
