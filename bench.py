@@ -14,6 +14,12 @@ independent replica of the workload (the path has no exchange step on one
 GPU): ``value`` is the sum of all ranks' FLOPs over the max-over-ranks time.
 ``--impl reference`` times the float64 CPU oracle (the only reference this
 method has) on a bounded sample of the same workload.
+
+Besides the layer number the line carries ``roofline`` (the dominant
+attention kernel: algorithmic FLOPs per launch over its live CUDA-event launch
+time) and ``hbm_kernels`` (the HBM-bound kernels: algorithmic bytes per layer
+call over their summed live launch time), both timed through the library's
+measurement hook.
 """
 from __future__ import annotations
 
