@@ -22,10 +22,15 @@
 // registers the block is launched with.
 // TMEM (512 columns): S_0 | S_1 | O_0 | O_1.  P_t (bf16) is written over the
 // first half of S_t and fed to the PV MMA straight from TMEM.
-// Softmax runs in base 2 with a lazily updated row max: O and l are rescaled
-// only when the max grows by more than 8 (a factor 256), so almost every step
-// skips the O read-modify-write.  The diagonal KV tile of each query tile is
-// the only one masked; KV tiles beyond it are never loaded (causal skipping).
+// Softmax runs in base 2 with the row max taken only on demand: P is computed
+// with the running max m, and while m is the row's max every p <= 1, so the
+// tile's row sum is at most 128.  Only a sum above 256 (or inf / NaN on a
+// row's first tile, where m = -inf) makes the thread take the tile's max,
+// rescale O and l to it and recompute P.  Growth that keeps the sum within
+// 256 keeps m (p stays within 256, far inside bf16 and fp32 range), so almost
+// every step skips both the max and the O read-modify-write.
+// The diagonal KV tile of each query tile is the only one masked; KV tiles
+// beyond it are never loaded (causal skipping).
 // Grid: heaviest query blocks first, all heads of a block together.
 // Long rows: the tensor core's fp32 accumulation of O drifts over hundreds of
 // thousands of MMA steps (measured: the error grows linearly with position
@@ -50,7 +55,7 @@ __device__ __forceinline__ uint32_t sm_id() {
   asm volatile("mov.u32 %0, %%smid;" : "=r"(v));
   return v;
 }
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kSumLimit = 256.0f;  // row sum of one tile's p that asks for a new max
 
 template <int D>
 struct FwdCfg {
@@ -252,56 +257,72 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 128; ++c)
           if (c > r) s[c] = -INFINITY;
       }
-      // row max: four independent three-input chains (depth 16, not 127)
-      float mq[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) mq[k] = fmaxf(s[2 * k], s[2 * k + 1]);
-#pragma unroll
-      for (int c = 8; c < 128; c += 8)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) mq[k] = fmax3(mq[k], s[c + 2 * k], s[c + 2 * k + 1]);
-      const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
-      const float m_new = fmaxf(m_run, mx * sl2);
-      const bool need = m_new > m_run + kRescaleThreshold;
-      if (__any_sync(0xffffffffu, need) && j > 0) {
-        const float alpha = need ? ex2(m_run - m_new) : 1.f;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t rr[32];
-          tmem_ld32(o_tmem + 32 * c, rr);
-          tmem_ld_wait(rr);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-          tmem_st32(o_tmem + 32 * c, rr);
-        }
-        tmem_st_wait();
-      }
-      if (need) {
-        l_run *= ex2(m_run - m_new);
-        m_run = m_new;
-      }
-      // p = 2^(s * scale_log2 - m): pairs through one packed FMA each; the
-      // row sum in four packed partial sums (depth 16)
+      // p = 2^(s * scale_log2 - m_run) with the running max: pairs through one
+      // packed FMA each, the row sum in four packed partial sums (depth 16).
+      // Writes P (bf16) over S in TMEM and returns the row sum.
       const float2 sc2 = make_float2(sl2, sl2);
-      const float2 nm2 = make_float2(-m_run, -m_run);
-      float2 ps[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                      make_float2(0.f, 0.f)};
+      auto p_tile = [&](float m) -> float {
+        const float2 nm2 = make_float2(-m, -m);
+        float2 ps[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                        make_float2(0.f, 0.f)};
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float2 x = ffma2(make_float2(s[64 * h + 2 * i], s[64 * h + 2 * i + 1]), sc2, nm2);
-          x.x = ex2(x.x);
-          x.y = ex2(x.y);
-          ps[i & 3] = fadd2(ps[i & 3], x);
-          pk[i] = pack_bf16(x.x, x.y);
+          for (int i = 0; i < 32; ++i) {
+            float2 x = ffma2(make_float2(s[64 * h + 2 * i], s[64 * h + 2 * i + 1]), sc2, nm2);
+            x.x = ex2(x.x);
+            x.y = ex2(x.y);
+            ps[i & 3] = fadd2(ps[i & 3], x);
+            pk[i] = pack_bf16(x.x, x.y);
+          }
+          tmem_st32(s_tmem + 32 * h, pk);
         }
-        tmem_st32(s_tmem + 32 * h, pk);
+        const float2 s01 = fadd2(ps[0], ps[1]);
+        const float2 s23 = fadd2(ps[2], ps[3]);
+        return (s01.x + s23.x) + (s01.y + s23.y);
+      };
+      float l_tile = p_tile(m_run);
+      // Every p <= 1 while m_run is the row's max, so a row sum above
+      // kSumLimit (or inf / NaN: the first tile, m_run = -inf) means the
+      // max has grown.  Only then is the row max taken; O and l are rescaled
+      // to it and P is recomputed.  A smaller growth keeps m_run: its p stay
+      // below kSumLimit, far inside the range of bf16 P and the fp32 O.
+      const bool grow = !(l_tile <= kSumLimit);
+      if (__any_sync(0xffffffffu, grow)) {
+        float m_new = m_run;
+        if (grow) {
+          // four independent three-input chains (depth 16, not 127)
+          float mq[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mq[k] = fmaxf(s[2 * k], s[2 * k + 1]);
+#pragma unroll
+          for (int c = 8; c < 128; c += 8)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mq[k] = fmax3(mq[k], s[c + 2 * k], s[c + 2 * k + 1]);
+          const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+          m_new = fmaxf(m_run, mx * sl2);
+        }
+        if (j > 0) {
+          const float alpha = grow ? ex2(m_run - m_new) : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t rr[32];
+            tmem_ld32(o_tmem + 32 * c, rr);
+            tmem_ld_wait(rr);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+            tmem_st32(o_tmem + 32 * c, rr);
+          }
+        }
+        if (grow) {
+          l_run *= ex2(m_run - m_new);
+          m_run = m_new;
+        }
+        tmem_st_wait();   // the first P's stores land before they are rewritten
+        l_tile = p_tile(m_run);
       }
-      const float2 s01 = fadd2(ps[0], ps[1]);
-      const float2 s23 = fadd2(ps[2], ps[3]);
-      l_run += (s01.x + s23.x) + (s01.y + s23.y);
+      l_run += l_tile;
       if (folding && j > 0 && j % kFlushTiles == 0) {
         // O in TMEM holds PV(0 .. j-1) since the last fold, in units of m_run
         const bool have_acc = m_acc != -INFINITY;
