@@ -452,7 +452,9 @@ def main():
 
     e2e_run(2)
     k_e2e = max(2, args.steps)
-    t_e2e = timed(lambda: e2e_run(k_e2e), 1)
+    with Clocks(gpu_id) as clk_e2e:
+        t_e2e = timed(lambda: e2e_run(k_e2e), 1)
+    e2e_clocks = clk_e2e.summary()
     e2e_value = replica_throughput(flops, k_e2e, world, t_e2e)
     del dbufs, rbufs
 
@@ -588,7 +590,7 @@ def main():
                 "h2d_bytes_per_step": int(sum(h.numel() * h.element_size()
                                               for h in hosts.values())),
                 "d2h_bytes_per_step": int(res_host.numel() * res_host.element_size()),
-                "steps": k_e2e, "pipelined_buffers": nbuf},
+                "steps": k_e2e, "pipelined_buffers": nbuf, "clocks": e2e_clocks},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
