@@ -543,10 +543,16 @@ def main():
                            "skips the per-chunk attention recompute"}
         del o_all
 
-    # ---- chunk sweep: throughput and workspace against chunk_heads
+    # ---- chunk sweep: throughput and workspace against chunk_heads.  The
+    # chunk sizes are timed in order and then in reverse, and each reports
+    # the mean of its two passes: a clock that drifts through the sweep (the
+    # power cap settles over seconds) then biases no chunk size against
+    # another.
     sweep = []
     if not args.no_sweep:
-        for c in w.chunk_heads:
+        rates = {c: [] for c in w.chunk_heads}
+        info = {}
+        for c in list(w.chunk_heads) + list(reversed(w.chunk_heads)):
             sh = u.Shape.of(w, c)
             wb = u.workspace_bytes(sh, mode)
             del ws
@@ -556,9 +562,14 @@ def main():
             ws = torch.empty(wb, dtype=torch.uint8, device=dev)
             pk = torch.cuda.max_memory_allocated() - a0
             step(sh, ws)
-            k = max(2, args.steps // 3)
+            k = max(2, args.steps // 6)
             tc = timed(lambda: step(sh, ws), k)
-            sweep.append({"chunk_heads": c, "tflops": round(flops * k / tc / 1e12, 2),
+            rates[c].append(flops * k / tc / 1e12)
+            info[c] = (wb, pk)
+        for c in w.chunk_heads:
+            wb, pk = info[c]
+            sweep.append({"chunk_heads": c, "tflops": round(sum(rates[c]) / len(rates[c]), 2),
+                          "tflops_passes": [round(r, 2) for r in rates[c]],
                           "workspace_gb": round(wb / 1e9, 4), "peak_alloc_gb": round(pk / 1e9, 4)})
 
     launches_per_step = 1 + 3 * nchunks
