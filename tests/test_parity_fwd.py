@@ -98,3 +98,20 @@ def test_chunked_out_close_to_unchunked():
     for ch in (3, 6):
         out, _, _ = run_fwd(w, ch, inp, debug=False)
         assert_close(f64(out), f64(ref), f"out ch={ch} vs ch=24", 1e-3, 1e-4)
+
+
+@pytest.mark.parametrize("alpha", [2.0, 6.0])
+def test_forward_row_max_growing_late_in_rows(alpha):
+    # The hidden rows of keys 900..1019 are scaled by alpha, so their scores
+    # are alpha times larger.  For every later query the row max then jumps
+    # in the eighth KV tile: at alpha = 6 by many powers of two (the kernel
+    # must take the tile's max and rescale O and l mid-row); at alpha = 2 by
+    # little enough that it may keep its running max with p above 1.
+    w = Workload("late-max", S=1500, hidden=256, Hq=2, Hkv=1, d=128, chunk_heads=(1, 2),
+                 rope_theta=1e4)
+    inp = make_inputs(w, seed=11)
+    x = inp["x"].float()
+    x[900:1020] *= alpha
+    inp["x"] = x.to(torch.bfloat16)
+    for ch in w.chunk_heads:
+        check_full(w, ch, inp)
