@@ -456,6 +456,18 @@ def main():
         t_e2e = timed(lambda: e2e_run(k_e2e), 1)
     e2e_clocks = clk_e2e.summary()
     e2e_value = replica_throughput(flops, k_e2e, world, t_e2e)
+    # the host link as this process sees it (other jobs share it): one
+    # upload and one download alone, after the e2e region
+    def copy_gbs(dst, src):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        dst.copy_(src, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        return src.numel() * src.element_size() / (e0.elapsed_time(e1) / 1e3) / 1e9
+    h2d_gbs = copy_gbs(dbufs[0][in_names[0]], hosts[in_names[0]])
+    d2h_gbs = copy_gbs(res_host, rbufs[0])
     del dbufs, rbufs
 
     # ---- roofline of the attention kernels (algorithmic FLOPs per launch over
@@ -601,7 +613,8 @@ def main():
                 "h2d_bytes_per_step": int(sum(h.numel() * h.element_size()
                                               for h in hosts.values())),
                 "d2h_bytes_per_step": int(res_host.numel() * res_host.element_size()),
-                "steps": k_e2e, "pipelined_buffers": nbuf, "clocks": e2e_clocks},
+                "steps": k_e2e, "pipelined_buffers": nbuf, "clocks": e2e_clocks,
+                "h2d_gbs": round(h2d_gbs, 1), "d2h_gbs": round(d2h_gbs, 1)},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
