@@ -55,6 +55,15 @@ def layer_flops(w, mode="fwd"):
     return proj + attn + wo + bwd, attn
 
 
+def recompute_flops(w, saved_o=False):
+    """FLOPs the backward executes beyond the model count: it projects each
+    chunk's Q/K/V again and, unless the forward's attention output is saved,
+    runs the chunk's attention forward again."""
+    S, hid, d = w.S, w.hidden, w.d
+    proj = 2.0 * S * hid * d * (w.Hq + 2 * w.Hkv)
+    return proj if saved_o else proj + 4.0 * d * w.Hq * S * (S + 1) / 2
+
+
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
 # ncu capture, keyed by kernel, workload and chunk size, with the sha256 of the
 # kernel's source file at capture time: a changed kernel reports null.
@@ -548,7 +557,9 @@ def main():
         step_saved_o()
         k = max(1, args.steps // 2)
         ts = timed(step_saved_o, k)
-        saved_o = {"tflops": round(replica_throughput(flops, k, world, ts), 2),
+        so_tf = replica_throughput(flops, k, world, ts)
+        saved_o = {"tflops": round(so_tf, 2),
+                   "hardware_tflops": round(so_tf * (flops + recompute_flops(w, True)) / flops, 2),
                    "ms_per_step": round(1e3 * ts / k, 3), "steps": k,
                    "extra_bytes": int(o_all.numel() * 2),
                    "note": "forward keeps the [S, Hq*d] bf16 attention output; the backward "
@@ -602,6 +613,11 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": config_of(w, ch, args),
         "frac_of_bf16_peak": round(value / world / burst, 4),
+        # model FLOPs count each unmasked (query, key) pair and each GEMM once;
+        # hardware FLOPs add what the backward recomputes
+        "flops_per_step": {"model": flops,
+                           "hardware": flops + (recompute_flops(w) if mode else 0.0)},
+        "hardware_tflops": round(value * (flops + (recompute_flops(w) if mode else 0.0)) / flops, 2),
         "peak_workspace_gb": round(peak_ws / 1e9, 4),
         "workspace_gb_planned": round(u.workspace_bytes(shape, mode) / 1e9, 4),
         "chunk_sweep": sweep,
