@@ -643,7 +643,10 @@ def main():
                                 "sample": f"float64 oracle: full K/V projection of {groups} kv "
                                           f"head(s) + {nrows} seeded random query rows of each "
                                           "of their query heads (attention over all earlier "
-                                          "keys), batches of 256 rows until 12 s of CPU work"}
+                                          "keys), batches of 256 rows until 12 s of CPU work",
+                                # the whole layer at the sample's rate: an
+                                # extrapolation, not a measurement
+                                "full_layer_seconds_extrapolated": round(flops / (v * 1e12), 1)}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
