@@ -540,6 +540,21 @@ def main():
                                       lambda n: w.S * w.Hkv * w.d * 8))
     hbm_kernels = [h for h in hbm_kernels if h]
 
+    # ---- paired accumulates: the forward given the third chunk buffer
+    # (upipe_workspace_bytes mode 2) adds two chunks per Wo-slice accumulate
+    paired = None
+    if not mode and nchunks >= 3:
+        ws2 = torch.empty(u.workspace_bytes(shape, 2), dtype=torch.uint8, device=dev)
+        step(shape, ws2)
+        k = max(2, args.steps // 4)
+        tp = timed(lambda: step(shape, ws2), k)
+        paired = {"tflops": round(replica_throughput(flops, k, world, tp), 2),
+                  "ms_per_step": round(1e3 * tp / k, 3), "steps": k,
+                  "workspace_gb": round(ws2.numel() / 1e9, 4),
+                  "note": "a third chunk buffer lets each Wo-slice accumulate add two chunks, "
+                          "halving the fp32 read-modify-write passes over out"}
+        del ws2
+
     # ---- the saved-O backward: the forward keeps every head's attention
     # output and the backward reuses it instead of recomputing the attention
     saved_o = None
@@ -622,6 +637,7 @@ def main():
         "workspace_gb_planned": round(u.workspace_bytes(shape, mode) / 1e9, 4),
         "chunk_sweep": sweep,
         "saved_o_backward": saved_o,
+        "paired_accumulate": paired,
         "roofline": roof_bwd if roof_bwd else roof_fwd,
         "roofline_attn_fwd": roof_fwd,
         "hbm_kernels": hbm_kernels,

@@ -193,6 +193,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 struct Layout {
   size_t rope_hi, rope_lo, rope_lo_t, q, k, v, o, flush;     // forward
+  size_t o2;                                               // forward, mode 2
   size_t dO, D, dq, dk, dv, dklo, dvlo, yq, rq, yk, rk;  // backward
   size_t total;
 };
@@ -215,6 +216,8 @@ Layout plan(const Geo& g, int mode) {
   L.o = take(S * ch * d * 2);
   // per-SM fp32 rows into which long attention rows fold their O accumulator
   L.flush = S > (size_t)kFlushTiles * 128 ? take((size_t)kFlushSlots * 256 * d * 4) : (size_t)-1;
+  // mode 2: a third chunk buffer, last so that every other offset is mode 0's
+  L.o2 = mode == 2 ? take(S * ch * d * 2) : (size_t)-1;
   if (mode == 1) {
     L.dO = take(S * ch * d * 2);
     L.D = take(ch * S * 4);
@@ -386,7 +389,7 @@ using namespace upipe;
 
 extern "C" size_t upipe_workspace_bytes(const upipe_shape_t* shape, int mode) {
   Geo g;
-  if (mode != 0 && mode != 1) return 0;
+  if (mode < 0 || mode > 2) return 0;
   if (check_shape(shape, &g) != UPIPE_OK) return 0;
   return plan(g, mode).total;
 }
@@ -414,8 +417,9 @@ static int attn_fwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
                         (const void*)q_norm_w, (const void*)k_norm_w})
     if (p && !aligned16(p)) return UPIPE_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return UPIPE_ERR_INVALID_ARG;
-  const Layout L = plan(g, 0);
-  if (ws_bytes < L.total) return UPIPE_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_bytes < plan(g, 0).total) return UPIPE_ERR_WORKSPACE_TOO_SMALL;
+  const bool third = ws_bytes >= plan(g, 2).total;
+  const Layout L = plan(g, third ? 2 : 0);
   DeviceState* ds = nullptr;
   UPIPE_TRY(device_state(&ds));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -444,9 +448,17 @@ static int attn_fwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
   // caller's stream with every SM, after the side stream's work.  Without the
   // side stream each accumulate follows its chunk's attention on the caller's
   // stream.
-  bf16* QO[2] = {Q, Ows};
+  // Paired accumulates: with three or more chunks, a side stream and room
+  // for the chunks' O (a third buffer, or the caller's attn_o), one GEMM adds
+  // chunks c - 2 and c - 1 (K = 2 ch d) beside chunk c's attention, which
+  // halves the fp32 read-modify-write passes over out.  Chunk c then projects
+  // into buffer c % 3, whose previous chunk c - 3 belongs to the pair added
+  // beside chunk c - 1 or c - 2.
+  bf16* QO[3] = {Q, Ows, third ? at<bf16>(workspace, L.o2) : nullptr};
   cudaStream_t side = (fork && g.nchunks > 1) ? side_stream(ds) : nullptr;
   const bool overlap = side != nullptr;
+  const bool pair = overlap && g.nchunks >= 3 && (o_all || third);
+  const int nbuf = (pair && !o_all) ? 3 : 2;
   Events ev;
   if (overlap) {
     UPIPE_CUDA(ev.create());
@@ -457,7 +469,7 @@ static int attn_fwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
   // the call's stream with every SM, not the ones beside the next attention
   auto out_gemm = [&](int c, cudaStream_t s, int sms, bool timed) -> int {
     const int h0 = c * g.ch;
-    const bf16* O = o_all ? o_all + (size_t)h0 * g.d : QO[c & 1];
+    const bf16* O = o_all ? o_all + (size_t)h0 * g.d : QO[c % nbuf];
     const int ldo = o_all ? g.Hq * g.d : g.ch * g.d;
     // out (+)= O_c Wo[:, h0*d : (h0+ch)*d]^T  (the chunk's partial result)
     CUtensorMap om, wom;
@@ -475,16 +487,56 @@ static int attn_fwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
     if (timed) prof_end(2, s);
     return UPIPE_OK;
   };
+  // out (+)= O_c0 Wo_c0^T + O_c0+1 Wo_c0+1^T: two K segments, one per chunk
+  auto out_gemm_pair = [&](int c0, cudaStream_t s, int sms, bool timed) -> int {
+    CUtensorMap om[2], wom[2];
+    for (int i = 0; i < 2; ++i) {
+      const int h0 = (c0 + i) * g.ch;
+      const bf16* O = o_all ? o_all + (size_t)h0 * g.d : QO[(c0 + i) % nbuf];
+      const int ldo = o_all ? g.Hq * g.d : g.ch * g.d;
+      UPIPE_MAP(&om[i], O, g.S, (uint64_t)g.ch * g.d, ldo, 128, 64);
+      UPIPE_MAP(&wom[i], Wo + (size_t)h0 * g.d, g.hidden, (uint64_t)g.ch * g.d,
+                (uint64_t)g.Hq * g.d, out_bn, 64);
+    }
+    EpiParams ep{};
+    ep.C = out;
+    ep.ldc = g.hidden;
+    ep.beta = c0 > 0;
+    GemmArgs ga{(int)g.S, g.hidden, 2 * g.ch * g.d, 1, g.d};
+    ga.nkseg = 2;
+    ga.kseg_end[0] = g.ch * g.d / 64;
+    ga.kseg_end[1] = 2 * g.ch * g.d / 64;
+    ga.kseg_a[0] = 0;
+    ga.kseg_a[1] = 1;
+    ga.kseg_b[0] = 0;
+    ga.kseg_b[1] = 1;
+    if (timed) prof_begin(2, s);
+    UPIPE_CUDA(launch_gemm(out_bn, false, false, EPI_F32, om, 2, wom, 2, ga, ep, ds->err, sms, s,
+                           &outmap));
+    if (timed) prof_end(2, s);
+    return UPIPE_OK;
+  };
   for (int c = 0; c < g.nchunks; ++c) {
     const int h0 = c * g.ch;
     const int kv0 = h0 / g.g;
     const bool new_group = (g.ch >= g.g) || (h0 % g.g == 0);
-    bf16* Qc = QO[c & 1];
-    if (overlap && c >= 2) UPIPE_CUDA(cudaStreamWaitEvent(st, ev.out[c & 1], 0));
+    bf16* Qc = QO[c % nbuf];
+    if (pair) {
+      // buffer c % 3 last held O of chunk c - 3: wait for its pair's accumulate
+      if (!o_all && c >= 3 && (c - 3) % 2 == 0)
+        UPIPE_CUDA(cudaStreamWaitEvent(st, ev.out[((c - 3) / 2) & 1], 0));
+    } else if (overlap && c >= 2) {
+      UPIPE_CUDA(cudaStreamWaitEvent(st, ev.out[c & 1], 0));
+    }
     UPIPE_TRY(project_chunk(g, ds, st, xmap, Wq, Wk, Wv, q_norm_w, k_norm_w, shape->norm_eps, h0,
                             kv0, new_group, Qc, K, V, rhi, rlo_t, nullptr, nullptr, nullptr,
                             nullptr));
-    if (overlap && c >= 1) {
+    if (pair && c >= 2 && c % 2 == 0) {
+      UPIPE_CUDA(cudaEventRecord(ev.proj, st));
+      UPIPE_CUDA(cudaStreamWaitEvent(side, ev.proj, 0));
+      UPIPE_TRY(out_gemm_pair(c - 2, side, side_sms(ds->num_sms), false));
+      UPIPE_CUDA(cudaEventRecord(ev.out[((c - 2) / 2) & 1], side));
+    } else if (!pair && overlap && c >= 1) {
       UPIPE_CUDA(cudaEventRecord(ev.proj, st));
       UPIPE_CUDA(cudaStreamWaitEvent(side, ev.proj, 0));
       UPIPE_TRY(out_gemm(c - 1, side, side_sms(ds->num_sms), false));
@@ -495,6 +547,16 @@ static int attn_fwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
     UPIPE_TRY(attention_chunk(g, ds, st, Qc, K, V, h0, kv0, O, ldo, lse + (size_t)h0 * g.S,
                               flush));
     if (!overlap && c + 1 < g.nchunks) UPIPE_TRY(out_gemm(c, st, ds->num_sms, true));
+  }
+  if (pair) {
+    // pairs 0 .. np - 1 went to the side stream (chunks 0 .. 2 np - 1); the
+    // one or two chunks left follow on the caller's stream with every SM
+    const int np = (g.nchunks - 1) / 2;
+    UPIPE_CUDA(cudaStreamWaitEvent(st, ev.out[(np - 1) & 1], 0));
+    ev.joined = true;
+    if (g.nchunks - 2 * np == 2) UPIPE_TRY(out_gemm_pair(2 * np, st, ds->num_sms, true));
+    else UPIPE_TRY(out_gemm(g.nchunks - 1, st, ds->num_sms, true));
+    return UPIPE_OK;
   }
   if (overlap) {
     UPIPE_CUDA(cudaStreamWaitEvent(st, ev.out[(g.nchunks - 2) & 1], 0));

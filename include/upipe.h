@@ -81,6 +81,9 @@ enum {
 
 /* Workspace bytes needed by upipe_attn_fwd (mode 0) or upipe_attn_bwd
  * (mode 1) for this shape, or 0 if the shape is invalid.  Pure host function.
+ * Mode 2 is mode 0 plus a third chunk buffer (S * chunk_heads * d bf16): given
+ * that much, upipe_attn_fwd adds two chunks' partial results into out per
+ * pass (see there).
  * The bytes are affine in chunk_heads: the per-chunk Q/O (and backward) parts
  * scale with chunk_heads, the K/V part is one KV group (or chunk_heads/(Hq/Hkv)
  * groups when a chunk spans several), plus RoPE tables of
@@ -99,6 +102,12 @@ size_t upipe_workspace_bytes(const upipe_shape_t* shape, int mode);
  *         to check that o_h does not depend on chunk_heads.
  *   workspace / ws_bytes: device buffer of at least
  *         upipe_workspace_bytes(shape, 0) bytes, 256-byte aligned
+ * Paired accumulates: with three or more chunks, when the forward forks and
+ * either attn_o is given or ws_bytes >= upipe_workspace_bytes(shape, 2), each
+ * Wo-slice accumulate adds two chunks (K = 2 * chunk_heads * d) and out is
+ * read and written half as often.  out then differs from the unpaired
+ * forward by the order of its fp32 additions (~1e-7 relative); lse and the
+ * attention output are bit-identical.
  * Returns UPIPE_OK or an error code (nothing launched on error). */
 int upipe_attn_fwd(const upipe_shape_t* shape, const upipe_bf16* x, const upipe_bf16* Wq,
                    const upipe_bf16* Wk, const upipe_bf16* Wv, const upipe_bf16* Wo,

@@ -54,6 +54,8 @@ def test_workspace_closed_form(u):
                 expect += 256 * 256 * d * 4
             assert ws(u, w, ch) == expect, (w.name, ch)
             assert ws(u, w, ch, 1) > ws(u, w, ch)
+            # mode 2: the forward's third chunk buffer for paired accumulates
+            assert ws(u, w, ch, 2) == expect + al(S * ch * d * 2), (w.name, ch)
 
 
 def test_workspace_affine_in_chunk_heads_and_golden_reduction(u):

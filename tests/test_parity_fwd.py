@@ -129,3 +129,39 @@ def test_forward_row_max_growing_late_in_rows():
         assert_close(o_g[:, keep], ref["o"][:, keep], f"attention output ch={ch}")
         dl = np.abs(f64(lse)[:, keep] - ref["lse"][:, keep]).max()
         assert dl <= 6 * LSE_ABS, f"lse max abs err {dl:.3e} ch={ch}"
+
+
+@pytest.mark.parametrize("w", [
+    # 4, 3 and 6 chunks: pairs only, a pair and a single last chunk, pairs
+    # across KV groups with the per-head RMSNorm
+    Workload("pair4-s1500", S=1500, hidden=256, Hq=4, Hkv=1, d=128, chunk_heads=(1,),
+             rope_theta=1e4),
+    Workload("pair3-d64-s1000", S=1000, hidden=384, Hq=3, Hkv=1, d=64, chunk_heads=(1,),
+             rope_theta=1e4),
+    Workload("pair6-qknorm-s777", S=777, hidden=384, Hq=6, Hkv=2, d=128, chunk_heads=(1,),
+             rope_theta=1e6, qk_norm=True),
+], ids=lambda w: w.name)
+def test_paired_accumulates(w):
+    # A workspace with the third chunk buffer makes the forward add two
+    # chunks' partial results per accumulate: out within the layer's bounds
+    # of the oracle and within fp32 summation order of the unpaired forward;
+    # lse bit-identical.
+    u = U()
+    inp = make_inputs(w, seed=0, norm_gains="random")
+    t = {k: v.to("cuda") for k, v in inp.items()}
+    sh = u.Shape.of(w, 1)
+    res = {}
+    for mode in (0, 2):
+        ws = torch.empty(u.workspace_bytes(sh, mode), device="cuda", dtype=torch.uint8)
+        out = torch.empty(w.S, w.hidden, device="cuda")
+        lse = torch.empty(w.Hq, w.S, device="cuda")
+        u.attn_fwd(sh, t["x"], t["Wq"], t["Wk"], t["Wv"], t["Wo"], out, lse, ws,
+                   t.get("q_gamma"), t.get("k_gamma"))
+        torch.cuda.synchronize()
+        assert u.last_error() == 0
+        res[mode] = (f64(out), lse.cpu())
+    assert torch.equal(res[0][1], res[2][1])
+    scale = np.abs(res[0][0]).max()
+    assert np.abs(res[2][0] - res[0][0]).max() / scale < 1e-5
+    ref = oracle_fwd(w, inp, store="bf16")
+    assert_close(res[2][0], ref["out"], "paired out")
