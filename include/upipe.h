@@ -185,8 +185,9 @@ int upipe_attn_fwd_noalloc(const upipe_shape_t* shape, const upipe_bf16* x, cons
  * call's stream, for i = 0, 1, ... < capacity; later launches are not timed.
  *   kernel 0: the attention forward kernel;  kernel 1: the attention backward
  *   kernel 2: the Wo-slice accumulate GEMMs that run on the call's stream
- *             with every SM (the last chunk's; every chunk's when the
- *             forward does not fork), not those beside the next attention
+ *             with every SM (the last chunk's, or the last pair's when the
+ *             accumulates are paired; every chunk's when the forward does not
+ *             fork), not those beside the next attention
  *   kernel 3: the RoPE/RMSNorm backward of dQ (one per chunk) and of dK
  *             (one per KV group), in launch order
  *   kernel 4: the fp32 -> bf16 hi/lo split of dV (one per KV group)
