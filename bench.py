@@ -577,8 +577,9 @@ def main():
                    "hardware_tflops": round(so_tf * (flops + recompute_flops(w, True)) / flops, 2),
                    "ms_per_step": round(1e3 * ts / k, 3), "steps": k,
                    "extra_bytes": int(o_all.numel() * 2),
-                   "note": "forward keeps the [S, Hq*d] bf16 attention output; the backward "
-                           "skips the per-chunk attention recompute"}
+                   "note": "forward keeps the [S, Hq*d] bf16 attention output (and, with three "
+                           "or more chunks, pairs its Wo-slice accumulates); the backward skips "
+                           "the per-chunk attention recompute"}
         del o_all
 
     # ---- chunk sweep: throughput and workspace against chunk_heads.  The
