@@ -13,7 +13,9 @@ _lib = None
 
 ERR_NAMES = {0: "UPIPE_OK", 1: "UPIPE_ERR_INVALID_ARG", 2: "UPIPE_ERR_UNSUPPORTED",
              3: "UPIPE_ERR_WORKSPACE_TOO_SMALL", 4: "UPIPE_ERR_CUDA",
-             5: "UPIPE_ERR_DEVICE_TIMEOUT"}
+             5: "UPIPE_ERR_DEVICE_TIMEOUT", 6: "UPIPE_ERR_RANGE"}
+ERR_DEVICE_TIMEOUT = 5
+ERR_RANGE = 6
 
 
 class UpipeError(RuntimeError):

@@ -10,6 +10,15 @@
 // dimanyen.com "activation checkpointing"; per-chunk recomputation of the
 // heads, memeeeeeex.com "Untied Ulysses (UPipe)").
 //
+// Precision: Q, K, V and dO arrive in fp16 and P and dS are written in fp16,
+// so every MMA here is an fp16 MMA with fp32 accumulation (11 significant bits
+// in each operand; bf16 has 8).  fp16's range is narrow, so P, dO and dS carry
+// exact power-of-two factors (see "backward fp16 scales" in internal.h):
+//   P'' = rho P (rho = 2^14, folded into the LSE), dO' = sigma dO (applied by
+//   the dO GEMM), dS'' = P'' (lambda dP' - lambda D') (lambda folded into the
+//   packed FMA that subtracts D), so dV'' = rho sigma dV and dQ'', dK'' =
+//   lambda rho sigma dQ, dK; the epilogue divides the factors out.
+//
 // One CTA owns 128 keys (one KV tile) of one head and walks the queries from
 // its diagonal to the end of the sequence in sub-tiles of 64.  Two TMEM slots
 // alternate between sub-tiles, each with its own warpgroup, so that the
@@ -30,8 +39,8 @@
 // 65536, the registers the block is launched with (512 threads x 128).
 // TMEM (512 columns), slot s in {0, 1} at column 128 s, two 64-column blocks
 // per slot; for sub-tile u, with b = (u >> 1) & 1:
-//   block b     S^T_u = K Q_u^T (fp32); then P^T_u (bf16, +0..31) and
-//               dS^T_u (bf16, +32..63), A operands of the dV / dK MMAs; then
+//   block b     S^T_u = K Q_u^T (fp32); then P^T_u (fp16, +0..31) and
+//               dS^T_u (fp16, +32..63), A operands of the dV / dK MMAs; then
 //               dQ^T_u = K^T dS^T_u (fp32)
 //   block 1-b   dP^T_u = V dO_u^T (fp32)
 //   [256, 256+d) dV accumulator      [384, 384+d) dK accumulator
@@ -71,7 +80,7 @@ struct BwdCfg {
   static constexpr uint32_t V_OFF = KV_TILE;
   static constexpr uint32_t ST_OFF = 2 * KV_TILE;        // NST x (Q tile, dO tile)
   static constexpr uint32_t ST_BYTES = 2 * Q_TILE;
-  static constexpr uint32_t DS_OFF = ST_OFF + NST * ST_BYTES;   // 2 x [128 keys][64 q] bf16
+  static constexpr uint32_t DS_OFF = ST_OFF + NST * ST_BYTES;   // 2 x [128 keys][64 q] fp16
   static constexpr uint32_t DS_BYTES = BK * BQ * 2;
   // 4 epilogue warps x 4 buffers x [16 q][32 d] fp32
   static constexpr uint32_t DQS_OFF = DS_OFF + 2 * DS_BYTES;
@@ -188,9 +197,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
   } else if (warp == kWarpMma) {
     // ---------------------------------------------------------- MMA issue
     {  // whole warp; one elected lane issues
-      constexpr uint32_t ID_S = idesc_bf16(128, BQ, false, false);   // S^T, dP^T
-      constexpr uint32_t ID_ACC = idesc_bf16(128, D, false, true);   // dV, dK (A in TMEM)
-      constexpr uint32_t ID_DQ = idesc_bf16(128, BQ, true, true);    // dQ^T = K^T dS^T
+      constexpr uint32_t ID_S = idesc_f16(128, BQ, false, false);   // S^T, dP^T
+      constexpr uint32_t ID_ACC = idesc_f16(128, D, false, true);   // dV, dK (A in TMEM)
+      constexpr uint32_t ID_DQ = idesc_f16(128, BQ, true, true);    // dQ^T = K^T dS^T
       const uint32_t kb = smem_u32(smem + Cfg::K_OFF);
       const uint32_t vb = smem_u32(smem + Cfg::V_OFF);
       bool ok = mbar_wait_warp(kv_full, 0, err, abort_flag);
@@ -264,6 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
     const uint32_t slot = tmem + lane_off + 128 * wg;
     const float sl2 = a.scale * 1.4426950408889634f;
     const float2 sl2x2 = make_float2(sl2, sl2);
+    const float lam = grad_lambda(*a.do_max, *a.vmax);
+    const float2 lam2 = make_float2(lam, lam);
     const float* lse_g = a.lse + (long long)head * a.lse_stride;
     const float* D_g = a.D + (long long)head * S;
     // lse/D of the current sub-tile, shared by the warpgroup and double-buffered
@@ -289,9 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
         const bool live = k0 + u * BQ + 32 * m + lane < S;  // queries past S: P = 0
-        // stored negated, as the packed FMA / add below take them
-        ld_w[32 * m + lane] = live ? -nl[m] * 1.4426950408889634f : -INFINITY;
-        ld_w[BQ + 32 * m + lane] = live ? -nd[m] : 0.f;
+        // stored negated, as the packed FMAs below take them: -lse (log2
+        // units) + log2(rho), so that exp2 gives P'' = rho P; and -lambda D'
+        ld_w[32 * m + lane] = live ? kGradRhoLog2 - nl[m] * 1.4426950408889634f : -INFINITY;
+        ld_w[BQ + 32 * m + lane] = live ? -lam * nd[m] : 0.f;
       }
       __syncwarp();
       if (u + 2 < n_u) fetch(u + 2);
@@ -317,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
           tmem_ld_wait(rr);
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
-            const float4 l4 = lse4[(32 * h + i) / 4];  // -lse (log2 units)
+            const float4 l4 = lse4[(32 * h + i) / 4];  // log2(rho) - lse (log2 units)
             const float2 x0 = ffma2(make_float2(__uint_as_float(rr[i]), __uint_as_float(rr[i + 1])),
                                     sl2x2, make_float2(l4.x, l4.y));
             const float2 x1 = ffma2(make_float2(__uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3])),
@@ -337,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
         {
           uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(p[2 * i], p[2 * i + 1]);
+          for (int i = 0; i < 16; ++i) pk[i] = pack_f16(p[2 * i], p[2 * i + 1]);
           tmem_st16(sblk + 16 * h, pk);
         }
         {
@@ -346,15 +358,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
           tmem_ld_wait(rr);
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
-            const float4 d4 = dd4[(32 * h + i) / 4];  // -D
+            const float4 d4 = dd4[(32 * h + i) / 4];  // -lambda D'
+            // dS'' = P'' (lambda dP' - lambda D')
             const float2 g0 = fmul2(make_float2(p[i], p[i + 1]),
-                                    fadd2(make_float2(__uint_as_float(rr[i]), __uint_as_float(rr[i + 1])),
-                                          make_float2(d4.x, d4.y)));
+                                    ffma2(make_float2(__uint_as_float(rr[i]), __uint_as_float(rr[i + 1])),
+                                          lam2, make_float2(d4.x, d4.y)));
             const float2 g1 = fmul2(make_float2(p[i + 2], p[i + 3]),
-                                    fadd2(make_float2(__uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3])),
-                                          make_float2(d4.z, d4.w)));
-            pk[i / 2] = pack_bf16(g0.x, g0.y);
-            pk[i / 2 + 1] = pack_bf16(g1.x, g1.y);
+                                    ffma2(make_float2(__uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3])),
+                                          lam2, make_float2(d4.z, d4.w)));
+            pk[i / 2] = pack_f16(g0.x, g0.y);
+            pk[i / 2 + 1] = pack_f16(g1.x, g1.y);
           }
           if (h == 0) {
 #pragma unroll
@@ -385,6 +398,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
     const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
     uint8_t* stage_w = smem + Cfg::DQS_OFF + qw * Cfg::NDQS * Cfg::DQS_BYTES;
     uint32_t round = 0;  // dQ staging rounds issued by this warp
+    // the exact power-of-two factors to divide out: dQ'' and dK'' carry
+    // lambda rho sigma, dV'' carries rho sigma (and dQ, dK take 1/sqrt(d))
+    const double rs = (double)kGradRho * (double)grad_sigma(a.bound);
+    const float dq_mul = (float)((double)a.scale / (rs * (double)grad_lambda(*a.do_max, *a.vmax)));
+    const float dv_mul = (float)(1.0 / rs);
     bool ok = true;
     for (int u = 0; u < n_u; ++u) {
       const int s = u & 1;
@@ -412,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
           for (int c = 0; c < DQR; ++c) {
             const int q = rd * DQR + c;   // compile-time after unrolling
             *reinterpret_cast<float*>(buf + c * 128 + ((cb ^ (c & 7)) << 4) + cw) =
-                __uint_as_float(q < 32 ? lo[q & 31] : hi[q & 31]) * a.scale;
+                __uint_as_float(q < 32 ? lo[q & 31] : hi[q & 31]) * dq_mul;
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -440,12 +458,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
           const long long off = (long long)key * a.ld_dkv + kvh * D + 32 * c;
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
-            red_add_v4_f32(a.dV + off + i, __uint_as_float(rv[i]), __uint_as_float(rv[i + 1]),
-                           __uint_as_float(rv[i + 2]), __uint_as_float(rv[i + 3]));
-            red_add_v4_f32(a.dK + off + i, __uint_as_float(rk[i]) * a.scale,
-                           __uint_as_float(rk[i + 1]) * a.scale,
-                           __uint_as_float(rk[i + 2]) * a.scale,
-                           __uint_as_float(rk[i + 3]) * a.scale);
+            red_add_v4_f32(a.dV + off + i, __uint_as_float(rv[i]) * dv_mul,
+                           __uint_as_float(rv[i + 1]) * dv_mul,
+                           __uint_as_float(rv[i + 2]) * dv_mul,
+                           __uint_as_float(rv[i + 3]) * dv_mul);
+            red_add_v4_f32(a.dK + off + i, __uint_as_float(rk[i]) * dq_mul,
+                           __uint_as_float(rk[i + 1]) * dq_mul,
+                           __uint_as_float(rk[i + 2]) * dq_mul,
+                           __uint_as_float(rk[i + 3]) * dq_mul);
           }
         }
       }

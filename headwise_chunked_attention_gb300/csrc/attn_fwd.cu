@@ -20,15 +20,22 @@
 // setmaxnreg gives the softmax warpgroups 216 registers a thread and
 // warpgroup 2 72: 2 x 128 x 216 + 128 x 72 = 64512 = 384 threads x 168, the
 // registers the block is launched with.
-// TMEM (512 columns): S_0 | S_1 | O_0 | O_1.  P_t (bf16) is written over the
+// TMEM (512 columns): S_0 | S_1 | O_0 | O_1.  P_t (fp16) is written over the
 // first half of S_t and fed to the PV MMA straight from TMEM.
+// Operands: Q, K, V arrive in fp16 and P is stored in fp16 (11 significant
+// bits; bf16 has 8), so QK^T and PV both run as fp16 MMAs with fp32
+// accumulation.  P carries a fixed factor 2^kPShift: a probability p relative
+// to the row max is stored as p * 2^8, so every p >= 2^-22 is a normal fp16
+// number (long rows hold millions of small p; without the shift those below
+// 2^-14 would lose precision or flush to zero).  l and O carry the same factor,
+// which cancels in O / l and is taken out of the LSE.
 // Softmax runs in base 2 with the row max taken only on demand: P is computed
 // with the running max m, and while m is the row's max every p <= 1, so the
-// tile's row sum is at most 128.  Only a sum above 256 (or inf / NaN on a
+// tile's row sum is at most 128.  Only a sum above 128 (or inf / NaN on a
 // row's first tile, where m = -inf) makes the thread take the tile's max,
 // rescale O and l to it and recompute P.  Growth that keeps the sum within
-// 256 keeps m (p stays within 256, far inside bf16 and fp32 range), so almost
-// every step skips both the max and the O read-modify-write.
+// 128 keeps m (p <= 128, so p * 2^8 <= 2^15 stays inside fp16's range), so
+// almost every step skips both the max and the O read-modify-write.
 // The diagonal KV tile of each query tile is the only one masked; KV tiles
 // beyond it are never loaded (causal skipping).
 // Grid: heaviest query blocks first, all heads of a block together.
@@ -55,7 +62,9 @@ __device__ __forceinline__ uint32_t sm_id() {
   asm volatile("mov.u32 %0, %%smid;" : "=r"(v));
   return v;
 }
-constexpr float kSumLimit = 256.0f;  // row sum of one tile's p that asks for a new max
+constexpr float kPShift = 8.0f;       // P is stored as p * 2^kPShift (see above)
+// shifted row sum of one tile's p that asks for a new max (128 * 2^kPShift)
+constexpr float kSumLimit = 128.0f * 256.0f;
 
 template <int D>
 struct FwdCfg {
@@ -166,8 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 8) {
     // ---------------------------------------------------------- MMA issue
     {  // whole warp; one elected lane issues
-      constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t IDESC_O = idesc_bf16(128, D, false, true);
+      constexpr uint32_t IDESC_S = idesc_f16(128, 128, false, false);
+      constexpr uint32_t IDESC_O = idesc_f16(128, D, false, true);
       const uint32_t q_base = smem_u32(smem + Cfg::Q_OFF);
       const uint32_t slot_base = smem_u32(smem + Cfg::SLOT_OFF);
       uint32_t p_phase[2] = {0, 0};
@@ -257,12 +266,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 128; ++c)
           if (c > r) s[c] = -INFINITY;
       }
-      // p = 2^(s * scale_log2 - m_run) with the running max: pairs through one
-      // packed FMA each, the row sum in four packed partial sums (depth 16).
-      // Writes P (bf16) over S in TMEM and returns the row sum.
+      // p = 2^(s * scale_log2 - m_run + kPShift) with the running max: pairs
+      // through one packed FMA each, the row sum in four packed partial sums
+      // (depth 16).  Writes P (fp16) over S in TMEM and returns the row sum.
       const float2 sc2 = make_float2(sl2, sl2);
       auto p_tile = [&](float m) -> float {
-        const float2 nm2 = make_float2(-m, -m);
+        const float2 nm2 = make_float2(kPShift - m, kPShift - m);
         float2 ps[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                         make_float2(0.f, 0.f)};
 #pragma unroll
@@ -274,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             x.x = ex2(x.x);
             x.y = ex2(x.y);
             ps[i & 3] = fadd2(ps[i & 3], x);
-            pk[i] = pack_bf16(x.x, x.y);
+            pk[i] = pack_f16(x.x, x.y);
           }
           tmem_st32(s_tmem + 32 * h, pk);
         }
@@ -286,8 +295,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Every p <= 1 while m_run is the row's max, so a row sum above
       // kSumLimit (or inf / NaN: the first tile, m_run = -inf) means the
       // max has grown.  Only then is the row max taken; O and l are rescaled
-      // to it and P is recomputed.  A smaller growth keeps m_run: its p stay
-      // below kSumLimit, far inside the range of bf16 P and the fp32 O.
+      // to it and P is recomputed.  A smaller growth keeps m_run: its shifted
+      // p stay below kSumLimit = 2^15, inside the range of fp16 P.
       const bool grow = !(l_tile <= kSumLimit);
       if (__any_sync(0xffffffffu, grow)) {
         float m_new = m_run;
@@ -388,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (live && a.lse)
         a.lse[(long long)head * a.lse_stride + qpos] =
-            (m_run + __log2f(l_run)) * 0.69314718055994531f;
+            (m_run - kPShift + __log2f(l_run)) * 0.69314718055994531f;
     }
   }
 

@@ -2,7 +2,8 @@
 //   * the RoPE angle table (built in float64, stored as fp32 cos/sin pairs);
 //   * the backward of the q/k post-processing: RoPE transpose, then (Qwen3
 //     geometry) the RMSNorm backward with its gain gradient;
-//   * fp32 -> bf16 hi/lo split of an accumulated gradient.
+//   * fp32 -> bf16 hi/lo split of an accumulated gradient;
+//   * the norm bounds behind the backward's fp16 gradient scale.
 // Gradients leave these kernels as two bf16 tensors, hi = bf16(v) and
 // lo = bf16(v - hi), which the dX / dW GEMMs consume as two bf16 operands: the
 // tensor cores then see ~16 significant bits of the fp32 gradient instead of 8.
@@ -231,6 +232,72 @@ cudaError_t launch_f32_to_bf16x2(const float* in, int ld_in, bf16* hi, bf16* lo,
   const long long total = S * (cols / 4);
   const int blocks = (int)std::min<long long>((total + 511) / 512, (long long)sms * 8);
   f32_to_bf16x2_kernel<<<blocks, 256, 0, stream>>>(in, ld_in, hi, lo, ld_out, S, cols / 4);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------- gradient bounds --
+// The backward's fp16 scale of dO (internal.h, "backward fp16 scales") needs
+// max_i ||dout_i||_2 and max_j ||Wo[:, j]||_2.  Blocks [0, row_blocks) take
+// dout rows, one warp per row with 16-byte loads (hidden is a multiple of
+// 128); each later block takes 32 columns of Wo with 8 warps over its rows
+// (consecutive columns per warp: coalesced), then reduces the 8 partial sums.
+__global__ void __launch_bounds__(256)
+    grad_bound_kernel(const bf16* __restrict__ dout, long long S, int hidden,
+                      const bf16* __restrict__ Wo, int ncols, int row_blocks,
+                      float* __restrict__ bound) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if ((int)blockIdx.x < row_blocks) {
+    float mx = 0.f;
+    for (long long r = (long long)blockIdx.x * 8 + warp; r < S; r += (long long)row_blocks * 8) {
+      const bf16* row = dout + r * hidden;
+      float ss = 0.f;
+      for (int c = lane * 8; c < hidden; c += 256) {
+        const uint4 v = *reinterpret_cast<const uint4*>(row + c);
+        const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = __bfloat1622float2(p2[k]);
+          ss = fmaf(f.x, f.x, ss);
+          ss = fmaf(f.y, f.y, ss);
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+      mx = fmaxf(mx, ss);
+    }
+    if (lane == 0) atomic_max_nonneg(bound, sqrtf(mx));
+  } else {
+    __shared__ float part[8][32];
+    const int col = ((int)blockIdx.x - row_blocks) * 32 + lane;
+    float ss = 0.f;
+    if (col < ncols)
+      for (int r = warp; r < hidden; r += 8) {
+        const float v = __bfloat162float(Wo[(long long)r * ncols + col]);
+        ss = fmaf(v, v, ss);
+      }
+    part[warp][lane] = ss;
+    __syncthreads();
+    if (warp == 0) {
+      float t = 0.f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) t += part[w][lane];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, off));
+      if (lane == 0) atomic_max_nonneg(bound + 1, sqrtf(t));
+    }
+  }
+}
+
+cudaError_t launch_grad_bound(const bf16* dout, long long S, int hidden, const bf16* Wo,
+                              int ncols, float* bound, cudaStream_t stream) {
+  if (S <= 0 || hidden <= 0 || ncols <= 0) return cudaSuccess;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int row_blocks = (int)std::min<long long>((S + 7) / 8, (long long)sms * 8);
+  const int col_blocks = (ncols + 31) / 32;
+  grad_bound_kernel<<<row_blocks + col_blocks, 256, 0, stream>>>(dout, S, hidden, Wo, ncols,
+                                                                 row_blocks, bound);
   return cudaGetLastError();
 }
 

@@ -23,12 +23,14 @@
 //
 // Epilogues (what the attention layer needs around the attention kernel):
 //   EPI_PROJ        Q/K/V projection of one head chunk: optional per-head
-//                   RMSNorm (Qwen3 geometry), RoPE, bf16 store to workspace;
+//                   RMSNorm (Qwen3 geometry), RoPE, fp16 store to workspace
+//                   (the attention kernels' operand type);
 //   EPI_F32         Wo-slice partial result: out (+)= O_c Wo_c^T in fp32,
 //                   staged per warp in shared memory and written by TMA store
 //                   (first chunk) or TMA reduce-add (later chunks: the
 //                   read-modify-write runs in L2, the SM never reads out);
-//   EPI_DO          dO_c = dOut Wo_c with D = rowsum(dO * O) per head;
+//   EPI_DO          dO_c = dOut Wo_c, scaled and stored in fp16, with
+//                   D = rowsum(dO * O) per head;
 //   EPI_F32_ATOMIC  split-K weight gradients, reduced with red.global.add.
 #include <algorithm>
 
@@ -102,7 +104,7 @@ __device__ __forceinline__ void rope_cs(const float2* __restrict__ hi,
 
 template <int D>
 __device__ __forceinline__ void epi_proj_row(const EpiParams& ep, const ProjSeg& sg, long long m,
-                                             int n_local, float (&v)[D]) {
+                                             int n_local, float (&v)[D], int* err) {
   constexpr int H = D / 2;
   if (sg.mode == PROJ_NORM_ROPE) {
     float ss = 0.f;
@@ -132,14 +134,25 @@ __device__ __forceinline__ void epi_proj_row(const EpiParams& ep, const ProjSeg&
       v[i + H] = b * c + a * s;
     }
   }
-  bf16* op = sg.out + m * sg.ld + sg.col0 + n_local;
+  // fp16 store: values beyond its range (|v| > 65504) would become inf; the
+  // error word reports them (UPIPE_ERR_RANGE).  The optional row norm feeds
+  // the backward's fp16 scale of dS.
+  float amax = 0.f, ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < D; ++i) {
+    amax = fmaxf(amax, fabsf(v[i]));
+    if (sg.norm_max) ss = fmaf(v[i], v[i], ss);
+  }
+  if (amax > 65504.f) atomicCAS(err, 0, kErrRange);
+  if (sg.norm_max) atomic_max_nonneg(sg.norm_max, sqrtf(ss));
+  __half* op = sg.out + m * sg.ld + sg.col0 + n_local;
 #pragma unroll
   for (int i = 0; i < D; i += 8) {
     uint4 w;
-    w.x = pack_bf16(v[i + 0], v[i + 1]);
-    w.y = pack_bf16(v[i + 2], v[i + 3]);
-    w.z = pack_bf16(v[i + 4], v[i + 5]);
-    w.w = pack_bf16(v[i + 6], v[i + 7]);
+    w.x = pack_f16(v[i + 0], v[i + 1]);
+    w.y = pack_f16(v[i + 2], v[i + 3]);
+    w.z = pack_f16(v[i + 4], v[i + 5]);
+    w.w = pack_f16(v[i + 6], v[i + 7]);
     *reinterpret_cast<uint4*>(op + i) = w;
   }
 }
@@ -361,12 +374,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < D; ++i) ss = fmaf(v[i], v[i], ss);
             sg.rstd[(long long)(n_local / D) * g.M + m] = rsqrtf(ss * (1.0f / D) + ep.eps);
           }
-          epi_proj_row<D>(ep, sg, m, n_local, v);
+          epi_proj_row<D>(ep, sg, m, n_local, v, err);
         }
       } else if constexpr (EPI == EPI_DO) {
         constexpr int D = BN;
-        float dot = 0.f;
+        float dot = 0.f, ss = 0.f;
         const int head = n0 / D;
+        const float sigma = grad_sigma(ep.bound);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
@@ -374,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait(r);
           if (live) {
             const bf16* op = ep.O + m * ep.ld_o + n0 + c * 32;
-            bf16* dp = ep.dO + m * ep.ld_do + n0 + c * 32;
+            __half* dp = ep.dO + m * ep.ld_do + n0 + c * 32;
 #pragma unroll
             for (int i = 0; i < 32; i += 8) {
               const uint4 ov = *reinterpret_cast<const uint4*>(op + i);
@@ -383,19 +397,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               uint32_t* wp = &w.x;
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
-                // D uses the bf16 dO the attention backward will read, so that
-                // sum_j dS_ij stays consistent with dP
-                wp[j] = pack_bf16(__uint_as_float(r[i + 2 * j]), __uint_as_float(r[i + 2 * j + 1]));
-                const float2 dv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wp[j]));
+                // D' and the norm use the fp16 dO' the attention backward
+                // will read, so that sum_j dS_ij stays consistent with dP
+                wp[j] = pack_f16(__uint_as_float(r[i + 2 * j]) * sigma,
+                                 __uint_as_float(r[i + 2 * j + 1]) * sigma);
+                const float2 dv = unpack_f16(wp[j]);
                 const float2 of = __bfloat1622float2(o2[j]);
                 dot = fmaf(dv.x, of.x, dot);
                 dot = fmaf(dv.y, of.y, dot);
+                ss = fmaf(dv.x, dv.x, ss);
+                ss = fmaf(dv.y, dv.y, ss);
               }
               *reinterpret_cast<uint4*>(dp + i) = w;
             }
           }
         }
-        if (live) ep.D[(long long)head * g.M + m] = dot;
+        if (live) {
+          ep.D[(long long)head * g.M + m] = dot;
+          atomic_max_nonneg(ep.do_max, sqrtf(ss));
+        }
       } else if constexpr (EPI == EPI_F32) {
         // [32 rows x 32 cols] fp32 blocks of this warp's rows, 128-byte
         // swizzled in shared memory, then one TMA store / reduce-add each

@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -32,9 +33,11 @@ using bf16 = __nv_bfloat16;
 
 // ----------------------------------------------------------- tensor maps --
 
-// Encode a 2-D bf16 tensor map over a row-major matrix [rows, cols] with
-// leading dimension ``ld`` elements, box [box_rows, box_cols] (box_cols * 2
-// must be 128: 128-byte swizzle).  Returns false when the driver refuses.
+// Encode a 2-D tensor map of 16-bit elements over a row-major matrix [rows,
+// cols] with leading dimension ``ld`` elements, box [box_rows, box_cols]
+// (box_cols * 2 must be 128: 128-byte swizzle).  The map is declared bf16; it
+// carries fp16 data as well (TMA copies the bits, and its zero fill is zero in
+// both types).  Returns false when the driver refuses.
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                     uint64_t ld, uint32_t box_rows, uint32_t box_cols);
 
@@ -42,12 +45,68 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 bool make_tmap_f32(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                    uint64_t ld, uint32_t box_rows, uint32_t box_cols);
 
+// ------------------------------------------------- backward fp16 scales --
+//
+// The attention backward runs its MMAs in fp16 (11 significant bits), whose
+// range (normal numbers 2^-14 .. 65504) is far narrower than bf16's.  Three
+// quantities pass through fp16 there, each with a power-of-two factor chosen
+// on the device from exact norms, so that nothing overflows and small values
+// stay normal; the factors are exact and are divided out of dQ, dK and dV:
+//   P''  = rho * P,       rho = 2^14  (0 <= P <= 1, so P'' <= 2^14)
+//   dO'  = sigma * dO,    sigma = 2^(13 - floor(log2(Mdout * Wcol)))
+//          with Mdout = max_i ||dout_i||_2 and Wcol = max_j ||Wo[:, j]||_2, so
+//          |dO'_ij| <= sigma * ||dout_i|| ||Wo[:, j]|| < 2^14
+//   dS'' = P'' (lambda dP' - lambda D') = lambda rho sigma dS,
+//          lambda = 2^(-1 - floor(log2(MdO' * Vmax))), MdO' = max ||dO'_i||_2
+//          over the chunk's rows and heads, Vmax = max_j ||v_j||_2 of its
+//          KV group: |dP'_ij| <= MdO' Vmax and |D'_i| <= MdO' max||o_i|| <=
+//          MdO' Vmax, so |dS''| <= rho * 2 * lambda MdO' Vmax < 2^15.
+// The scalars live in the backward workspace, zeroed at the start of a call:
+//   [0] Mdout   [1] Wcol   [2 + kv0] Vmax of the group starting at kv head kv0
+//   [2 + Hkv + c] MdO' of chunk c
+constexpr float kGradRho = 16384.0f;   // rho, and its log2 below
+constexpr float kGradRhoLog2 = 14.0f;
+
+// 2^e as a float for |e| <= 100.
+__host__ __device__ inline float pow2i(int e) {
+  e = e < -100 ? -100 : (e > 100 ? 100 : e);
+  union { unsigned int u; float f; } v;
+  v.u = (unsigned int)(e + 127) << 23;
+  return v.f;
+}
+
+// floor(log2(v)) for a finite v > 0 (subnormals count as 2^-127).
+__host__ __device__ inline int floor_log2(float v) {
+  union { float f; unsigned int u; } b;
+  b.f = v;
+  return (int)((b.u >> 23) & 255u) - 127;
+}
+
+// 2^(top - floor(log2(m))) for a finite m > 0; 1 otherwise (all-zero or
+// non-finite inputs: the factor then does not matter).
+__host__ __device__ inline float pow2_scale_for(float m, int top) {
+  if (!(m > 0.f) || !(m <= 3.0e38f)) return 1.f;
+  return pow2i(top - floor_log2(m));
+}
+
+__host__ __device__ inline float grad_sigma(const float* bound) {
+  return pow2_scale_for(bound[0] * bound[1], 13);
+}
+__host__ __device__ inline float grad_lambda(float do_max, float vmax) {
+  return pow2_scale_for(do_max * vmax, -1);
+}
+
+// max_i ||dout_i||_2 -> bound[0] and max_j ||Wo[:, j]||_2 -> bound[1]
+// (atomic maxima: bound must start at zero).
+cudaError_t launch_grad_bound(const bf16* dout, long long S, int hidden, const bf16* Wo,
+                              int ncols, float* bound, cudaStream_t stream);
+
 // ------------------------------------------------------------------ GEMM --
 
 enum EpiKind : int {
-  EPI_PROJ = 0,        // bf16 store with optional per-head RMSNorm and RoPE
+  EPI_PROJ = 0,        // fp16 store with optional per-head RMSNorm and RoPE
   EPI_F32 = 1,         // fp32 store (beta = 0) or read-modify-write add (beta = 1)
-  EPI_DO = 2,          // bf16 store of dO plus D = rowsum(dO * O) per head
+  EPI_DO = 2,          // scaled fp16 store of dO plus D = rowsum(dO * O) per head
   EPI_F32_ATOMIC = 3,  // fp32 reduction-add (split-K partial sums)
 };
 
@@ -56,12 +115,13 @@ enum ProjMode : int { PROJ_PLAIN = 0, PROJ_ROPE = 1, PROJ_NORM_ROPE = 2 };
 // One contiguous run of output columns of the fused projection GEMM.  The
 // GEMM's N range [n_begin, n_end) comes from B map ``bmap`` starting at
 // weight row ``b_row0`` and lands in ``out`` (row stride ``ld``) starting at
-// column ``col0``.
+// column ``col0``, as fp16 (the attention kernels' operand type).  A value
+// outside fp16's range sets kErrRange in the error word.
 struct ProjSeg {
   int n_begin, n_end;
   int bmap;
   int b_row0;
-  bf16* out;
+  __half* out;
   int ld;
   int col0;
   int mode;
@@ -69,6 +129,7 @@ struct ProjSeg {
   float* yhat;         // optional: normalised, pre-gain, pre-RoPE values (fp32)
   int ld_yhat;
   float* rstd;         // optional: 1/sqrt(mean(a^2)+eps) per (head, row): [heads][rows]
+  float* norm_max;     // optional: running max over rows and heads of ||row||_2
 };
 
 struct EpiParams {
@@ -84,12 +145,16 @@ struct EpiParams {
   int beta;          // EPI_F32: 0 store, 1 add (both through the C tensor map)
   // EPI_F32_ATOMIC with M segments: output base of each segment (row 0)
   float* mseg_c[6];
-  // EPI_DO
-  bf16* dO;
+  // EPI_DO: dO' = sigma * dO in fp16 with sigma = grad_sigma(bound), D' =
+  // rowsum(dO' * O) from the stored fp16 dO', and the running max of
+  // ||dO'_row||_2 over rows and heads in *do_max
+  __half* dO;
   int ld_do;
   const bf16* O;
   int ld_o;
   float* D;  // [heads][M]
+  const float* bound;   // [Mdout, Wcol] (backward fp16 scales, above)
+  float* do_max;
 };
 
 constexpr int kMaxASegs = 6;  // A tensor maps of one GEMM
@@ -130,6 +195,7 @@ cudaError_t launch_gemm(int bn, bool a_mn, bool b_mn, EpiKind epi, const CUtenso
 
 // ------------------------------------------------------------- attention --
 
+// Q, K, V: fp16 [S, heads*d] / [S, kv heads*d] through the tensor maps.
 struct AttnFwdArgs {
   int S;
   int heads;        // query heads in this launch
@@ -156,14 +222,17 @@ cudaError_t launch_attn_fwd(const CUtensorMap& qmap, const CUtensorMap& kmap,
 
 struct AttnBwdArgs {
   int S, heads, group, h0, kv0, d;
-  const bf16* Q; int ldq;       // [S, ldq]
-  const bf16* K; const bf16* V; int ldkv;
-  const bf16* dO; int ld_do;
+  const __half* Q; int ldq;     // [S, ldq] fp16
+  const __half* K; const __half* V; int ldkv;
+  const __half* dO; int ld_do;  // dO' = sigma * dO, fp16
   const float* lse; long long lse_stride;   // caller's LSE, rows of this chunk
   const float* D;               // [heads][S]
   float* dQ; int ld_dq;         // fp32 [S, ld_dq], accumulated
   float* dK; float* dV; int ld_dkv;  // fp32, accumulated across the group's chunks
   float scale;                  // 1/sqrt(d)
+  const float* bound;           // GradScales [0], [1] (sigma)
+  const float* vmax;            // Vmax of the chunk's KV group
+  const float* do_max;          // MdO' of the chunk (lambda)
 };
 
 cudaError_t launch_attn_bwd(const AttnBwdArgs& a, int* err, cudaStream_t stream);

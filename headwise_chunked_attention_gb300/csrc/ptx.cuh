@@ -7,11 +7,13 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace upipe {
 
 constexpr int kErrDeviceTimeout = 5;                         // UPIPE_ERR_DEVICE_TIMEOUT
+constexpr int kErrRange = 6;                                 // UPIPE_ERR_RANGE
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s per wait
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -258,6 +260,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// The same with fp16 A and B (format code 0): the attention kernels' operands.
+// fp16 keeps 11 significant bits against bf16's 8 at the same tensor-core
+// rate; both operands of one MMA always share the type.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4)                                 // D format: f32; A, B: f16
+         | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand.
 //  K-major:  rows of 128 B (64 bf16 along K), 8-row atoms of 1024 B;
 //            sbo = byte distance between 8-row groups, lbo unused.
@@ -355,6 +366,23 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two floats to a packed fp16 pair (round to nearest even; |v| > 65504 -> inf).
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float2 unpack_f16(uint32_t v) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&v));
+}
+
+// Maximum of non-negative floats by their bit patterns, which order like
+// unsigned integers (a NaN pattern is larger than every finite value and
+// stays, so a NaN input is not hidden).
+__device__ __forceinline__ void atomic_max_nonneg(float* p, float v) {
+  atomicMax(reinterpret_cast<unsigned int*>(p), __float_as_uint(v));
 }
 
 // Three-input maximum (one instruction on sm_100 and later).

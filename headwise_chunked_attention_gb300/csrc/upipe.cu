@@ -194,7 +194,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct Layout {
   size_t rope_hi, rope_lo, rope_lo_t, q, k, v, o, flush;     // forward
   size_t o2;                                               // forward, mode 2
-  size_t dO, D, dq, dk, dv, dklo, dvlo, yq, rq, yk, rk;  // backward
+  size_t dO, D, dq, dk, dv, dklo, dvlo, yq, rq, yk, rk, sc;  // backward
   size_t total;
 };
 
@@ -232,6 +232,9 @@ Layout plan(const Geo& g, int mode) {
       L.yk = take(S * kvc * d * 4);
       L.rk = take(kvc * S * 4);
     }
+    // the fp16 gradient scales' norm maxima: [Mdout, Wcol, Vmax per KV head
+    // that starts a group, MdO' per chunk] (internal.h)
+    L.sc = take((size_t)(2 + g.Hkv + g.nchunks) * sizeof(float));
   }
   L.total = off;
   return L;
@@ -322,11 +325,13 @@ inline int side_sms(int num_sms) { return std::max(8, num_sms / 5); }
 // Fused projection of one chunk: Q heads [h0, h0+ch) and, when the chunk
 // starts a new KV group, K and V heads [kv0, kv0+kvc).  Each 128-row x d
 // output tile is one head, so a head's values never depend on chunk_heads.
+// Q, K, V are written in fp16 (the attention kernels' operand type).  vmax:
+// nullptr, or where the running max of the V rows' norms goes (backward).
 int project_chunk(const Geo& g, const DeviceState* ds, cudaStream_t st, const CUtensorMap& xmap,
                   const bf16* Wq, const bf16* Wk, const bf16* Wv, const float* qgw,
-                  const float* kgw, float eps, int h0, int kv0, bool new_group, bf16* Q, bf16* K,
-                  bf16* V, const float2* rhi, const float2* rlo_t, float* yq, float* rq, float* yk,
-                  float* rk) {
+                  const float* kgw, float eps, int h0, int kv0, bool new_group, __half* Q,
+                  __half* K, __half* V, const float2* rhi, const float2* rlo_t, float* yq,
+                  float* rq, float* yk, float* rk, float* vmax = nullptr) {
   const int d = g.d;
   CUtensorMap bm[3];
   EpiParams ep{};
@@ -336,16 +341,17 @@ int project_chunk(const Geo& g, const DeviceState* ds, cudaStream_t st, const CU
   const int qk_mode = g.norm ? PROJ_NORM_ROPE : PROJ_ROPE;
   int n = 0, ns = 0;
   UPIPE_MAP(&bm[0], Wq, (uint64_t)g.Hq * d, g.hidden, g.hidden, d, 64);
-  ep.seg[ns++] = ProjSeg{n, n + g.ch * d, 0, h0 * d, Q, g.ch * d, 0, qk_mode, qgw, yq, g.ch * d, rq};
+  ep.seg[ns++] =
+      ProjSeg{n, n + g.ch * d, 0, h0 * d, Q, g.ch * d, 0, qk_mode, qgw, yq, g.ch * d, rq, nullptr};
   n += g.ch * d;
   if (new_group) {
     UPIPE_MAP(&bm[1], Wk, (uint64_t)g.Hkv * d, g.hidden, g.hidden, d, 64);
     UPIPE_MAP(&bm[2], Wv, (uint64_t)g.Hkv * d, g.hidden, g.hidden, d, 64);
     ep.seg[ns++] = ProjSeg{n, n + g.kvc * d, 1, kv0 * d, K, g.kvc * d, 0, qk_mode, kgw, yk,
-                           g.kvc * d, rk};
+                           g.kvc * d, rk, nullptr};
     n += g.kvc * d;
     ep.seg[ns++] = ProjSeg{n, n + g.kvc * d, 2, kv0 * d, V, g.kvc * d, 0, PROJ_PLAIN, nullptr,
-                           nullptr, 0, nullptr};
+                           nullptr, 0, nullptr, vmax};
     n += g.kvc * d;
   }
   ep.nseg = ns;
@@ -355,8 +361,8 @@ int project_chunk(const Geo& g, const DeviceState* ds, cudaStream_t st, const CU
   return UPIPE_OK;
 }
 
-int attention_chunk(const Geo& g, const DeviceState* ds, cudaStream_t st, const bf16* Q,
-                    const bf16* K, const bf16* V, int h0, int kv0, bf16* O, int ldo,
+int attention_chunk(const Geo& g, const DeviceState* ds, cudaStream_t st, const __half* Q,
+                    const __half* K, const __half* V, int h0, int kv0, bf16* O, int ldo,
                     float* lse, float* flush) {
   const int d = g.d;
   CUtensorMap qm, km, vm;
@@ -428,8 +434,8 @@ static int attn_fwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
   float2* rlo = at<float2>(workspace, L.rope_lo);
   float2* rlo_t = at<float2>(workspace, L.rope_lo_t);
   bf16* Q = at<bf16>(workspace, L.q);
-  bf16* K = at<bf16>(workspace, L.k);
-  bf16* V = at<bf16>(workspace, L.v);
+  __half* K = at<__half>(workspace, L.k);
+  __half* V = at<__half>(workspace, L.v);
   bf16* Ows = at<bf16>(workspace, L.o);
   float* flush = L.flush == (size_t)-1 ? nullptr : at<float>(workspace, L.flush);
   UPIPE_CUDA(launch_rope_table(rhi, rlo, rlo_t, g.S, g.d, shape->rope_theta, st));
@@ -439,9 +445,9 @@ static int attn_fwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
   if (!make_tmap_f32(&outmap, out, g.S, g.hidden, g.hidden, 32, 32)) return UPIPE_ERR_CUDA;
   const int out_bn = (g.hidden % 256 == 0) ? 256 : 128;
 
-  // Chunk c projects Q into buffer c % 2 and the attention writes O over it in
-  // place (each Q tile is read only by the CTA that writes the same O rows, and
-  // before it writes them).  With more than one chunk, the Wo-slice accumulate
+  // Chunk c projects Q (fp16) into buffer c % 2 and the attention writes O
+  // (bf16) over it in place (each Q tile is read only by the CTA that writes
+  // the same O rows, and before it writes them).  With more than one chunk, the Wo-slice accumulate
   // of chunk c - 1 runs on the side stream with a few SMs, after the projection
   // of chunk c and beside its attention; the projection of chunk c + 1 waits
   // for it, since it overwrites that buffer.  The last accumulate runs on the
@@ -528,8 +534,9 @@ static int attn_fwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
     } else if (overlap && c >= 2) {
       UPIPE_CUDA(cudaStreamWaitEvent(st, ev.out[c & 1], 0));
     }
+    __half* Qh = reinterpret_cast<__half*>(Qc);
     UPIPE_TRY(project_chunk(g, ds, st, xmap, Wq, Wk, Wv, q_norm_w, k_norm_w, shape->norm_eps, h0,
-                            kv0, new_group, Qc, K, V, rhi, rlo_t, nullptr, nullptr, nullptr,
+                            kv0, new_group, Qh, K, V, rhi, rlo_t, nullptr, nullptr, nullptr,
                             nullptr));
     if (pair && c >= 2 && c % 2 == 0) {
       UPIPE_CUDA(cudaEventRecord(ev.proj, st));
@@ -544,7 +551,7 @@ static int attn_fwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
     }
     bf16* O = o_all ? o_all + (size_t)h0 * g.d : Qc;
     const int ldo = o_all ? g.Hq * g.d : g.ch * g.d;
-    UPIPE_TRY(attention_chunk(g, ds, st, Qc, K, V, h0, kv0, O, ldo, lse + (size_t)h0 * g.S,
+    UPIPE_TRY(attention_chunk(g, ds, st, Qh, K, V, h0, kv0, O, ldo, lse + (size_t)h0 * g.S,
                               flush));
     if (!overlap && c + 1 < g.nchunks) UPIPE_TRY(out_gemm(c, st, ds->num_sms, true));
   }
@@ -627,12 +634,18 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
   float2* rhi = at<float2>(workspace, L.rope_hi);
   float2* rlo = at<float2>(workspace, L.rope_lo);
   float2* rlo_t = at<float2>(workspace, L.rope_lo_t);
-  bf16* Q = at<bf16>(workspace, L.q);
-  bf16* K = at<bf16>(workspace, L.k);
-  bf16* V = at<bf16>(workspace, L.v);
+  // Q, K, V and dO' hold fp16 operands of the attention kernels; once those
+  // are done, their buffers take the bf16 hi parts of the gradients
+  __half* Q = at<__half>(workspace, L.q);
+  __half* K = at<__half>(workspace, L.k);
+  __half* V = at<__half>(workspace, L.v);
   bf16* Ows = at<bf16>(workspace, L.o);
   float* flush = L.flush == (size_t)-1 ? nullptr : at<float>(workspace, L.flush);
-  bf16* dO = at<bf16>(workspace, L.dO);
+  __half* dO = at<__half>(workspace, L.dO);
+  bf16* dO_hi = reinterpret_cast<bf16*>(dO);
+  bf16* K_hi = reinterpret_cast<bf16*>(K);
+  bf16* V_hi = reinterpret_cast<bf16*>(V);
+  float* sc = at<float>(workspace, L.sc);
   float* Dv = at<float>(workspace, L.D);
   float* dQ = at<float>(workspace, L.dq);
   float* dK = at<float>(workspace, L.dk);
@@ -645,6 +658,10 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
   float* rk = g.norm ? at<float>(workspace, L.rk) : nullptr;
 
   UPIPE_CUDA(launch_rope_table(rhi, rlo, rlo_t, g.S, d, shape->rope_theta, st));
+  // the fp16 gradient scales: norm maxima start at zero; the dO scale's
+  // bound (max ||dout_i||, max ||Wo[:, j]||) is taken once per call
+  UPIPE_CUDA(cudaMemsetAsync(sc, 0, sizeof(float) * (size_t)(2 + g.Hkv + g.nchunks), st));
+  UPIPE_CUDA(launch_grad_bound(dout, g.S, g.hidden, Wo, g.Hq * d, sc, st));
   // split-K weight gradients accumulate with reductions: start from zero
   UPIPE_CUDA(cudaMemsetAsync(dWq, 0, sizeof(float) * (size_t)g.Hq * d * g.hidden, st));
   UPIPE_CUDA(cudaMemsetAsync(dWk, 0, sizeof(float) * (size_t)g.Hkv * d * g.hidden, st));
@@ -745,8 +762,10 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
     const bool new_group = (g.ch >= g.g) || (h0 % g.g == 0);
     const bool last_of_group = (g.ch >= g.g) || ((h0 + g.ch) % g.g == 0);
     // 1. recompute Q (and K, V) and the attention output of the chunk
+    float* vmax = sc + 2 + kv0;     // the norm maximum of this group's V rows
+    float* do_max = sc + 2 + g.Hkv + c;
     UPIPE_TRY(project_chunk(g, ds, st, xmap, Wq, Wk, Wv, q_norm_w, k_norm_w, shape->norm_eps, h0,
-                            kv0, new_group, Q, K, V, rhi, rlo_t, yq, rq, yk, rk));
+                            kv0, new_group, Q, K, V, rhi, rlo_t, yq, rq, yk, rk, vmax));
     if (new_group) {
       UPIPE_CUDA(cudaMemsetAsync(dK, 0, sizeof(float) * S * g.kvc * d, st));
       UPIPE_CUDA(cudaMemsetAsync(dV, 0, sizeof(float) * S * g.kvc * d, st));
@@ -768,6 +787,8 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
       ep.O = Oc;
       ep.ld_o = ldo;
       ep.D = Dv;
+      ep.bound = sc;
+      ep.do_max = do_max;
       GemmArgs ga{(int)g.S, g.ch * d, g.hidden, 1, d};
       UPIPE_CUDA(launch_gemm(d, false, true, EPI_DO, &dout_k, 1, &wom, 1, ga, ep, ds->err,
                              ds->num_sms, st));
@@ -808,6 +829,9 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
       a.dV = dV;
       a.ld_dkv = g.kvc * d;
       a.scale = (float)(1.0 / std::sqrt((double)d));
+      a.bound = sc;
+      a.vmax = vmax;
+      a.do_max = do_max;
       prof_begin(1, st);
       const cudaError_t e = launch_attn_bwd(a, ds->err, st);
       prof_end(1, st);
@@ -824,7 +848,7 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
       q.d = d;
       q.g = dQ;
       q.ld_g = g.ch * d;
-      q.out = dO;
+      q.out = dO_hi;
       q.out_lo = Ows;
       q.ld_out = g.ch * d;
       q.mode = g.norm ? PROJ_NORM_ROPE : PROJ_ROPE;
@@ -840,9 +864,9 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
       prof_end(3, st);
     }
     const bf16* Wq_c = Wq + (size_t)h0 * d * g.hidden;
-    DxSeg dxs[kMaxASegs] = {{dO, g.ch * d, Wq_c}, {Ows, g.ch * d, Wq_c}};
+    DxSeg dxs[kMaxASegs] = {{dO_hi, g.ch * d, Wq_c}, {Ows, g.ch * d, Wq_c}};
     float* dWq_c = dWq + (size_t)h0 * d * g.hidden;
-    DwSeg dws[kMaxASegs] = {{dO, g.ch * d, dWq_c}, {Ows, g.ch * d, dWq_c}};
+    DwSeg dws[kMaxASegs] = {{dO_hi, g.ch * d, dWq_c}, {Ows, g.ch * d, dWq_c}};
     int ndx = 2;
     // 5. at the group's last chunk: dK -> dA_k (hi over K, lo beside it),
     //    dV -> hi over V and lo beside it
@@ -853,7 +877,7 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
       q.d = d;
       q.g = dK;
       q.ld_g = g.kvc * d;
-      q.out = K;
+      q.out = K_hi;
       q.out_lo = dKlo;
       q.ld_out = g.kvc * d;
       q.mode = g.norm ? PROJ_NORM_ROPE : PROJ_ROPE;
@@ -868,15 +892,15 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
       UPIPE_CUDA(launch_qk_bwd(q, st));
       prof_end(3, st);
       prof_begin(4, st);
-      UPIPE_CUDA(launch_f32_to_bf16x2(dV, g.kvc * d, V, dVlo, g.kvc * d, g.S, g.kvc * d, st));
+      UPIPE_CUDA(launch_f32_to_bf16x2(dV, g.kvc * d, V_hi, dVlo, g.kvc * d, g.S, g.kvc * d, st));
       prof_end(4, st);
       const bf16* Wk_g = Wk + (size_t)kv0 * d * g.hidden;
       const bf16* Wv_g = Wv + (size_t)kv0 * d * g.hidden;
       float* dWk_g = dWk + (size_t)kv0 * d * g.hidden;
       float* dWv_g = dWv + (size_t)kv0 * d * g.hidden;
       for (int part = 0; part < 2; ++part) {
-        const bf16* gk = part ? dKlo : K;
-        const bf16* gv = part ? dVlo : V;
+        const bf16* gk = part ? dKlo : K_hi;
+        const bf16* gv = part ? dVlo : V_hi;
         dws[ndx] = {gk, g.kvc * d, dWk_g};
         dxs[ndx++] = {gk, g.kvc * d, Wk_g};
         dws[ndx] = {gv, g.kvc * d, dWv_g};
@@ -952,6 +976,7 @@ extern "C" const char* upipe_strerror(int code) {
     case UPIPE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case UPIPE_ERR_CUDA: return "CUDA error";
     case UPIPE_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case UPIPE_ERR_RANGE: return "projected value outside the fp16 range";
     default: return "unknown error";
   }
 }

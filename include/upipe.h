@@ -37,7 +37,18 @@
  *    ``workspace``.
  *  - Errors: every argument is validated on the host before the first launch;
  *    a failed check returns a code and launches nothing.  A device-side wait
- *    that exceeds its time limit is reported by upipe_last_error().
+ *    that exceeds its time limit, or a projected value outside the fp16 range,
+ *    is reported by upipe_last_error().
+ *  - Precision: inputs are bf16 and every contraction accumulates in fp32.
+ *    The per-chunk q, k, v (after norm and RoPE) and the attention kernels'
+ *    probabilities and gradients are held in fp16, whose 11 significant bits
+ *    (bf16: 8) keep the layer within max 2e-2 / mean 2e-3 (relative to unit
+ *    scale) and |lse| 1e-3 of the float64 definition; q, k and v must
+ *    therefore lie within fp16's range (|v| <= 65504, else UPIPE_ERR_RANGE).
+ *    The backward scales dO and dS by exact powers of two derived on the
+ *    device from norms of dout, Wo, v and dO, so gradients of any magnitude
+ *    keep their precision.  The attention output o (attn_o) is bf16 and out,
+ *    lse and all gradients are fp32.
  */
 #ifndef UPIPE_H_
 #define UPIPE_H_
@@ -76,7 +87,9 @@ enum {
   UPIPE_ERR_UNSUPPORTED = 2,          /* a shape this build does not handle  */
   UPIPE_ERR_WORKSPACE_TOO_SMALL = 3,  /* ws_bytes < upipe_workspace_bytes()  */
   UPIPE_ERR_CUDA = 4,                 /* a CUDA runtime/driver call failed    */
-  UPIPE_ERR_DEVICE_TIMEOUT = 5        /* a kernel's bounded wait expired      */
+  UPIPE_ERR_DEVICE_TIMEOUT = 5,       /* a kernel's bounded wait expired      */
+  UPIPE_ERR_RANGE = 6                 /* a projected q, k or v value exceeds
+                                         the fp16 range (|v| > 65504)        */
 };
 
 /* Workspace bytes needed by upipe_attn_fwd (mode 0) or upipe_attn_bwd
@@ -209,8 +222,9 @@ int upipe_profile_count(void);
 int upipe_selftest_wait_timeout(int limit_us, void* stream);
 
 /* Synchronises the current device, then returns and clears the device error
- * word (UPIPE_OK or UPIPE_ERR_DEVICE_TIMEOUT), or UPIPE_ERR_CUDA if the
- * device reports a CUDA error. */
+ * word (UPIPE_OK, UPIPE_ERR_DEVICE_TIMEOUT or UPIPE_ERR_RANGE: the first error
+ * a kernel recorded since the last call), or UPIPE_ERR_CUDA if the device
+ * reports a CUDA error. */
 int upipe_last_error(void);
 
 /* Static description of an error code. */

@@ -53,7 +53,15 @@ def test_workspace_closed_form(u):
             if S > 512 * 128:   # per-SM fp32 rows for folding long attention rows
                 expect += 256 * 256 * d * 4
             assert ws(u, w, ch) == expect, (w.name, ch)
-            assert ws(u, w, ch, 1) > ws(u, w, ch)
+            # backward: dO (fp16), D, dQ (fp32), dK, dV (fp32) and their bf16
+            # low halves, the saved RMSNorm values (qk-norm), and the fp16
+            # gradient scales' norm maxima (2 + Hkv + chunks floats)
+            bwd = (al(S * ch * d * 2) + al(ch * S * 4) + al(S * ch * d * 4)
+                   + 2 * al(S * kvc * d * 4) + 2 * al(S * kvc * d * 2))
+            if w.qk_norm:
+                bwd += al(S * ch * d * 4) + al(ch * S * 4) + al(S * kvc * d * 4) + al(kvc * S * 4)
+            bwd += al((2 + w.Hkv + w.Hq // ch) * 4)
+            assert ws(u, w, ch, 1) == expect + bwd, (w.name, ch)
             # mode 2: the forward's third chunk buffer for paired accumulates
             assert ws(u, w, ch, 2) == expect + al(S * ch * d * 2), (w.name, ch)
 

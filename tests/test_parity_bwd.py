@@ -13,7 +13,7 @@ from tests._util import f64, assert_close, GAIN_MAX_REL, GAIN_MEAN_REL
 pytestmark = pytest.mark.gpu
 
 
-def run_fwd_bwd(w, ch, inp, saved_o=False):
+def run_fwd_bwd(w, ch, inp, saved_o=False, dout_scale=None):
     import headwise_chunked_attention_gb300 as u
     dev = "cuda"
     t = {k: v.to(dev) for k, v in inp.items()}
@@ -26,12 +26,13 @@ def run_fwd_bwd(w, ch, inp, saved_o=False):
                t.get("q_gamma"), t.get("k_gamma"), o)
     if saved_o:   # the backward must not depend on what the forward left in ws
         ws.fill_(0xFF)
+    dout = t["dout"] if dout_scale is None else (t["dout"].float() * dout_scale).to(torch.bfloat16)
     g = {n: torch.full(t[src].shape, float("nan"), device=dev)
          for n, src in [("dx", "x"), ("dWq", "Wq"), ("dWk", "Wk"), ("dWv", "Wv"),
                         ("dWo", "Wo")]}
     dqg = torch.full((w.d,), float("nan"), device=dev) if w.qk_norm else None
     dkg = torch.full((w.d,), float("nan"), device=dev) if w.qk_norm else None
-    u.attn_bwd(sh, t["x"], t["Wq"], t["Wk"], t["Wv"], t["Wo"], t["dout"], lse,
+    u.attn_bwd(sh, t["x"], t["Wq"], t["Wk"], t["Wv"], t["Wo"], dout, lse,
                g["dx"], g["dWq"], g["dWk"], g["dWv"], g["dWo"], ws,
                t.get("q_gamma"), t.get("k_gamma"), dqg, dkg, attn_o=o)
     torch.cuda.synchronize()
@@ -40,12 +41,11 @@ def run_fwd_bwd(w, ch, inp, saved_o=False):
     return g
 
 
-def oracle_bwd(w, inp, store="bf16"):
-    # q, k, v are bf16 in the workspace by design: the tolerance applies
-    # against the oracle that attends over bf16-rounded q, k, v (as forward)
+def oracle_bwd(w, inp):
+    # the plain float64 chain rule: no rounding of any intermediate
     a = {k: f64(v) for k, v in inp.items()}
     return O.layer_backward(w, a["x"], a["Wq"], a["Wk"], a["Wv"], a["Wo"], a["dout"],
-                            a.get("q_gamma"), a.get("k_gamma"), store_dtype=store)
+                            a.get("q_gamma"), a.get("k_gamma"))
 
 
 CASES = [
@@ -96,3 +96,28 @@ def test_backward_with_saved_attention_output(w, chs):
             a, b = f64(g[name]), f64(r[name])
             scale = np.sqrt(np.mean(b ** 2)) + 1e-30
             assert np.max(np.abs(a - b)) / scale < 1e-4, f"saved-O vs recompute {name} ch={ch}"
+
+
+@pytest.mark.parametrize("w,chs", [CASES[1], CASES[4]],
+                         ids=lambda c: getattr(c, "name", str(c)))
+def test_backward_gradient_magnitude_invariance(w, chs):
+    # The backward keeps dO and dS in fp16 with power-of-two factors derived
+    # on the device from the norms of dout, Wo, v and dO.  Multiplying dout by
+    # a power of two multiplies those factors' inputs by it, so the fp16
+    # operands are the same bits and every gradient (the gains' included)
+    # scales exactly: tiny (2^-40) and large (2^20) upstream gradients lose no
+    # precision.  The fp32 reductions across CTAs (dQ, dK, dV, split-K weight
+    # gradients) run in no fixed order, and a one-ulp change of an fp32
+    # gradient moves the bf16 low half of its hi/lo split by up to ~2^-18 of
+    # the value, so the comparison allows 1e-4 of the tensor's RMS; a lost
+    # factor or an fp16 underflow would be off by orders of magnitude more.
+    inp = make_inputs(w, seed=0, with_grad=True, norm_gains="random")
+    for ch in chs:
+        base = {k: f64(v) for k, v in run_fwd_bwd(w, ch, inp).items() if v is not None}
+        for e in (-40, 20):
+            g = run_fwd_bwd(w, ch, inp, dout_scale=2.0 ** e)
+            for name, v in base.items():
+                got = f64(g[name]) * 2.0 ** -e
+                rms = np.sqrt(np.mean(v * v))
+                err = np.max(np.abs(got - v)) / rms
+                assert err < 1e-4, f"{name} ch={ch} scale 2^{e}: {err:.2e}"

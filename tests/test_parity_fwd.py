@@ -17,7 +17,7 @@ def U():
     return mod
 
 
-def run_fwd(w, ch, inp, debug=True):
+def run_fwd(w, ch, inp, debug=True, expect_error=0):
     u = U()
     dev = "cuda"
     t = {k: v.to(dev) for k, v in inp.items()}
@@ -29,26 +29,24 @@ def run_fwd(w, ch, inp, debug=True):
     u.attn_fwd(shape, t["x"], t["Wq"], t["Wk"], t["Wv"], t["Wo"], out, lse, ws,
                t.get("q_gamma"), t.get("k_gamma"), o)
     torch.cuda.synchronize()
-    assert u.last_error() == 0
+    assert u.last_error() == expect_error
     return out, lse, o
 
 
-def oracle_fwd(w, inp, rows=None, store=None):
+def oracle_fwd(w, inp, rows=None):
     a = {k: f64(v) for k, v in inp.items()}
     return O.layer_forward(w, a["x"], a["Wq"], a["Wk"], a["Wv"], a["Wo"],
-                           a.get("q_gamma"), a.get("k_gamma"), rows=rows,
-                           store_dtype=store)
+                           a.get("q_gamma"), a.get("k_gamma"), rows=rows)
 
 
 def check_full(w, ch, inp):
+    # against the plain float64 definition: no rounding of any intermediate
     out, lse, o = run_fwd(w, ch, inp)
-    refb = oracle_fwd(w, inp, store="bf16")
-    # q, k, v, P and O are bf16 by design (the workspace precision): the
-    # tolerance applies against the oracle that stores q, k, v in bf16
-    assert_close(f64(out), refb["out"], "out")
+    ref = oracle_fwd(w, inp)
+    assert_close(f64(out), ref["out"], "out")
     o_g = f64(o).reshape(w.S, w.Hq, w.d).transpose(1, 0, 2)
-    assert_close(o_g, refb["o"], "attention output")
-    dl = np.abs(f64(lse) - refb["lse"]).max()
+    assert_close(o_g, ref["o"], "attention output")
+    dl = np.abs(f64(lse) - ref["lse"]).max()
     assert dl <= LSE_ABS, f"lse max abs err {dl:.3e}"
     return out, lse, o
 
@@ -100,35 +98,82 @@ def test_chunked_out_close_to_unchunked():
         assert_close(f64(out), f64(ref), f"out ch={ch} vs ch=24", 1e-3, 1e-4)
 
 
-def test_forward_row_max_growing_late_in_rows():
-    # The hidden rows of keys 900..1019 are scaled by 6, so their scores
-    # against every later query are 6 times larger: the row max of each of
-    # those queries jumps by 10 to 34 powers of two in the eighth KV tile, and
-    # the kernel must take that tile's max and rescale O and l mid-row.
-    # The block's own rows are left out of the comparison: their queries are
-    # scaled too, so their scores among themselves are 36 times larger, and a
-    # one-ulp difference in the bf16 rounding of a projected q or k (float64
-    # oracle against the fp32 tensor-core sum) moves such a score by ~1%.
-    # Every other row is compared in full, out and O with the layer's bounds.
-    # Their scores against the scaled keys are 6 times larger too, and the
-    # LSE error (absolute, in the scores' units) grows with them: one ulp of
-    # a k element moves such a score 6 times as far, so the LSE bound here is
-    # 6 x 1e-3.  A fault in the rescale would be off by whole powers of two.
-    w = Workload("late-max", S=1500, hidden=256, Hq=2, Hkv=1, d=128, chunk_heads=(1, 2),
-                 rope_theta=1e4)
+def _late_max_inputs(w, scale):
     inp = make_inputs(w, seed=11)
     x = inp["x"].float()
-    x[900:1020] *= 6.0
+    x[900:1020] *= scale
     inp["x"] = x.to(torch.bfloat16)
-    keep = np.r_[0:900, 1020:w.S]
-    ref = oracle_fwd(w, inp, store="bf16")
+    return inp
+
+
+LATE = Workload("late-max", S=1500, hidden=256, Hq=2, Hkv=1, d=128, chunk_heads=(1, 2),
+                rope_theta=1e4)
+
+
+def test_forward_row_max_growing_late_in_rows():
+    # The hidden rows of keys 900..1019 are scaled by 2, so their scores
+    # against every later query are about twice as large: the row max of
+    # those queries grows by up to ~8 powers of two inside the eighth KV tile,
+    # and the kernel either keeps its running max (growth within the p <= 128
+    # allowance) or takes the tile's max and rescales O and l mid-row.  Every
+    # row is compared with the plain float64 layer: out and O at the layer's
+    # bounds, lse within 1e-3 outside the scaled block.  Inside the block q and
+    # k are both doubled, so its scores are 4 times the unit-scale ones and
+    # the fp16 rounding of q and k moves them 4 times as far: there the lse
+    # bound is 4 x 1e-3 (a fault in the rescale would be off by whole powers
+    # of two).
+    w = LATE
+    inp = _late_max_inputs(w, 2.0)
+    out_rows = np.r_[0:900, 1020:w.S]
+    blk = np.r_[900:1020]
+    ref = oracle_fwd(w, inp)
     for ch in w.chunk_heads:
         out, lse, o = run_fwd(w, ch, inp)
-        assert_close(f64(out)[keep], ref["out"][keep], f"out ch={ch}")
+        assert_close(f64(out), ref["out"], f"out ch={ch}")
         o_g = f64(o).reshape(w.S, w.Hq, w.d).transpose(1, 0, 2)
-        assert_close(o_g[:, keep], ref["o"][:, keep], f"attention output ch={ch}")
-        dl = np.abs(f64(lse)[:, keep] - ref["lse"][:, keep]).max()
-        assert dl <= 6 * LSE_ABS, f"lse max abs err {dl:.3e} ch={ch}"
+        assert_close(o_g, ref["o"], f"attention output ch={ch}")
+        dl = np.abs(f64(lse) - ref["lse"])
+        assert dl[:, out_rows].max() <= LSE_ABS, f"lse {dl[:, out_rows].max():.3e} ch={ch}"
+        assert dl[:, blk].max() <= 4 * LSE_ABS, f"block lse {dl[:, blk].max():.3e} ch={ch}"
+
+
+def test_forward_row_max_jump_forces_rescale():
+    # Scaled by 6, the block's keys raise every later row's max by 10 to 34
+    # powers of two in one tile: each such row must take the new max and
+    # rescale mid-row.  The rows after the block are compared with the layer's
+    # bounds (their scores against the block are 6 times the unit-scale ones,
+    # so lse gets 6 x 1e-3).  The block's own rows (scores 36 times the unit
+    # scale, far outside what the unit-scale bounds describe) are checked for
+    # the rescale only: finite, and lse within 36 x 1e-3.
+    w = LATE
+    inp = _late_max_inputs(w, 6.0)
+    after = np.r_[1020:w.S]
+    blk = np.r_[900:1020]
+    ref = oracle_fwd(w, inp)
+    for ch in w.chunk_heads:
+        out, lse, o = run_fwd(w, ch, inp)
+        assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+        assert_close(f64(out)[after], ref["out"][after], f"out ch={ch}")
+        o_g = f64(o).reshape(w.S, w.Hq, w.d).transpose(1, 0, 2)
+        assert_close(o_g[:, after], ref["o"][:, after], f"attention output ch={ch}")
+        assert_close(f64(out)[:900], ref["out"][:900], f"out before the block ch={ch}")
+        dl = np.abs(f64(lse) - ref["lse"])
+        assert dl[:, :900].max() <= LSE_ABS
+        assert dl[:, after].max() <= 6 * LSE_ABS, f"lse {dl[:, after].max():.3e} ch={ch}"
+        assert dl[:, blk].max() <= 36 * LSE_ABS, f"block lse {dl[:, blk].max():.3e} ch={ch}"
+
+
+def test_forward_reports_values_beyond_fp16_range():
+    # q, k, v are kept in fp16: a projection beyond +-65504 does not fit,
+    # and the call must report it (UPIPE_ERR_RANGE) instead of returning
+    # silently; the next call starts with a clear error word.
+    import headwise_chunked_attention_gb300 as u
+    w = Workload("range", S=300, hidden=256, Hq=2, Hkv=1, d=128, chunk_heads=(1,),
+                 rope_theta=1e4)
+    inp = make_inputs(w, seed=5)
+    inp["x"] = (inp["x"].float() * 2.0 ** 17).to(torch.bfloat16)
+    run_fwd(w, 1, inp, expect_error=u.ERR_RANGE)
+    run_fwd(w, 1, make_inputs(w, seed=5))
 
 
 @pytest.mark.parametrize("w", [
@@ -163,5 +208,5 @@ def test_paired_accumulates(w):
     assert torch.equal(res[0][1], res[2][1])
     scale = np.abs(res[0][0]).max()
     assert np.abs(res[2][0] - res[0][0]).max() / scale < 1e-5
-    ref = oracle_fwd(w, inp, store="bf16")
+    ref = oracle_fwd(w, inp)
     assert_close(res[2][0], ref["out"], "paired out")
