@@ -50,6 +50,16 @@
 // dS^T_u is also written to shared memory (one 128-byte swizzled row per key)
 // where it is the MN-major B operand of dQ^T = K^T dS^T.  MMAs issued by one
 // thread complete in order, which makes the reuse of the TMEM slots safe.
+// Long walks: dK and dV accumulate in TMEM over every query sub-tile of a
+// CTA's walk, and the tensor core's fp32 accumulation drifts over hundreds of
+// thousands of steps (the forward's O drifted out of bounds past ~1M keys,
+// 65536 accumulation steps).  A CTA therefore walks at most a.walk sub-tiles:
+// a longer walk is cut into segments that separate CTAs run, each adding its
+// dK / dV partial into the fp32 global accumulators (which every CTA does
+// anyway).  Up to 1M tokens (16384 sub-tiles) the host passes the whole walk,
+// so every key tile is one CTA; beyond, segments of 8192 sub-tiles.  Grid
+// order: segment 0 of every key tile (ascending, heaviest first), then
+// segment 1 of the key tiles that have one, and so on.
 // For d = 64 the dQ^T MMA still runs with M = 128: its A operand reads past
 // the 64-wide K tile into the V tile (inside this CTA's shared memory) and
 // the extra 64 output rows are never stored.
@@ -123,11 +133,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int S = a.S;
-  const int jt = blockIdx.x;
   const int head = blockIdx.y;
   const int kvh = (a.h0 + head) / a.group - a.kv0;
+  // (key tile, segment) of this CTA: key tile jt walks n_u(jt) = NU0 - 2 jt
+  // sub-tiles from its diagonal; segment kseg of it exists while
+  // n_u(jt) > kseg * walk, i.e. for the first ceil((NU0 - kseg walk) / 2)
+  // key tiles
+  const int NU0 = (S + BQ - 1) / BQ;
+  const int NT = (S + BK - 1) / BK;
+  int jt = (int)blockIdx.x, kseg = 0;
+  for (;;) {
+    const int over = NU0 - kseg * a.walk;
+    const int J = over > 0 ? min(NT, (over + 1) / 2) : 0;
+    if (J == 0) { jt = -1; break; }   // past the grid the host computed: no work
+    if (jt < J) break;
+    jt -= J;
+    ++kseg;
+  }
+  if (jt < 0) return;
   const int k0 = jt * BK;
-  const int n_u = (S - k0 + BQ - 1) / BQ;  // query sub-tiles from the diagonal on
+  const int u0 = kseg * a.walk;                        // first sub-tile of the segment
+  const int n_u = min(a.walk, NU0 - 2 * jt - u0);      // query sub-tiles of this CTA
+  const int qs0 = k0 + u0 * BQ;                        // its first query
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -178,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
         const uint32_t ph = (u / NST) & 1;
         if (!mbar_wait(&q_empty[st], ph ^ 1, err, abort_flag)) break;
         mbar_expect_tx(&q_full[st], Cfg::ST_BYTES);
-        const int q0 = k0 + u * BQ;
+        const int q0 = qs0 + u * BQ;
         uint8_t* base = smem + Cfg::ST_OFF + st * Cfg::ST_BYTES;
         for (int b = 0; b < D / 64; ++b) {
           tma_load_2d(base + b * Cfg::Q_BLOCK, &qmap, &q_full[st], head * D + 64 * b, q0);
@@ -287,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
     auto fetch = [&](int u) {
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
-        const int q = min(k0 + u * BQ + 32 * m + lane, S - 1);  // clamp: masked below
+        const int q = min(qs0 + u * BQ + 32 * m + lane, S - 1);  // clamp: masked below
         nl[m] = ld_nc_f32(lse_g + q);
         nd[m] = ld_nc_f32(D_g + q);
       }
@@ -299,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
       float* ld_w = ld_wg + ph * (2 * BQ);
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
-        const bool live = k0 + u * BQ + 32 * m + lane < S;  // queries past S: P = 0
+        const bool live = qs0 + u * BQ + 32 * m + lane < S;  // queries past S: P = 0
         // stored negated, as the packed FMAs below take them: -lse (log2
         // units) + log2(rho), so that exp2 gives P'' = rho P; and -lambda D'
         ld_w[32 * m + lane] = live ? kGradRhoLog2 - nl[m] * 1.4426950408889634f : -INFINITY;
@@ -312,7 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
       tc_fence_after();
       const float4* lse4 = reinterpret_cast<const float4*>(ld_w);
       const float4* dd4 = reinterpret_cast<const float4*>(ld_w + BQ);
-      const int mask_from = r - u * BQ;  // columns c < mask_from hold key > query: masked
+      // columns c < mask_from hold key > query: masked (first segment only)
+      const int mask_from = r - (u0 + u) * BQ;
       uint8_t* row = ds_rows;
       // the slot's two 64-column blocks swap roles on every use of the slot
       const uint32_t sblk = slot + 64 * ph, pblk = slot + 64 * (ph ^ 1);
@@ -419,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
       __syncwarp();
       if (lane == 0) mbar_arrive(&dq_free[s]);
       if (qw * 32 < D) {
-        const int q0 = k0 + u * BQ;
+        const int q0 = qs0 + u * BQ;
         const uint32_t cb = (uint32_t)(lane >> 2), cw = (uint32_t)(lane & 3) * 4;
 #pragma unroll
         for (int rd = 0; rd < BQ / DQR; ++rd, ++round) {
@@ -501,7 +529,14 @@ static cudaError_t launch_bwd_t(const AttnBwdArgs& a, int* err, cudaStream_t str
       !make_tmap_bf16(&vm, a.V, a.S, (uint64_t)a.ldkv, a.ldkv, BK, 64) ||
       !make_tmap_bf16(&dm, a.dO, a.S, (uint64_t)a.heads * D, a.ld_do, BQ, 64))
     return cudaErrorInvalidValue;
-  dim3 grid((a.S + BK - 1) / BK, a.heads);
+  // CTAs: segment k of the walks for the key tiles whose walk is longer than
+  // k * walk sub-tiles (see the kernel)
+  const long long NU0 = (a.S + BQ - 1) / BQ, NT = (a.S + BK - 1) / BK;
+  long long ctas = 0;
+  for (long long k = 0; NU0 - k * a.walk > 0; ++k)
+    ctas += std::min(NT, (NU0 - k * a.walk + 1) / 2);
+  if (a.walk <= 0 || a.walk % 2 != 0 || ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+  dim3 grid((unsigned)ctas, a.heads);
   attn_bwd_kernel<D><<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(qm, km, vm, dm, dqm, a, err);
   return cudaGetLastError();
 }

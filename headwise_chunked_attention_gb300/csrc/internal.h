@@ -233,6 +233,7 @@ struct AttnBwdArgs {
   const float* bound;           // GradScales [0], [1] (sigma)
   const float* vmax;            // Vmax of the chunk's KV group
   const float* do_max;          // MdO' of the chunk (lambda)
+  int walk;                     // max query sub-tiles (of 64) one CTA walks; even
 };
 
 cudaError_t launch_attn_bwd(const AttnBwdArgs& a, int* err, cudaStream_t stream);

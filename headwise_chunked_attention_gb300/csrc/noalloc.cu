@@ -51,7 +51,9 @@ extern "C" int upipe_attn_fwd_noalloc(const upipe_shape_t* shape, const upipe_bf
   const int rc = static_scratch(&scratch);
   if (rc != UPIPE_OK) return rc;
   // Nothing in the scratch has to start at zero: every byte the forward reads
-  // is written earlier in the same call.
+  // is written earlier in the same call.  The forward is given exactly the
+  // minimal (mode 0) workspace size, so it always takes the mode-0 layout
+  // whatever else would fit in the array.
   return upipe::attn_fwd_unforked(shape, x, Wq, Wk, Wv, Wo, q_norm_w, k_norm_w, out, lse, scratch,
-                                  (size_t)UPIPE_STATIC_SCRATCH_BYTES, stream);
+                                  need, stream);
 }

@@ -316,6 +316,23 @@ int wgrad_splits(int64_t S, int M, int N, int bn, int sms) {
   return best;
 }
 
+// Longest query walk (sub-tiles of 64 queries) of one attention-backward CTA,
+// whose dK / dV accumulate in TMEM over the walk: the whole walk up to 1M
+// tokens (16384 sub-tiles, as many accumulation steps as the forward's O takes
+// over 1M keys), else segments of 8192 sub-tiles.  UPIPE_BWD_WALK (an even
+// number >= 2) overrides it, e.g. to run the segmented walk on short
+// sequences.
+int bwd_walk(int64_t S) {
+  static const int forced = [] {
+    const char* v = std::getenv("UPIPE_BWD_WALK");
+    const int w = v ? std::atoi(v) : 0;
+    return (w >= 2 && w % 2 == 0) ? w : 0;
+  }();
+  if (forced) return forced;
+  const int64_t nu = (S + 63) / 64;
+  return nu <= 16384 ? (int)((nu + 1) / 2 * 2) : 8192;
+}
+
 // SMs given to a Wo-slice accumulate that runs beside an attention launch: it
 // is bound by HBM (a read-modify-write of the fp32 layer output), which a
 // fifth of the SMs can nearly saturate, and the rest keep the tensor cores of
@@ -832,6 +849,7 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
       a.bound = sc;
       a.vmax = vmax;
       a.do_max = do_max;
+      a.walk = bwd_walk(g.S);
       prof_begin(1, st);
       const cudaError_t e = launch_attn_bwd(a, ds->err, st);
       prof_end(1, st);

@@ -7,6 +7,6 @@ never called by it.  Every function cites the passage it follows; see
 """
 from .attention_layer import (  # noqa: F401
     apply_rope, apply_rope_transpose, causal_attention,
-    layer_backward, layer_backward_tail, layer_forward, layer_loss, project_kv, rms_norm,
+    layer_backward, layer_backward_key_rows, layer_backward_tail, layer_forward, layer_loss, project_kv, rms_norm,
     rms_norm_backward, rope_cos_sin,
 )

@@ -337,6 +337,59 @@ def layer_backward_tail(geom, x: ArrayOrRows, Wq, Wk, Wv, Wo, dout_tail: np.ndar
     return dx
 
 
+def layer_backward_key_rows(geom, x: ArrayOrRows, Wq, Wk, Wv, Wo, q_rows: Sequence[int],
+                            dout_rows: np.ndarray, key_rows: Sequence[int], q_gamma=None,
+                            k_gamma=None):
+    """dx of the early rows ``key_rows`` when the upstream gradient is zero
+    everywhere except on the query rows ``q_rows`` (``dout_rows`` holds those
+    rows of dout), every key row before every query row.  Same chain rule as
+    ``layer_backward``.
+
+    A key row j before every gradient-carrying query has dO_j = 0, so its dq
+    vanishes and dx_j = dk_j Wk + dv_j Wv with dk_j = sum_i ds_ij q_i / sqrt(d)
+    and dv_j = sum_i p_ij do_i over the query rows i only.  Each of those needs
+    p_i and o_i over its full causal row (K, V of positions 0..i), but not the
+    other queries of the sequence: the longest dk / dv sums of a
+    million-token layer (those of its first keys) stay within reach.
+    Returns dx_rows [len(key_rows), hidden]."""
+    q_rows = np.asarray(sorted(q_rows))
+    key_rows = np.asarray(sorted(key_rows))
+    assert key_rows.max() < q_rows.min()
+    d, Hq, Hkv = geom.d, geom.Hq, geom.Hkv
+    g = Hq // Hkv
+    Wq, Wk, Wv, Wo = (np.asarray(w, dtype=np.float64) for w in (Wq, Wk, Wv, Wo))
+    dout_rows = np.asarray(dout_rows, dtype=np.float64)
+    upto = int(q_rows.max()) + 1
+    scale = 1.0 / math.sqrt(d)
+    xq = np.concatenate([_rows(x, int(r), int(r) + 1) for r in q_rows])
+    xk = np.concatenate([_rows(x, int(r), int(r) + 1) for r in key_rows])
+    cos_k, sin_k = rope_cos_sin(key_rows, d, geom.rope_theta)
+    dx = np.zeros((len(key_rows), Wq.shape[1]))
+    for kvh in range(Hkv):
+        sl = slice(kvh * d, (kvh + 1) * d)
+        K, V = project_kv(x, Wk, Wv, geom, kvh, upto, k_gamma)
+        dk = np.zeros((len(key_rows), d))
+        dv = np.zeros((len(key_rows), d))
+        for h in range(kvh * g, (kvh + 1) * g):
+            hs = slice(h * d, (h + 1) * d)
+            q = _qk_post(_head_proj(xq, Wq, h, d), q_rows, geom, q_gamma)
+            o, _, p = causal_attention(q, K, V, q_rows, return_p=True)    # p [nq, upto]
+            do = dout_rows @ Wo[:, hs]
+            D = np.sum(do * o, axis=1, keepdims=True)
+            pk = p[:, key_rows]
+            ds = pk * (do @ V[key_rows].T - D)
+            dk += ds.T @ q * scale
+            dv += pk.T @ do
+        ak = xk @ Wk[sl].T
+        if geom.qk_norm:
+            _, rk = rms_norm(ak, k_gamma, geom.norm_eps)
+            dak = rms_norm_backward(apply_rope_transpose(dk, cos_k, sin_k), ak, rk, k_gamma)[0]
+        else:
+            dak = apply_rope_transpose(dk, cos_k, sin_k)
+        dx += dak @ Wk[sl] + dv @ Wv[sl]
+    return dx
+
+
 def layer_loss(geom, x, Wq, Wk, Wv, Wo, dout, q_gamma=None, k_gamma=None):
     """Scalar L = sum(out * dout); the function whose gradient
     ``layer_backward`` returns (used by the finite-difference pin)."""

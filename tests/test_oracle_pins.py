@@ -357,3 +357,23 @@ def test_tail_backward_equals_full_backward_rows(qk_norm):
     for n in (1, 7, 40):
         tail = O.layer_backward_tail(g, x, Wq, Wk, Wv, Wo, dout[S - n:], n, qg, kg)
         np.testing.assert_allclose(tail, full["dx"][S - n:], atol=1e-12)
+
+
+@pytest.mark.parametrize("qk_norm", [False, True])
+def test_key_rows_backward_equals_full_backward_with_sparse_dout(qk_norm):
+    """dx of early key rows from a few gradient-carrying query rows equals the
+    full chain-rule backward run with dout zero on every other row."""
+    rng = np.random.default_rng(21)
+    g = geom(hidden=24, Hq=4, Hkv=2, d=8, qk_norm=qk_norm)
+    S = 50
+    x, Wq, Wk, Wv, Wo = rand_layer(rng, g, S)
+    qg = 1 + 0.2 * rng.standard_normal(8) if qk_norm else None
+    kg = 1 + 0.2 * rng.standard_normal(8) if qk_norm else None
+    q_rows = [9, 10, 30, 31, 49]
+    dout = np.zeros((S, g.hidden))
+    dout[q_rows] = rng.standard_normal((len(q_rows), g.hidden))
+    full = O.layer_backward(g, x, Wq, Wk, Wv, Wo, dout, qg, kg)
+    keys = list(range(9))
+    part = O.layer_backward_key_rows(g, x, Wq, Wk, Wv, Wo, q_rows, dout[q_rows], keys, qg, kg)
+    np.testing.assert_allclose(part, full["dx"][keys], atol=1e-12)
+    assert np.abs(full["dx"][keys]).max() > 1e-3     # the rows do receive gradient

@@ -121,3 +121,20 @@ def test_backward_gradient_magnitude_invariance(w, chs):
                 rms = np.sqrt(np.mean(v * v))
                 err = np.max(np.abs(got - v)) / rms
                 assert err < 1e-4, f"{name} ch={ch} scale 2^{e}: {err:.2e}"
+
+
+@pytest.mark.parametrize("walk", [2, 6])
+def test_backward_segmented_walks(walk):
+    # Past 1M tokens a key tile's walk over the queries is cut into segments
+    # run by separate CTAs, each adding its dK / dV partial.  UPIPE_BWD_WALK
+    # forces short segments here (2 and 6 sub-tiles of 64 queries), so that
+    # small shapes take that path; the environment is read once per process,
+    # hence the child process.
+    import os
+    import subprocess
+    import sys
+    env = dict(os.environ, UPIPE_BWD_WALK=str(walk))
+    child = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_bwd_walk_child.py")
+    r = subprocess.run([sys.executable, child], env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]

@@ -9,8 +9,13 @@ prefix [0, T] of the sequence, which the oracle's tail backward covers (the
 query rows up to T against the full prefix K and V, and every later query of
 that prefix for their dk, dv); the rows after T must come out exactly zero.
 T = S - 1 checks the last rows and T = S/2 the middle of the sequence.  The
-weight and gain gradients are checked in full on the same geometries at
-8192 tokens, where the whole oracle backward is feasible."""
+first rows, whose dk and dv sum over every later query (the backward's
+longest accumulations: up to 1M tokens one CTA walks all the queries of a key
+tile, 65536 tensor-core accumulation steps at 1M), are checked
+with the upstream gradient non-zero on three windows of query rows only: right
+after the checked rows, in the middle and at the end.  The weight and gain
+gradients are checked in full on the same geometries at 8192 tokens, where
+the whole oracle backward is feasible."""
 import numpy as np
 import pytest
 import torch
@@ -138,3 +143,28 @@ def test_backward_weight_gradients_full_geometry(name):
             for nm in ("dq_gamma", "dk_gamma"):
                 assert_close(f64(g[nm]), ref[nm], f"{name} {nm} ch={ch}",
                              GAIN_MAX_REL, GAIN_MEAN_REL)
+
+
+@pytest.mark.parametrize("name", ["llama3-8b-rank-s1m", "qwen3-32b-rank-s1m"])
+def test_backward_first_rows_at_full_size(name):
+    import headwise_chunked_attention_gb300 as u
+    w = WORKLOADS[name]
+    ch = w.chunk_heads[0]
+    t = make_inputs(w, seed=3, device="cuda", with_grad=True, norm_gains="random")
+    n = N_ROWS
+    q_rows = np.concatenate([np.arange(n, n + 128), np.arange(w.S // 2 - 64, w.S // 2 + 64),
+                             np.arange(w.S - 128, w.S)])
+    idx = torch.from_numpy(q_rows).to("cuda")
+    dout = torch.zeros_like(t["dout"])
+    dout[idx] = t["dout"][idx]
+    g = _gpu_fwd_bwd(u, w, ch, t, dout, False)
+    for k, v in g.items():
+        assert v is None or torch.isfinite(v).all(), k
+    dx_rows = f64(g["dx"][:n])
+    del g
+    xg = t["x"]
+    a = {k: f64(v) for k, v in t.items() if k not in ("x", "dout")}
+    ref = O.layer_backward_key_rows(w, lambda lo, hi: f64(xg[lo:hi]), a["Wq"], a["Wk"],
+                                    a["Wv"], a["Wo"], q_rows, f64(dout[idx]), np.arange(n),
+                                    a.get("q_gamma"), a.get("k_gamma"))
+    assert_close(dx_rows, ref, f"{name} dx rows 0..{n - 1}")
