@@ -80,6 +80,12 @@ def recompute_flops(w, saved_o=False):
 # ncu capture, keyed by kernel, workload and chunk size, with the sha256 of the
 # kernel's source file at capture time: a changed kernel reports null.
 NCU_TRAFFIC = {
+    # full captures of these launches exceed the profiling size rule, so the
+    # bytes were taken at S = 262144 (same geometry and chunk size) and scaled
+    # by the causal pairs to S = 1,048,576 (x16.0); from 65536 to 262144 the
+    # traffic grew 3.7-4.0x per doubling of S, in step with the pairs
+    ("attn_fwd_kernel", "llama3-8b-rank-s1m", 1): (11314091008, "d17eb830287fe861"),
+    ("attn_bwd_kernel", "llama3-8b-rank-s1m", 1): (53681712128, "74fa113cbcfbec9a"),
 }
 KERNEL_SOURCES = {"attn_fwd_kernel": "attn_fwd.cu", "attn_bwd_kernel": "attn_bwd.cu"}
 
@@ -90,7 +96,10 @@ def kernel_source_sha(kernel):
     return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
 
 
-def traffic_of(kernel, workload, ch):
+def traffic_of(kernel, workload, ch, S=None):
+    from workloads import WORKLOADS
+    if S is not None and workload in WORKLOADS and S != WORKLOADS[workload].S:
+        return None
     ent = NCU_TRAFFIC.get((kernel, workload, ch))
     if ent is None or ent[1] != kernel_source_sha(kernel):
         return None
@@ -420,7 +429,7 @@ def measure(u, w, ch, mode, steps, warmup, dist, world, rank, dev, full=True, sw
                 "peak_kind": peak_kind, "launches_timed": len(durations),
                 "avg_launch_ms": round(avg_ms, 4), "flops_per_launch": fl,
                 "ms_per_step_timed_pass": round(1e3 * t_pass / k, 3),
-                "traffic": traffic_of(kernel, w.name, ch)}
+                "traffic": traffic_of(kernel, w.name, ch, w.S)}
 
     roof_fwd = roofline("attn_fwd_kernel", 0, 4.0, nchunks * (2 if mode else 1))
     roof_bwd = roofline("attn_bwd_kernel", 1, 10.0, nchunks) if mode else None
@@ -667,11 +676,17 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end and HBM-kernel measurements (profiling runs)")
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="run the workload's geometry at this many tokens instead")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
     from workloads import WORKLOADS
     w = WORKLOADS[args.workload]
+    if args.seq_len:
+        w = w.with_(S=args.seq_len)
     if args.pass_ is None:
         args.pass_ = "fwdbwd" if "bwd" in w.passes else "fwd"
     ch = args.chunk_heads or w.chunk_heads[0]
@@ -699,7 +714,7 @@ def main():
     dev = torch.device("cuda", local)
     mode = 1 if args.pass_ == "fwdbwd" else 0
     r = measure(u, w, ch, mode, args.steps, args.warmup, dist, world, rank, dev,
-                sweep_on=not args.no_sweep, cpu_on=not args.no_cpu)
+                full=not args.no_e2e, sweep_on=not args.no_sweep, cpu_on=not args.no_cpu)
     secondary = None
     if not args.no_secondary and args.workload != SECONDARY_WORKLOAD:
         w2 = WORKLOADS[SECONDARY_WORKLOAD]

@@ -20,12 +20,32 @@
 #include <cstring>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/upipe.h"
 #include "internal.h"
 
 namespace upipe {
 
 __device__ int g_device_error = 0;
+
+// NVTX range over the host-side enqueue of one entry point or one chunk, so
+// that a timeline tool shows the chunk loop (header-only NVTX: without a tool
+// attached each push/pop is a no-op call).
+struct NvtxRange {
+  explicit NvtxRange(const char* what, int chunk = -1) {
+    if (chunk < 0) {
+      nvtxRangePushA(what);
+    } else {
+      char name[64];
+      std::snprintf(name, sizeof name, "%s chunk %d", what, chunk);
+      nvtxRangePushA(name);
+    }
+  }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 namespace {
 
@@ -428,6 +448,7 @@ static int attn_fwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
                          upipe_bf16* attn_o, void* stream, bool fork) {
   Geo g;
   UPIPE_TRY(check_shape(shape, &g));
+  NvtxRange call_range("upipe_attn_fwd");
   const bf16* x = reinterpret_cast<const bf16*>(x_);
   const bf16* Wq = reinterpret_cast<const bf16*>(Wq_);
   const bf16* Wk = reinterpret_cast<const bf16*>(Wk_);
@@ -540,6 +561,7 @@ static int attn_fwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
     return UPIPE_OK;
   };
   for (int c = 0; c < g.nchunks; ++c) {
+    NvtxRange chunk_range("upipe_attn_fwd", c);
     const int h0 = c * g.ch;
     const int kv0 = h0 / g.g;
     const bool new_group = (g.ch >= g.g) || (h0 % g.g == 0);
@@ -621,6 +643,7 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
                          void* stream) {
   Geo g;
   UPIPE_TRY(check_shape(shape, &g));
+  NvtxRange call_range("upipe_attn_bwd");
   const bf16* o_saved = reinterpret_cast<const bf16*>(o_saved_);
   if (o_saved && !aligned16(o_saved)) return UPIPE_ERR_INVALID_ARG;
   const bf16* x = reinterpret_cast<const bf16*>(x_);
@@ -774,6 +797,7 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
   };
 
   for (int c = 0; c < g.nchunks; ++c) {
+    NvtxRange chunk_range("upipe_attn_bwd", c);
     const int h0 = c * g.ch;
     const int kv0 = h0 / g.g;
     const bool new_group = (g.ch >= g.g) || (h0 % g.g == 0);

@@ -136,3 +136,19 @@ def test_saved_o_backward_validates_before_any_launch(u):
     assert L.upipe_attn_bwd_saved_o(*args(p[13] + 8)) == 1  # misaligned attn_o
     bad = u.Shape.of(w, 3)                                   # 3 does not divide Hq
     assert L.upipe_attn_bwd_saved_o(ctypes.byref(bad), *args(p[13])[1:]) == 1
+
+
+def test_guard_margins_catch_writes_outside_the_buffer():
+    # the guard helper itself, on the CPU: writes inside the buffer pass, one
+    # byte changed just after its end or just before its start is reported
+    import torch
+    from tests._guard import guarded
+    g = guarded((3, 5), device="cpu")
+    g.t.fill_(1.0)
+    assert (g.raw.data_ptr() + g.off) % 256 == 0
+    g.check("inside only")
+    for edge in ("after", "before"):
+        h = guarded((3, 5), device="cpu")
+        h.raw[h.off + h.nbytes if edge == "after" else h.off - 1] = 0
+        with pytest.raises(AssertionError):
+            h.check(edge)

@@ -9,6 +9,7 @@ import torch
 import oracle as O
 from workloads import WORKLOADS, Workload, make_inputs
 from tests._util import f64, assert_close, GAIN_MAX_REL, GAIN_MEAN_REL
+from tests._guard import guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -18,25 +19,34 @@ def run_fwd_bwd(w, ch, inp, saved_o=False, dout_scale=None):
     dev = "cuda"
     t = {k: v.to(dev) for k, v in inp.items()}
     sh = u.Shape.of(w, ch)
-    out = torch.empty(w.S, w.hidden, device=dev)
-    lse = torch.empty(w.Hq, w.S, device=dev)
-    ws = torch.empty(u.workspace_bytes(sh, 1), dtype=torch.uint8, device=dev)
-    o = torch.empty(w.S, w.Hq * w.d, dtype=torch.bfloat16, device=dev) if saved_o else None
+    # every buffer the library writes sits inside guard margins that must come
+    # back untouched
+    gb = {"out": guarded((w.S, w.hidden)), "lse": guarded((w.Hq, w.S)),
+          "workspace": guarded((u.workspace_bytes(sh, 1),), torch.uint8)}
+    if saved_o:
+        gb["attn_o"] = guarded((w.S, w.Hq * w.d), torch.bfloat16)
+    out, lse, ws = gb["out"].t, gb["lse"].t, gb["workspace"].t
+    o = gb["attn_o"].t if saved_o else None
     u.attn_fwd(sh, t["x"], t["Wq"], t["Wk"], t["Wv"], t["Wo"], out, lse, ws,
                t.get("q_gamma"), t.get("k_gamma"), o)
     if saved_o:   # the backward must not depend on what the forward left in ws
         ws.fill_(0xFF)
     dout = t["dout"] if dout_scale is None else (t["dout"].float() * dout_scale).to(torch.bfloat16)
-    g = {n: torch.full(t[src].shape, float("nan"), device=dev)
-         for n, src in [("dx", "x"), ("dWq", "Wq"), ("dWk", "Wk"), ("dWv", "Wv"),
-                        ("dWo", "Wo")]}
-    dqg = torch.full((w.d,), float("nan"), device=dev) if w.qk_norm else None
-    dkg = torch.full((w.d,), float("nan"), device=dev) if w.qk_norm else None
+    for n, src in [("dx", "x"), ("dWq", "Wq"), ("dWk", "Wk"), ("dWv", "Wv"), ("dWo", "Wo")]:
+        gb[n] = guarded(tuple(t[src].shape), fill=float("nan"))
+    if w.qk_norm:
+        gb["dq_gamma"] = guarded((w.d,), fill=float("nan"))
+        gb["dk_gamma"] = guarded((w.d,), fill=float("nan"))
+    g = {n: gb[n].t for n in ("dx", "dWq", "dWk", "dWv", "dWo")}
+    dqg = gb["dq_gamma"].t if w.qk_norm else None
+    dkg = gb["dk_gamma"].t if w.qk_norm else None
     u.attn_bwd(sh, t["x"], t["Wq"], t["Wk"], t["Wv"], t["Wo"], dout, lse,
                g["dx"], g["dWq"], g["dWk"], g["dWv"], g["dWo"], ws,
                t.get("q_gamma"), t.get("k_gamma"), dqg, dkg, attn_o=o)
     torch.cuda.synchronize()
     assert u.last_error() == 0
+    for name, b in gb.items():
+        b.check(name)
     g["dq_gamma"], g["dk_gamma"] = dqg, dkg
     return g
 

@@ -7,6 +7,7 @@ import torch
 import oracle as O
 from workloads import WORKLOADS, Workload, make_inputs, sample_rows
 from tests._util import f64, assert_close, LSE_ABS
+from tests._guard import guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -18,18 +19,24 @@ def U():
 
 
 def run_fwd(w, ch, inp, debug=True, expect_error=0):
+    # out, lse, attn_o and the workspace sit inside guard margins that must
+    # come back untouched
     u = U()
     dev = "cuda"
     t = {k: v.to(dev) for k, v in inp.items()}
     shape = u.Shape.of(w, ch)
-    out = torch.empty(w.S, w.hidden, device=dev, dtype=torch.float32)
-    lse = torch.empty(w.Hq, w.S, device=dev, dtype=torch.float32)
-    ws = torch.empty(u.workspace_bytes(shape, 0), device=dev, dtype=torch.uint8)
-    o = torch.empty(w.S, w.Hq * w.d, device=dev, dtype=torch.bfloat16) if debug else None
+    g = {"out": guarded((w.S, w.hidden)), "lse": guarded((w.Hq, w.S)),
+         "workspace": guarded((u.workspace_bytes(shape, 0),), torch.uint8)}
+    if debug:
+        g["attn_o"] = guarded((w.S, w.Hq * w.d), torch.bfloat16)
+    out, lse, ws = g["out"].t, g["lse"].t, g["workspace"].t
+    o = g["attn_o"].t if debug else None
     u.attn_fwd(shape, t["x"], t["Wq"], t["Wk"], t["Wv"], t["Wo"], out, lse, ws,
                t.get("q_gamma"), t.get("k_gamma"), o)
     torch.cuda.synchronize()
     assert u.last_error() == expect_error
+    for name, b in g.items():
+        b.check(name)
     return out, lse, o
 
 

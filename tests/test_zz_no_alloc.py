@@ -13,6 +13,7 @@ import pytest
 import torch
 
 from workloads import WORKLOADS, Workload, make_inputs
+from tests._guard import guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -59,14 +60,18 @@ def test_noalloc_forward_matches_allocating_forward(w, ch):
     assert u.last_error() == 0
     stream = torch.cuda.current_stream().cuda_stream
     for call in range(2):   # two calls in a row share the static scratch
-        out = torch.full((w.S, w.hidden), float("nan"), device="cuda")
-        lse = torch.full((w.Hq, w.S), float("nan"), device="cuda")
+        # out and lse inside guard margins that must come back untouched
+        g_out = guarded((w.S, w.hidden), fill=float("nan"))
+        g_lse = guarded((w.Hq, w.S), fill=float("nan"))
+        out, lse = g_out.t, g_lse.t
         rc = fn(ctypes.byref(shape), ptr(inp["x"]), ptr(inp["Wq"]), ptr(inp["Wk"]),
                 ptr(inp["Wv"]), ptr(inp["Wo"]), ptr(inp.get("q_gamma")),
                 ptr(inp.get("k_gamma")), ptr(out), ptr(lse), stream)
         assert rc == 0, rc
         torch.cuda.synchronize()
         assert u.last_error() == 0
+        g_out.check("out")
+        g_lse.check("lse")
         assert torch.equal(out, out_ref), f"out, call {call}"
         assert torch.equal(lse, lse_ref), f"lse, call {call}"
 
