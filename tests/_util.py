@@ -29,10 +29,10 @@ def rel_errs(got, ref, rowwise=True):
 
 # tolerances of the attention layer (bf16 inputs, fp32 accumulation):
 MAX_REL, MEAN_REL, LSE_ABS = 2e-2, 2e-3, 1e-3
-# The layer's bounds are stated for its output and its input gradient.  The
-# RMSNorm gain gradients are d-long sums over every row and head of a group;
-# they are checked against the oracle with the weight-gradient sanity bound.
-GAIN_MAX_REL, GAIN_MEAN_REL = 5e-2, 5e-3
+# The layer's bounds are stated for its output and its input gradient; the
+# weight gradients and the RMSNorm gain gradients are held to the same bounds
+# (measured against the float64 layer: gain gradients ~8e-4 mean).
+GAIN_MAX_REL, GAIN_MEAN_REL = MAX_REL, MEAN_REL
 
 
 def assert_close(got, ref, what, max_rel=MAX_REL, mean_rel=MEAN_REL):
