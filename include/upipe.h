@@ -84,7 +84,7 @@ typedef struct {
 enum {
   UPIPE_OK = 0,
   UPIPE_ERR_INVALID_ARG = 1,          /* NULL pointer, bad size, misalignment */
-  UPIPE_ERR_UNSUPPORTED = 2,          /* a shape this build does not handle  */
+  UPIPE_ERR_UNSUPPORTED = 2,          /* a shape the library does not handle */
   UPIPE_ERR_WORKSPACE_TOO_SMALL = 3,  /* ws_bytes < upipe_workspace_bytes()  */
   UPIPE_ERR_CUDA = 4,                 /* a CUDA runtime/driver call failed    */
   UPIPE_ERR_DEVICE_TIMEOUT = 5,       /* a kernel's bounded wait expired      */

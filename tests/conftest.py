@@ -12,7 +12,7 @@ def pytest_configure(config):
     config.addinivalue_line(
         "markers", "gpu: needs a GB300 and the built CUDA library")
     config.addinivalue_line(
-        "markers", "slow: full-size workloads (minutes on a GPU box)")
+        "markers", "slow: full-size workloads (minutes on a GB300)")
 
 
 def pytest_collection_modifyitems(config, items):

@@ -58,3 +58,18 @@ def test_recompute_flops():
     proj = fwd - attn - wo
     assert bench.recompute_flops(w) == pytest.approx(proj + attn, rel=1e-12)
     assert bench.recompute_flops(w, saved_o=True) == pytest.approx(proj, rel=1e-12)
+
+
+def test_ncu_traffic_is_reported_only_for_the_captured_kernel_and_size():
+    # the DRAM bytes per launch belong to one kernel source and one workload
+    # size: a different S or an edited kernel reports null, never a stale figure
+    w = WORKLOADS["llama3-8b-rank-s1m"]
+    for kernel in ("attn_fwd_kernel", "attn_bwd_kernel"):
+        got = bench.traffic_of(kernel, w.name, 1, w.S)
+        ent = bench.NCU_TRAFFIC[(kernel, w.name, 1)]
+        assert got == (ent[0] if ent[1] == bench.kernel_source_sha(kernel) else None)
+        assert bench.traffic_of(kernel, w.name, 1, 65536) is None
+        assert bench.traffic_of(kernel, w.name, 2, w.S) is None
+    # the scaled 1M figures are 16x the 256K captures (the causal pairs ratio)
+    S1, S2 = w.S, 262144
+    assert abs(S1 * (S1 + 1) / (S2 * (S2 + 1)) - 16.0) < 1e-4
