@@ -373,6 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* acc_row =
           have_acc ? a.flush + ((size_t)sm_id() * 256 + 128 * t + r) * D : nullptr;
       bf16* op = a.O + (long long)qpos * a.ldo + head * D;
+      const __half* dop = a.dO ? a.dO + (long long)qpos * a.ld_do + head * D : nullptr;
+      float dot = 0.f;  // D' = dO' . o over the fp32 o (the backward's recompute)
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t rr[32];
@@ -382,6 +384,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             rr[i] = __float_as_uint(fmaf(acc_row[32 * c + i], keep, __uint_as_float(rr[i])));
+        }
+        if (live && dop) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            const uint4 dv = *reinterpret_cast<const uint4*>(dop + 32 * c + i);
+            const uint32_t* dw = &dv.x;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float2 g = unpack_f16(dw[j]);
+              dot = fmaf(g.x, __uint_as_float(rr[i + 2 * j]) * inv_l, dot);
+              dot = fmaf(g.y, __uint_as_float(rr[i + 2 * j + 1]) * inv_l, dot);
+            }
+          }
         }
         if (live) {
 #pragma unroll
@@ -398,6 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (live && a.lse)
         a.lse[(long long)head * a.lse_stride + qpos] =
             (m_run - kPShift + __log2f(l_run)) * 0.69314718055994531f;
+      if (live && dop) a.D[(long long)head * a.S + qpos] = dot;
     }
   }
 

@@ -29,8 +29,8 @@
 //                   staged per warp in shared memory and written by TMA store
 //                   (first chunk) or TMA reduce-add (later chunks: the
 //                   read-modify-write runs in L2, the SM never reads out);
-//   EPI_DO          dO_c = dOut Wo_c, scaled and stored in fp16, with
-//                   D = rowsum(dO * O) per head;
+//   EPI_DO          dO_c = dOut Wo_c, scaled and stored in fp16 (and, given
+//                   O, D = rowsum(dO * O) per head);
 //   EPI_F32_ATOMIC  split-K weight gradients, reduced with red.global.add.
 #include <algorithm>
 
@@ -387,12 +387,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tbase + c * 32, r);
           tmem_ld_wait(r);
           if (live) {
-            const bf16* op = ep.O + m * ep.ld_o + n0 + c * 32;
             __half* dp = ep.dO + m * ep.ld_do + n0 + c * 32;
 #pragma unroll
             for (int i = 0; i < 32; i += 8) {
-              const uint4 ov = *reinterpret_cast<const uint4*>(op + i);
-              const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
               uint4 w;
               uint32_t* wp = &w.x;
 #pragma unroll
@@ -402,18 +399,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 wp[j] = pack_f16(__uint_as_float(r[i + 2 * j]) * sigma,
                                  __uint_as_float(r[i + 2 * j + 1]) * sigma);
                 const float2 dv = unpack_f16(wp[j]);
-                const float2 of = __bfloat1622float2(o2[j]);
-                dot = fmaf(dv.x, of.x, dot);
-                dot = fmaf(dv.y, of.y, dot);
                 ss = fmaf(dv.x, dv.x, ss);
                 ss = fmaf(dv.y, dv.y, ss);
+              }
+              if (ep.O) {
+                const uint4 ov = *reinterpret_cast<const uint4*>(ep.O + m * ep.ld_o + n0 + c * 32 + i);
+                const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const float2 dv = unpack_f16(wp[j]);
+                  const float2 of = __bfloat1622float2(o2[j]);
+                  dot = fmaf(dv.x, of.x, dot);
+                  dot = fmaf(dv.y, of.y, dot);
+                }
               }
               *reinterpret_cast<uint4*>(dp + i) = w;
             }
           }
         }
         if (live) {
-          ep.D[(long long)head * g.M + m] = dot;
+          if (ep.O) ep.D[(long long)head * g.M + m] = dot;
           atomic_max_nonneg(ep.do_max, sqrtf(ss));
         }
       } else if constexpr (EPI == EPI_F32) {

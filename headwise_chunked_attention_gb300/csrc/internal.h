@@ -145,9 +145,10 @@ struct EpiParams {
   int beta;          // EPI_F32: 0 store, 1 add (both through the C tensor map)
   // EPI_F32_ATOMIC with M segments: output base of each segment (row 0)
   float* mseg_c[6];
-  // EPI_DO: dO' = sigma * dO in fp16 with sigma = grad_sigma(bound), D' =
-  // rowsum(dO' * O) from the stored fp16 dO', and the running max of
-  // ||dO'_row||_2 over rows and heads in *do_max
+  // EPI_DO: dO' = sigma * dO in fp16 with sigma = grad_sigma(bound), the
+  // running max of ||dO'_row||_2 over rows and heads in *do_max, and (when O
+  // is given: the saved-O backward) D' = rowsum(dO' * O) from the stored fp16
+  // dO'
   __half* dO;
   int ld_do;
   const bf16* O;
@@ -208,6 +209,11 @@ struct AttnFwdArgs {
   long long lse_stride;
   float scale_log2; // log2(e) / sqrt(d)
   float* flush;     // nullptr, or [kFlushSlots][256 rows][d] fp32 per-SM O accumulators
+  // optional (the backward's recompute): D'_i = dO'_i . o_i from the fp32 o
+  // before its bf16 rounding, so that D' matches the dP' = dO' v^T the
+  // attention backward forms from the same fp16 V
+  const __half* dO; int ld_do;  // [S, ld_do] fp16, head i at column i*d
+  float* D;                     // [heads][S]
 };
 
 // The attention forward folds its TMEM O accumulator into an fp32 row in

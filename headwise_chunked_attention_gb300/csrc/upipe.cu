@@ -398,9 +398,12 @@ int project_chunk(const Geo& g, const DeviceState* ds, cudaStream_t st, const CU
   return UPIPE_OK;
 }
 
+// dO / D (the backward's recompute): also form D' = dO' . o per row from the
+// kernel's fp32 o (see AttnFwdArgs).
 int attention_chunk(const Geo& g, const DeviceState* ds, cudaStream_t st, const __half* Q,
                     const __half* K, const __half* V, int h0, int kv0, bf16* O, int ldo,
-                    float* lse, float* flush) {
+                    float* lse, float* flush, const __half* dO = nullptr, int ld_do = 0,
+                    float* D = nullptr) {
   const int d = g.d;
   CUtensorMap qm, km, vm;
   UPIPE_MAP(&qm, Q, g.S, (uint64_t)g.ch * d, (uint64_t)g.ch * d, 128, 64);
@@ -418,6 +421,9 @@ int attention_chunk(const Geo& g, const DeviceState* ds, cudaStream_t st, const 
   a.lse_stride = g.S;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
   a.flush = flush;
+  a.dO = dO;
+  a.ld_do = ld_do;
+  a.D = D;
   prof_begin(0, st);
   const cudaError_t e = launch_attn_fwd(qm, km, vm, a, d, ds->err, st);
   prof_end(0, st);
@@ -802,7 +808,7 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
     const int kv0 = h0 / g.g;
     const bool new_group = (g.ch >= g.g) || (h0 % g.g == 0);
     const bool last_of_group = (g.ch >= g.g) || ((h0 + g.ch) % g.g == 0);
-    // 1. recompute Q (and K, V) and the attention output of the chunk
+    // 1. recompute Q (and K, V) of the chunk
     float* vmax = sc + 2 + kv0;     // the norm maximum of this group's V rows
     float* do_max = sc + 2 + g.Hkv + c;
     UPIPE_TRY(project_chunk(g, ds, st, xmap, Wq, Wk, Wv, q_norm_w, k_norm_w, shape->norm_eps, h0,
@@ -815,9 +821,9 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
     // forward's saved copy
     const bf16* Oc = o_saved ? o_saved + (size_t)h0 * d : Ows;
     const int ldo = o_saved ? g.Hq * d : g.ch * d;
-    if (!o_saved)
-      UPIPE_TRY(attention_chunk(g, ds, st, Q, K, V, h0, kv0, Ows, g.ch * d, nullptr, flush));
-    // 2. dO_c = dout Wo_c, D = rowsum(dO * O); dWo_c = dout^T O_c
+    // 2. dO'_c = sigma dout Wo_c; D' = rowsum(dO' * O): with the saved O from
+    //    its bf16 copy here, else from the fp32 o inside the recomputed
+    //    attention (3.), whose fp16 V the attention backward's dP' uses too
     {
       CUtensorMap wom;
       UPIPE_MAP(&wom, Wo + (size_t)h0 * d, g.hidden, (uint64_t)g.ch * d, (uint64_t)g.Hq * d, 64,
@@ -825,7 +831,7 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
       EpiParams ep{};
       ep.dO = dO;
       ep.ld_do = g.ch * d;
-      ep.O = Oc;
+      ep.O = o_saved ? Oc : nullptr;
       ep.ld_o = ldo;
       ep.D = Dv;
       ep.bound = sc;
@@ -833,6 +839,13 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
       GemmArgs ga{(int)g.S, g.ch * d, g.hidden, 1, d};
       UPIPE_CUDA(launch_gemm(d, false, true, EPI_DO, &dout_k, 1, &wom, 1, ga, ep, ds->err,
                              ds->num_sms, st));
+    }
+    // 3. the recomputed attention output (and D')
+    if (!o_saved)
+      UPIPE_TRY(attention_chunk(g, ds, st, Q, K, V, h0, kv0, Ows, g.ch * d, nullptr, flush, dO,
+                                g.ch * d, Dv));
+    // 4. dWo_c = dout^T O_c
+    {
       CUtensorMap om;
       UPIPE_MAP(&om, Oc, g.S, (uint64_t)g.ch * d, (uint64_t)ldo, 64, 64);
       EpiParams ep2{};
@@ -844,7 +857,7 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
       UPIPE_CUDA(launch_gemm(bn, true, true, EPI_F32_ATOMIC, &dout_mn, 1, &om, 1, gb, ep2, ds->err,
                              ds->num_sms, st));
     }
-    // 3. attention backward: dQ_c (fresh), dK/dV (accumulated over the group)
+    // 5. attention backward: dQ_c (fresh), dK/dV (accumulated over the group)
     UPIPE_CUDA(cudaMemsetAsync(dQ, 0, sizeof(float) * S * g.ch * d, st));
     {
       AttnBwdArgs a{};
@@ -879,7 +892,7 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
       prof_end(1, st);
       UPIPE_CUDA(e);
     }
-    // 4. dQ -> gradient of the Q projection output (RoPE^T, RMSNorm backward)
+    // 6. dQ -> gradient of the Q projection output (RoPE^T, RMSNorm backward)
     //    as bf16 hi (into the dO buffer: dO is dead now) + lo (into the O
     //    buffer: O is dead after the dO / dWo GEMMs); dx += dA_q Wq_c;
     //    dWq_c = dA_q^T x, each as a hi and a lo GEMM
@@ -910,7 +923,7 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
     float* dWq_c = dWq + (size_t)h0 * d * g.hidden;
     DwSeg dws[kMaxASegs] = {{dO_hi, g.ch * d, dWq_c}, {Ows, g.ch * d, dWq_c}};
     int ndx = 2;
-    // 5. at the group's last chunk: dK -> dA_k (hi over K, lo beside it),
+    // 7. at the group's last chunk: dK -> dA_k (hi over K, lo beside it),
     //    dV -> hi over V and lo beside it
     if (last_of_group) {
       QkBwdArgs q{};
@@ -949,7 +962,7 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
         dxs[ndx++] = {gv, g.kvc * d, Wv_g};
       }
     }
-    // 6. dWq (and the group's dWk, dWv) and dx (+)= the chunk's Q part (and
+    // 8. dWq (and the group's dWk, dWv) and dx (+)= the chunk's Q part (and
     //    the group's K and V parts), each as one GEMM over all parts
     UPIPE_TRY(dw_gemm(dws, ndx));
     UPIPE_TRY(dx_gemm(dxs, ndx));
