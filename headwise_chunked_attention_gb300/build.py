@@ -40,7 +40,20 @@ def _stale(obj: str, deps) -> bool:
 
 
 def build(verbose: bool = False, force: bool = False) -> str:
+    """Compile what is stale and link libupipe.so.  Processes that build at
+    the same time (one per rank under torchrun) take turns on a file lock,
+    so no object file is written by two nvcc runs at once."""
+    import fcntl
     os.makedirs(OUT, exist_ok=True)
+    with open(os.path.join(OUT, ".build.lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            return _build_locked(verbose, force)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build_locked(verbose: bool, force: bool) -> str:
     headers = [os.path.join(CSRC, h) for h in os.listdir(CSRC)
                if h.endswith((".h", ".cuh"))]
     headers.append(os.path.join(ROOT, "include", "upipe.h"))
