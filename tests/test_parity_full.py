@@ -168,3 +168,50 @@ def test_backward_first_rows_at_full_size(name):
                                     a["Wv"], a["Wo"], q_rows, f64(dout[idx]), np.arange(n),
                                     a.get("q_gamma"), a.get("k_gamma"))
     assert_close(dx_rows, ref, f"{name} dx rows 0..{n - 1}")
+
+
+def test_backward_first_rows_at_5m():
+    # Past 1M tokens a key tile's query walk is split across CTAs (segments of
+    # 8192 sub-tiles, 10 for the first key tiles at 5M), each adding its dK/dV
+    # partial: the first rows' dx, whose dk and dv sum over all 5M queries,
+    # checked against the oracle with dout non-zero on three windows.  x,
+    # dout, dx and out need ~190 GB of the device.
+    import headwise_chunked_attention_gb300 as u
+    free, _ = torch.cuda.mem_get_info()
+    if free < 200e9:
+        pytest.skip(f"needs ~190 GB of free device memory, {free / 1e9:.0f} GB free")
+    w = WORKLOADS["llama3-8b-rank-s5m"]
+    t = make_inputs(w, seed=3, device="cuda")
+    n = 192
+    q_rows = np.concatenate([np.arange(n, n + 64), np.arange(w.S // 2 - 32, w.S // 2 + 32),
+                             np.arange(w.S - 64, w.S)])
+    idx = torch.from_numpy(q_rows).to("cuda")
+    dout = torch.zeros(w.S, w.hidden, device="cuda", dtype=torch.bfloat16)
+    gen = torch.Generator(device="cuda").manual_seed(7)
+    dout[idx] = torch.randn(len(q_rows), w.hidden, device="cuda", generator=gen).to(torch.bfloat16)
+    sh = u.Shape.of(w, 1)
+    ws = torch.empty(u.workspace_bytes(sh, 1), dtype=torch.uint8, device="cuda")
+    lse = torch.empty(w.Hq, w.S, device="cuda")
+    out = torch.empty(w.S, w.hidden, device="cuda")
+    u.attn_fwd(sh, t["x"], t["Wq"], t["Wk"], t["Wv"], t["Wo"], out, lse, ws)
+    torch.cuda.synchronize()
+    del out
+    torch.cuda.empty_cache()
+    g = {n_: torch.empty(t[s].shape, device="cuda") for n_, s in
+         [("dx", "x"), ("dWq", "Wq"), ("dWk", "Wk"), ("dWv", "Wv"), ("dWo", "Wo")]}
+    u.attn_bwd(sh, t["x"], t["Wq"], t["Wk"], t["Wv"], t["Wo"], dout, lse, g["dx"], g["dWq"],
+               g["dWk"], g["dWv"], g["dWo"], ws)
+    torch.cuda.synchronize()
+    assert u.last_error() == 0
+    for k, v in g.items():           # in blocks: a whole-tensor isfinite needs 80 GB more
+        flat = v.view(-1)
+        for lo in range(0, flat.numel(), 1 << 28):
+            assert torch.isfinite(flat[lo:lo + (1 << 28)]).all().item(), k
+    dx_rows = f64(g["dx"][:n])
+    del g, ws
+    torch.cuda.empty_cache()
+    xg = t["x"]
+    a = {k: f64(v) for k, v in t.items() if k != "x"}
+    ref = O.layer_backward_key_rows(w, lambda lo, hi: f64(xg[lo:hi]), a["Wq"], a["Wk"], a["Wv"],
+                                    a["Wo"], q_rows, f64(dout[idx]), np.arange(n))
+    assert_close(dx_rows, ref, "5M dx rows 0..191")
