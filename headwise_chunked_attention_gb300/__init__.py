@@ -6,6 +6,6 @@ PyTorch only provides device memory and the current stream.  There is no CPU
 fallback: without the built library every call raises.
 """
 from ._binding import (  # noqa: F401
-    UpipeError, Shape, KernelTimer, attn_bwd, attn_fwd, last_error, lib, lib_path,
+    UpipeError, Shape, KernelTimer, attn_bwd, attn_fwd, attn_fwd_fused, last_error, lib, lib_path,
     workspace_bytes, selftest_wait_timeout, ERR_NAMES, ERR_DEVICE_TIMEOUT, ERR_RANGE,
 )

@@ -59,6 +59,9 @@ def lib():
         L.upipe_workspace_bytes.restype = ctypes.c_size_t
         L.upipe_attn_fwd.argtypes = [ctypes.POINTER(Shape)] + [P] * 9 + [ctypes.c_size_t, P, P]
         L.upipe_attn_fwd.restype = ctypes.c_int
+        L.upipe_attn_fwd_fused.argtypes = ([ctypes.POINTER(Shape)] + [P] * 9 +
+                                           [ctypes.c_size_t, P])
+        L.upipe_attn_fwd_fused.restype = ctypes.c_int
         L.upipe_attn_bwd.argtypes = ([ctypes.POINTER(Shape)] + [P] * 17 +
                                      [ctypes.c_size_t, P])
         L.upipe_attn_bwd.restype = ctypes.c_int
@@ -122,6 +125,21 @@ def attn_fwd(shape: Shape, x, Wq, Wk, Wv, Wo, out, lse, workspace,
     _check(rc, "upipe_attn_fwd")
 
 
+def attn_fwd_fused(shape: Shape, x, Wq, Wk, Wv, Wo, out, lse, workspace,
+                   q_norm_w=None, k_norm_w=None, stream=None):
+    """upipe_attn_fwd_fused on torch tensors: the forward with each chunk's
+    Wo-slice accumulate done by the attention kernel (workspace of
+    ``workspace_bytes(shape, 3)`` bytes)."""
+    bf = torch.bfloat16
+    rc = lib().upipe_attn_fwd_fused(
+        ctypes.byref(shape), _ptr(x, bf, "x"), _ptr(Wq, bf, "Wq"), _ptr(Wk, bf, "Wk"),
+        _ptr(Wv, bf, "Wv"), _ptr(Wo, bf, "Wo"), _ptr(q_norm_w, torch.float32, "q_norm_w"),
+        _ptr(k_norm_w, torch.float32, "k_norm_w"), _ptr(out, torch.float32, "out"),
+        _ptr(lse, torch.float32, "lse"), _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "upipe_attn_fwd_fused")
+
+
 def attn_bwd(shape: Shape, x, Wq, Wk, Wv, Wo, dout, lse, dx, dWq, dWk, dWv, dWo,
              workspace, q_norm_w=None, k_norm_w=None, dq_norm_w=None,
              dk_norm_w=None, attn_o=None, stream=None):
@@ -149,7 +167,8 @@ def attn_bwd(shape: Shape, x, Wq, Wk, Wv, Wo, dout, lse, dx, dWq, dWk, dWv, dWo,
 class KernelTimer:
     """Times every launch of one library kernel with CUDA events while the
     context is open: 0 attention forward, 1 attention backward, 2 Wo-slice
-    accumulate on all SMs, 3 q/k RoPE/RMSNorm backward, 4 dV hi/lo split."""
+    accumulate on all SMs, 3 q/k RoPE/RMSNorm backward, 4 dV hi/lo split,
+    5 attention forward with the fused Wo-slice accumulate."""
 
     def __init__(self, kernel: int, capacity: int):
         self.kernel = kernel

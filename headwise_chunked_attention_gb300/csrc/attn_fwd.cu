@@ -45,6 +45,17 @@
 // O row out of TMEM into an fp32 row in global memory (IEEE adds, rescaled to
 // the current row max) and the next PV MMA restarts the TMEM accumulator.  The
 // rows live in a per-SM slot (one CTA per SM), so the scratch is bounded.
+//
+// Fused Wo-slice accumulate (FUSE): instead of storing o, the CTA adds its
+// rows' partial result out[rows] += o_h Wo[:, h*d:(h+1)*d]^T itself (the
+// chunk's "store the partial result", memeeeeeex.com "Untied Ulysses (UPipe)",
+// without an O buffer).  After the attention loop the softmax warps write o
+// (bf16) over their Q tile in shared memory, the K/V ring is reused for two
+// 128-row tiles of the head's Wo slice and for fp32 staging, and for each
+// 128-column block n of out the MMA warp computes the two 128 x 128 products
+// into TMEM (double-buffered: S_t for even n, O_t's columns for odd n) while
+// the softmax warps stage the previous block and add it into out with TMA
+// reduce-adds (the read-modify-write runs in L2).
 #include <algorithm>
 
 #include "internal.h"
@@ -66,26 +77,39 @@ constexpr float kPShift = 8.0f;       // P is stored as p * 2^kPShift (see above
 // shifted row sum of one tile's p that asks for a new max (128 * 2^kPShift)
 constexpr float kSumLimit = 128.0f * 256.0f;
 
-template <int D>
+constexpr int kStgBufs = 2;                    // fp32 staging buffers per softmax warp (FUSE)
+constexpr uint32_t kStgBytes = 32 * 32 * 4;    // [32 rows][32 cols] fp32, 128-byte swizzled
+
+template <int D, bool FUSE>
 struct FwdCfg {
   static constexpr uint32_t TILE_BYTES = 128 * D * 2;     // one Q, K or V tile
   static constexpr uint32_t BLOCK_BYTES = 128 * 64 * 2;   // one 64-column swizzled block
   static constexpr uint32_t Q_OFF = 0;
   static constexpr uint32_t SLOT_OFF = 2 * TILE_BYTES;
-  static constexpr uint32_t BAR_OFF = SLOT_OFF + kSlots * TILE_BYTES;
+  static constexpr uint32_t RING_END = SLOT_OFF + kSlots * TILE_BYTES;
+  // FUSE, after the attention loop: two Wo tiles [128 outputs][D] over the
+  // first two ring slots, then the softmax warps' staging buffers
+  static constexpr uint32_t WO_OFF = SLOT_OFF;
+  static constexpr uint32_t STG_OFF = SLOT_OFF + 2 * TILE_BYTES;
+  static constexpr uint32_t STG_END = STG_OFF + 8 * kStgBufs * kStgBytes;
+  static constexpr uint32_t BAR_OFF = (FUSE && STG_END > RING_END) ? STG_END : RING_END;
   static constexpr uint32_t SMEM_BYTES = BAR_OFF + 256 + 1024;
   static constexpr uint32_t O_COL = 256;  // O_t at TMEM column O_COL + t * D
+  static_assert(WO_OFF % 1024 == 0 && STG_OFF % 1024 == 0, "swizzled tiles need 1 KB alignment");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per block");
 };
 
 }  // namespace
 
-template <int D>
+template <int D, bool FUSE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
                     const __grid_constant__ CUtensorMap kmap,
-                    const __grid_constant__ CUtensorMap vmap, const AttnFwdArgs a,
+                    const __grid_constant__ CUtensorMap vmap,
+                    const __grid_constant__ CUtensorMap womap,
+                    const __grid_constant__ CUtensorMap outmap, const AttnFwdArgs a,
                     int* __restrict__ err) {
-  using Cfg = FwdCfg<D>;
+  using Cfg = FwdCfg<D, FUSE>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -97,7 +121,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = s_full + 2;              // [2]
   uint64_t* o_done = p_full + 2;              // [2]
   uint64_t* drain_bar = o_done + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  // FUSE: o of both tiles in shared memory (8 softmax warps); Wo tiles
+  // loaded / consumed; product block in TMEM / read out (8 softmax warps)
+  uint64_t* o_stored = drain_bar + 1;
+  uint64_t* wo_full = o_stored + 1;           // [2]
+  uint64_t* wo_empty = wo_full + 2;           // [2]
+  uint64_t* acc_full = wo_empty + 2;          // [2]
+  uint64_t* acc_empty = acc_full + 2;         // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -125,6 +156,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&o_done[t], 1);
     }
     mbar_init(drain_bar, 1);
+    mbar_init(o_stored, 8);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&wo_full[b], 1);
+      mbar_init(&wo_empty[b], 1);
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 8);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -132,6 +170,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&qmap);
     prefetch_tmap(&kmap);
     prefetch_tmap(&vmap);
+    if constexpr (FUSE) {
+      prefetch_tmap(&womap);
+      prefetch_tmap(&outmap);
+    }
   }
   if (warp == 8) {
     tmem_alloc(tmem_slot, 512);
@@ -166,10 +208,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         issued |= 1u << slot;
         issued_phase = (issued_phase & ~(1u << slot)) | (ph << slot);
       }
+      uint32_t wo_issued = 0, wo_phase = 0;
+      if constexpr (FUSE) {
+        // the ring is free once both tiles' o is in shared memory (that
+        // follows the last PV MMA, which read the last V tile)
+        if (!*abort_flag && mbar_wait(o_stored, 0, err, abort_flag)) {
+          const int wcol = (a.h0 + head) * D;
+          for (int n = 0; n < a.wo_tiles; ++n) {
+            const int b = n & 1;
+            const uint32_t ph = (n >> 1) & 1;
+            if (!mbar_wait(&wo_empty[b], ph ^ 1, err, abort_flag)) break;
+            mbar_expect_tx(&wo_full[b], Cfg::TILE_BYTES);
+            uint8_t* dst = smem + Cfg::WO_OFF + b * Cfg::TILE_BYTES;
+            for (int k = 0; k < D / 64; ++k)
+              tma_load_2d(dst + k * Cfg::BLOCK_BYTES, &womap, &wo_full[b], wcol + 64 * k, 128 * n);
+            wo_issued |= 1u << b;
+            wo_phase = (wo_phase & ~(1u << b)) | (ph << b);
+          }
+        }
+      }
       if (*abort_flag) {
         mbar_wait_drain(q_full, 0);
         for (int s = 0; s < kSlots; ++s)
           if (issued & (1u << s)) mbar_wait_drain(&slot_full[s], (issued_phase >> s) & 1u);
+        for (int b = 0; b < 2; ++b)
+          if (wo_issued & (1u << b)) mbar_wait_drain(&wo_full[b], (wo_phase >> b) & 1u);
       }
     }
   } else if (warp == 8) {
@@ -228,6 +291,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit_w(&s_full[t]);
             if (t == 1) mma_commit_w(&slot_empty[kidx % kSlots]);
           }
+        }
+      }
+      if constexpr (FUSE) {
+        // out block n = o_t Wo_h[128 n : 128 n + 128, :]^T for both tiles,
+        // into S_t (n even) or the columns of O_t (n odd)
+        constexpr uint32_t IDESC_W = idesc_bf16(128, 128, false, false);
+        const uint32_t wo_base = smem_u32(smem + Cfg::WO_OFF);
+        if (ok && !*abort_flag) ok = mbar_wait_warp(o_stored, 0, err, abort_flag);
+        for (int n = 0; n < a.wo_tiles && ok; ++n) {
+          const int b = n & 1;
+          if (!mbar_wait_warp(&wo_full[b], (n >> 1) & 1, err, abort_flag)) break;
+          if (n >= 2 && !mbar_wait_warp(&acc_empty[b], ((n >> 1) - 1) & 1, err, abort_flag)) break;
+          tc_fence_after();
+          const uint32_t w_addr = wo_base + b * Cfg::TILE_BYTES;
+          for (int t = 0; t < 2; ++t) {
+            const uint32_t acc = tmem + (b ? Cfg::O_COL : 0u) + 128 * t;
+            const uint32_t oa = q_base + t * Cfg::TILE_BYTES;
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+              const uint32_t off = (k / 4) * Cfg::BLOCK_BYTES + (k % 4) * 32;
+              mma_ss_w(acc, sdesc_sw128(oa + off, 16, 1024), sdesc_sw128(w_addr + off, 16, 1024),
+                       IDESC_W, k > 0 ? 1u : 0u);
+            }
+          }
+          mma_commit_w(&wo_empty[b]);
+          mma_commit_w(&acc_full[b]);
         }
       }
     }
@@ -372,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float keep = have_acc ? ex2(m_acc - m_run) : 0.f;
       const float* acc_row =
           have_acc ? a.flush + ((size_t)sm_id() * 256 + 128 * t + r) * D : nullptr;
-      bf16* op = a.O + (long long)qpos * a.ldo + head * D;
+      bf16* op = FUSE ? nullptr : a.O + (long long)qpos * a.ldo + head * D;
       const __half* dop = a.dO ? a.dO + (long long)qpos * a.ld_do + head * D : nullptr;
       float dot = 0.f;  // D' = dO' . o over the fp32 o (the backward's recompute)
 #pragma unroll 1
@@ -398,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (live) {
+        if (FUSE || live) {
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
             uint4 w;
@@ -406,7 +495,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             w.y = pack_bf16(__uint_as_float(rr[i + 2]) * inv_l, __uint_as_float(rr[i + 3]) * inv_l);
             w.z = pack_bf16(__uint_as_float(rr[i + 4]) * inv_l, __uint_as_float(rr[i + 5]) * inv_l);
             w.w = pack_bf16(__uint_as_float(rr[i + 6]) * inv_l, __uint_as_float(rr[i + 7]) * inv_l);
-            *reinterpret_cast<uint4*>(op + 32 * c + i) = w;
+            if constexpr (FUSE) {
+              // row r of the tile's K-major, 128-byte swizzled A operand (the
+              // layout TMA gave Q): 16-byte chunk q of a 64-column block at
+              // (q ^ (r & 7))
+              const int col = 32 * c + i;
+              const int q = (col & 63) >> 3;
+              *reinterpret_cast<uint4*>(smem + Cfg::Q_OFF + t * Cfg::TILE_BYTES +
+                                        (col >> 6) * Cfg::BLOCK_BYTES + r * 128 +
+                                        ((q ^ (r & 7)) << 4)) = w;
+            } else {
+              *reinterpret_cast<uint4*>(op + 32 * c + i) = w;
+            }
           }
         }
       }
@@ -414,6 +514,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         a.lse[(long long)head * a.lse_stride + qpos] =
             (m_run - kPShift + __log2f(l_run)) * 0.69314718055994531f;
       if (live && dop) a.D[(long long)head * a.S + qpos] = dot;
+    }
+    if constexpr (FUSE) {
+      // o is in shared memory (for the async proxy) and every TMEM read of
+      // O_t is done: hand both to the MMA warp
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (ok && lane == 0) mbar_arrive(o_stored);
+      // the staging buffers lie over the ring, which the other tile's last
+      // PV MMA may still read until its O is done
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[1 - t], 0, err, abort_flag));
+      uint8_t* stg = smem + Cfg::STG_OFF + warp * kStgBufs * kStgBytes;
+      const int row0 = q0 + 128 * t + 32 * quarter;
+      const bool rows_live = row0 < a.S;   // rows past S: the TMA reduce drops them
+      uint32_t round = 0;
+#pragma unroll 1
+      for (int n = 0; n < a.wo_tiles && ok; ++n) {
+        const int b = n & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[b], (n >> 1) & 1, err, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t acc = tmem + (b ? Cfg::O_COL : 0u) + 128 * t + lane_off;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c, ++round) {
+          // two 16-column loads: a 32-column load here made ptxas spill in
+          // the softmax loop
+          uint32_t lo[16], hi[16];
+          tmem_ld16(acc + 32 * c, lo);
+          tmem_ld16(acc + 32 * c + 16, hi);
+          tmem_ld_wait(lo);
+          tmem_ld_wait(hi);
+          if (c == 3) {  // the block is read out: the MMA warp may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[b]);
+          }
+          if (rows_live) {
+            uint8_t* buf = stg + (round % kStgBufs) * kStgBytes;
+            if (lane == 0) bulk_wait_read<kStgBufs - 1>();   // buf's previous reduce has read it
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t* v = k < 4 ? lo + 4 * k : hi + 4 * (k - 4);
+              *reinterpret_cast<uint4*>(buf + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+                  make_uint4(v[0], v[1], v[2], v[3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_reduce_add_2d(&outmap, buf, 128 * n + 32 * c, row0);
+              bulk_commit();
+            }
+          }
+        }
+      }
+      if (lane == 0) bulk_wait_all();
+      __syncwarp();
     }
   }
 
@@ -433,27 +590,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool FUSE>
 static cudaError_t launch_fwd_t(const CUtensorMap& qmap, const CUtensorMap& kmap,
-                                const CUtensorMap& vmap, const AttnFwdArgs& a, int* err,
+                                const CUtensorMap& vmap, const CUtensorMap& womap,
+                                const CUtensorMap& outmap, const AttnFwdArgs& a, int* err,
                                 cudaStream_t stream) {
-  using Cfg = FwdCfg<D>;
+  using Cfg = FwdCfg<D, FUSE>;
   static std::atomic<unsigned long long> attr_done{0};
-  const cudaError_t ea = smem_attr_once(attn_fwd_kernel<D>, (int)Cfg::SMEM_BYTES, attr_done);
+  const cudaError_t ea =
+      smem_attr_once(attn_fwd_kernel<D, FUSE>, (int)Cfg::SMEM_BYTES, attr_done);
   if (ea != cudaSuccess) return ea;
   const long long nqb = (a.S + 255) / 256;
   const long long grid = nqb * a.heads;
-  attn_fwd_kernel<D><<<(unsigned)grid, kThreads, Cfg::SMEM_BYTES, stream>>>(qmap, kmap, vmap, a,
-                                                                           err);
+  attn_fwd_kernel<D, FUSE><<<(unsigned)grid, kThreads, Cfg::SMEM_BYTES, stream>>>(
+      qmap, kmap, vmap, womap, outmap, a, err);
   return cudaGetLastError();
 }
 
 cudaError_t launch_attn_fwd(const CUtensorMap& qmap, const CUtensorMap& kmap,
                             const CUtensorMap& vmap, const AttnFwdArgs& a, int d, int* err,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, const CUtensorMap* womap,
+                            const CUtensorMap* outmap) {
   if (a.S <= 0 || a.heads <= 0) return cudaSuccess;
-  if (d == 128) return launch_fwd_t<128>(qmap, kmap, vmap, a, err, stream);
-  if (d == 64) return launch_fwd_t<64>(qmap, kmap, vmap, a, err, stream);
+  const bool fuse = womap != nullptr;
+  if (fuse != (outmap != nullptr) || (fuse && (a.wo_tiles <= 0 || a.O || a.dO)))
+    return cudaErrorInvalidValue;
+  if (fuse) {
+    if (d == 128) return launch_fwd_t<128, true>(qmap, kmap, vmap, *womap, *outmap, a, err, stream);
+    if (d == 64) return launch_fwd_t<64, true>(qmap, kmap, vmap, *womap, *outmap, a, err, stream);
+  } else {
+    // the unused map parameters are passed as copies of the Q map
+    if (d == 128) return launch_fwd_t<128, false>(qmap, kmap, vmap, qmap, qmap, a, err, stream);
+    if (d == 64) return launch_fwd_t<64, false>(qmap, kmap, vmap, qmap, qmap, a, err, stream);
+  }
   return cudaErrorNotSupported;
 }
 

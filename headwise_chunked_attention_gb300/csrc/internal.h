@@ -214,6 +214,9 @@ struct AttnFwdArgs {
   // attention backward forms from the same fp16 V
   const __half* dO; int ld_do;  // [S, ld_do] fp16, head i at column i*d
   float* D;                     // [heads][S]
+  // fused Wo-slice accumulate (launch with womap / outmap; O and dO null):
+  // the hidden / 128 column blocks of out each CTA adds its rows into
+  int wo_tiles;
 };
 
 // The attention forward folds its TMEM O accumulator into an fp32 row in
@@ -222,9 +225,13 @@ struct AttnFwdArgs {
 constexpr int kFlushTiles = 512;
 constexpr int kFlushSlots = 256;
 
+// womap / outmap: nullptr (o is stored to a.O), or both (fused Wo-slice
+// accumulate): womap over Wo [hidden, Hq*d] bf16 with box [128 rows][64
+// cols], outmap over out [S, hidden] fp32 with box [32 rows][32 cols].
 cudaError_t launch_attn_fwd(const CUtensorMap& qmap, const CUtensorMap& kmap,
                             const CUtensorMap& vmap, const AttnFwdArgs& a, int d, int* err,
-                            cudaStream_t stream);
+                            cudaStream_t stream, const CUtensorMap* womap = nullptr,
+                            const CUtensorMap* outmap = nullptr);
 
 struct AttnBwdArgs {
   int S, heads, group, h0, kv0, d;

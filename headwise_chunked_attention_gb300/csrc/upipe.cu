@@ -233,7 +233,9 @@ Layout plan(const Geo& g, int mode) {
   L.q = take(S * ch * d * 2);
   L.k = take(S * kvc * d * 2);
   L.v = take(S * kvc * d * 2);
-  L.o = take(S * ch * d * 2);
+  // mode 3 (the fused forward) adds each chunk's partial result into out
+  // from the attention kernel: no O buffer
+  L.o = mode == 3 ? (size_t)-1 : take(S * ch * d * 2);
   // per-SM fp32 rows into which long attention rows fold their O accumulator
   L.flush = S > (size_t)kFlushTiles * 128 ? take((size_t)kFlushSlots * 256 * d * 4) : (size_t)-1;
   // mode 2: a third chunk buffer, last so that every other offset is mode 0's
@@ -400,10 +402,13 @@ int project_chunk(const Geo& g, const DeviceState* ds, cudaStream_t st, const CU
 
 // dO / D (the backward's recompute): also form D' = dO' . o per row from the
 // kernel's fp32 o (see AttnFwdArgs).
+// womap / outmap (the fused forward): the kernel adds the chunk's partial
+// result into out itself and stores no o (O must be nullptr).
 int attention_chunk(const Geo& g, const DeviceState* ds, cudaStream_t st, const __half* Q,
                     const __half* K, const __half* V, int h0, int kv0, bf16* O, int ldo,
                     float* lse, float* flush, const __half* dO = nullptr, int ld_do = 0,
-                    float* D = nullptr) {
+                    float* D = nullptr, const CUtensorMap* womap = nullptr,
+                    const CUtensorMap* outmap = nullptr) {
   const int d = g.d;
   CUtensorMap qm, km, vm;
   UPIPE_MAP(&qm, Q, g.S, (uint64_t)g.ch * d, (uint64_t)g.ch * d, 128, 64);
@@ -424,9 +429,11 @@ int attention_chunk(const Geo& g, const DeviceState* ds, cudaStream_t st, const 
   a.dO = dO;
   a.ld_do = ld_do;
   a.D = D;
-  prof_begin(0, st);
-  const cudaError_t e = launch_attn_fwd(qm, km, vm, a, d, ds->err, st);
-  prof_end(0, st);
+  a.wo_tiles = womap ? g.hidden / 128 : 0;
+  const int timer = womap ? 5 : 0;
+  prof_begin(timer, st);
+  const cudaError_t e = launch_attn_fwd(qm, km, vm, a, d, ds->err, st, womap, outmap);
+  prof_end(timer, st);
   UPIPE_CUDA(e);
   return UPIPE_OK;
 }
@@ -438,7 +445,7 @@ using namespace upipe;
 
 extern "C" size_t upipe_workspace_bytes(const upipe_shape_t* shape, int mode) {
   Geo g;
-  if (mode < 0 || mode > 2) return 0;
+  if (mode < 0 || mode > 3) return 0;
   if (check_shape(shape, &g) != UPIPE_OK) return 0;
   return plan(g, mode).total;
 }
@@ -625,6 +632,63 @@ extern "C" int upipe_attn_fwd(const upipe_shape_t* shape, const upipe_bf16* x,
                               upipe_bf16* attn_o, void* stream) {
   return attn_fwd_impl(shape, x, Wq, Wk, Wv, Wo, q_norm_w, k_norm_w, out, lse, workspace,
                        ws_bytes, attn_o, stream, true);
+}
+
+// Forward with the Wo-slice accumulate fused into the attention kernel.  One
+// Q buffer serves every chunk: the projection of chunk c + 1 follows chunk
+// c's attention on the same stream.  out starts from zero (the chunks' CTAs
+// add into it in no fixed order).
+extern "C" int upipe_attn_fwd_fused(const upipe_shape_t* shape, const upipe_bf16* x_,
+                                    const upipe_bf16* Wq_, const upipe_bf16* Wk_,
+                                    const upipe_bf16* Wv_, const upipe_bf16* Wo_,
+                                    const float* q_norm_w, const float* k_norm_w, float* out,
+                                    float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  Geo g;
+  UPIPE_TRY(check_shape(shape, &g));
+  NvtxRange call_range("upipe_attn_fwd_fused");
+  const bf16* x = reinterpret_cast<const bf16*>(x_);
+  const bf16* Wq = reinterpret_cast<const bf16*>(Wq_);
+  const bf16* Wk = reinterpret_cast<const bf16*>(Wk_);
+  const bf16* Wv = reinterpret_cast<const bf16*>(Wv_);
+  const bf16* Wo = reinterpret_cast<const bf16*>(Wo_);
+  if (!x || !Wq || !Wk || !Wv || !Wo || !out || !lse || !workspace) return UPIPE_ERR_INVALID_ARG;
+  for (const void* p : {(const void*)x, (const void*)Wq, (const void*)Wk, (const void*)Wv,
+                        (const void*)Wo, (const void*)out, (const void*)lse,
+                        (const void*)q_norm_w, (const void*)k_norm_w})
+    if (p && !aligned16(p)) return UPIPE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return UPIPE_ERR_INVALID_ARG;
+  const Layout L = plan(g, 3);
+  if (ws_bytes < L.total) return UPIPE_ERR_WORKSPACE_TOO_SMALL;
+  DeviceState* ds = nullptr;
+  UPIPE_TRY(device_state(&ds));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  float2* rhi = at<float2>(workspace, L.rope_hi);
+  float2* rlo = at<float2>(workspace, L.rope_lo);
+  float2* rlo_t = at<float2>(workspace, L.rope_lo_t);
+  __half* Q = at<__half>(workspace, L.q);
+  __half* K = at<__half>(workspace, L.k);
+  __half* V = at<__half>(workspace, L.v);
+  float* flush = L.flush == (size_t)-1 ? nullptr : at<float>(workspace, L.flush);
+  UPIPE_CUDA(launch_rope_table(rhi, rlo, rlo_t, g.S, g.d, shape->rope_theta, st));
+
+  CUtensorMap xmap, outmap, womap;
+  UPIPE_MAP(&xmap, x, g.S, g.hidden, g.hidden, 128, 64);
+  if (!make_tmap_f32(&outmap, out, g.S, g.hidden, g.hidden, 32, 32)) return UPIPE_ERR_CUDA;
+  UPIPE_MAP(&womap, Wo, g.hidden, (uint64_t)g.Hq * g.d, (uint64_t)g.Hq * g.d, 128, 64);
+  UPIPE_CUDA(cudaMemsetAsync(out, 0, (size_t)g.S * g.hidden * sizeof(float), st));
+  for (int c = 0; c < g.nchunks; ++c) {
+    NvtxRange chunk_range("upipe_attn_fwd_fused", c);
+    const int h0 = c * g.ch;
+    const int kv0 = h0 / g.g;
+    const bool new_group = (g.ch >= g.g) || (h0 % g.g == 0);
+    UPIPE_TRY(project_chunk(g, ds, st, xmap, Wq, Wk, Wv, q_norm_w, k_norm_w, shape->norm_eps, h0,
+                            kv0, new_group, Q, K, V, rhi, rlo_t, nullptr, nullptr, nullptr,
+                            nullptr));
+    UPIPE_TRY(attention_chunk(g, ds, st, Q, K, V, h0, kv0, nullptr, 0, lse + (size_t)h0 * g.S,
+                              flush, nullptr, 0, nullptr, &womap, &outmap));
+  }
+  return UPIPE_OK;
 }
 
 namespace upipe {

@@ -96,7 +96,8 @@ enum {
  * (mode 1) for this shape, or 0 if the shape is invalid.  Pure host function.
  * Mode 2 is mode 0 plus a third chunk buffer (S * chunk_heads * d bf16): given
  * that much, upipe_attn_fwd adds two chunks' partial results into out per
- * pass (see there).
+ * pass (see there).  Mode 3 is upipe_attn_fwd_fused's: mode 0 without the
+ * second chunk buffer (S * chunk_heads * d bf16 less).
  * The bytes are affine in chunk_heads: the per-chunk Q/O (and backward) parts
  * scale with chunk_heads, the K/V part is one KV group (or chunk_heads/(Hq/Hkv)
  * groups when a chunk spans several), plus RoPE tables of
@@ -126,6 +127,26 @@ int upipe_attn_fwd(const upipe_shape_t* shape, const upipe_bf16* x, const upipe_
                    const upipe_bf16* Wk, const upipe_bf16* Wv, const upipe_bf16* Wo,
                    const float* q_norm_w, const float* k_norm_w, float* out, float* lse,
                    void* workspace, size_t ws_bytes, upipe_bf16* attn_o, void* stream);
+
+/* Forward of the layer with each chunk's partial result added into out by the
+ * attention kernel itself (memeeeeeex.com, "Untied Ulysses (UPipe)": each
+ * chunk stores its partial result; here without an attention-output buffer).
+ * Same arguments and results as upipe_attn_fwd without attn_o:
+ *   out   [S, hidden] fp32, overwritten: zeroed on ``stream``, then every
+ *         head's o_h Wo[:, h*d:(h+1)*d]^T is added by the CTAs that computed
+ *         o_h (fp32 adds in L2, in no fixed order: out matches
+ *         upipe_attn_fwd's to fp32 rounding, ~1e-6 relative, and may differ
+ *         in its last bits between runs)
+ *   lse   [Hq, S] fp32, bit-identical to upipe_attn_fwd's
+ *   workspace / ws_bytes: at least upipe_workspace_bytes(shape, 3) bytes,
+ *         256-byte aligned (no O buffer: one chunk's Q, the K/V of its group
+ *         and the RoPE tables)
+ * Every launch runs on ``stream`` (no side stream, no events).
+ * Returns UPIPE_OK or an error code (nothing launched on error). */
+int upipe_attn_fwd_fused(const upipe_shape_t* shape, const upipe_bf16* x, const upipe_bf16* Wq,
+                         const upipe_bf16* Wk, const upipe_bf16* Wv, const upipe_bf16* Wo,
+                         const float* q_norm_w, const float* k_norm_w, float* out, float* lse,
+                         void* workspace, size_t ws_bytes, void* stream);
 
 /* Backward of the layer for L = sum(out * dout), chunk by chunk, recomputing
  * each chunk's Q/K/V and attention output in the reused workspace (activation
@@ -204,6 +225,8 @@ int upipe_attn_fwd_noalloc(const upipe_shape_t* shape, const upipe_bf16* x, cons
  *   kernel 3: the RoPE/RMSNorm backward of dQ (one per chunk) and of dK
  *             (one per KV group), in launch order
  *   kernel 4: the fp32 -> bf16 hi/lo split of dV (one per KV group)
+ *   kernel 5: the attention forward kernel of upipe_attn_fwd_fused (with its
+ *             fused Wo-slice accumulate)
  *   start_events/end_events: caller-created cudaEvent_t handles (timing
  *   enabled), owned by the caller.  capacity 0 detaches.
  * upipe_profile_count() returns how many launches were recorded since the

@@ -64,6 +64,9 @@ def test_workspace_closed_form(u):
             assert ws(u, w, ch, 1) == expect + bwd, (w.name, ch)
             # mode 2: the forward's third chunk buffer for paired accumulates
             assert ws(u, w, ch, 2) == expect + al(S * ch * d * 2), (w.name, ch)
+            # mode 3: the fused forward keeps no attention output, so one
+            # chunk buffer (Q) instead of two
+            assert ws(u, w, ch, 3) == expect - al(S * ch * d * 2), (w.name, ch)
 
 
 def test_workspace_affine_in_chunk_heads_and_golden_reduction(u):
@@ -88,6 +91,7 @@ def test_invalid_shapes_give_zero_workspace(u):
         assert ws(u, w, 2, **kw) == 0, kw
     assert ws(u, w, 3) == 0                   # 3 does not divide Hq = 4
     assert u.workspace_bytes(u.Shape.of(w, 2), 7) == 0
+    assert u.workspace_bytes(u.Shape.of(w, 2), 4) == 0
 
 
 def _fwd(u, shape, ptrs=None, ws_bytes=1 << 40, dbg=None):
@@ -152,3 +156,30 @@ def test_guard_margins_catch_writes_outside_the_buffer():
         h.raw[h.off + h.nbytes if edge == "after" else h.off - 1] = 0
         with pytest.raises(AssertionError):
             h.check(edge)
+
+
+def test_fused_forward_validates_before_any_launch(u):
+    # upipe_attn_fwd_fused checks the shape, every pointer and the mode-3
+    # workspace size on the host and launches nothing when one fails
+    L = u.lib()
+    w = WORKLOADS["tiny-s2048"]
+    sh = u.Shape.of(w, 2)
+    need = u.workspace_bytes(sh, 3)
+    assert 0 < need < u.workspace_bytes(sh, 0)
+    p = [0x100000 + 0x1000 * i for i in range(10)]
+    call = lambda shape, ptrs, nbytes: L.upipe_attn_fwd_fused(
+        ctypes.byref(shape) if shape is not None else None, *ptrs[:5], None, None,
+        ptrs[5], ptrs[6], ptrs[7], nbytes, None)
+    assert call(None, p, need) == 1                         # NULL shape
+    assert call(u.Shape.of(w, 3), p, need) == 1             # 3 does not divide Hq
+    assert call(u.Shape.of(w.with_(d=96), 2), p, need) == 2
+    q = list(p)
+    q[5] = 0
+    assert call(sh, q, need) == 1                           # NULL out
+    q = list(p)
+    q[6] += 4
+    assert call(sh, q, need) == 1                           # misaligned lse
+    q = list(p)
+    q[7] += 16
+    assert call(sh, q, need) == 1                           # workspace not 256-byte aligned
+    assert call(sh, p, need - 1) == 3                       # workspace too small
