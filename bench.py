@@ -26,6 +26,11 @@ GPU): ``value`` is the sum of all ranks' FLOPs over the max-over-ranks time.
 ``--impl reference`` times the float64 CPU oracle (the only reference this
 method has) on a bounded sample of the same workload.
 
+``fused_wo_forward`` (main and secondary workload; ``--no-fused`` skips it)
+times the forward whose attention kernel adds the Wo-slice partial results
+into out itself (upipe_attn_fwd_fused, no attention-output buffer) against
+upipe_attn_fwd, with the workspace each needs.
+
 Besides the layer number the line carries ``roofline`` (the dominant
 attention kernel: algorithmic FLOPs per launch over its live CUDA-event launch
 time) and ``hbm_kernels`` (the HBM-bound kernels: algorithmic bytes per layer
@@ -332,10 +337,11 @@ def gpu_uuid(dev):
 
 
 def measure(u, w, ch, mode, steps, warmup, dist, world, rank, dev, full=True, sweep_on=True,
-            cpu_on=True):
+            cpu_on=True, fused_on=True):
     """Everything one JSON line reports for workload ``w`` at ``ch`` heads per
     chunk (mode 0 forward, 1 forward + backward).  ``full``: also e2e, the
-    HBM-bound kernels, the saved-O backward and the CPU baseline."""
+    HBM-bound kernels, the saved-O backward and the CPU baseline.
+    ``fused_on``: also the forward with the fused Wo-slice accumulate."""
     import torch
     from workloads import make_inputs
 
@@ -577,6 +583,48 @@ def measure(u, w, ch, mode, steps, warmup, dist, world, rank, dev, full=True, sw
                                  "chunks, halving the fp32 read-modify-write passes over out"}
         del ws2
 
+    # ---- the fused forward (upipe_attn_fwd_fused): the attention kernel adds
+    # each head's Wo-slice partial result into out itself, so the workspace
+    # holds no attention output.  Timed against upipe_attn_fwd, each with its
+    # smallest workspace (modes 3 and 0), in alternating passes
+    if fused_on:
+        fwd_flops = layer_flops(w, "fwd")[0]
+        wsb = {"separate": u.workspace_bytes(shape, 0), "fused": u.workspace_bytes(shape, 3)}
+        wsf = {nm: torch.empty(b, dtype=torch.uint8, device=dev) for nm, b in wsb.items()}
+
+        def fwd_of(nm):
+            call = u.attn_fwd_fused if nm == "fused" else u.attn_fwd
+            return lambda: call(shape, inp["x"], inp["Wq"], inp["Wk"], inp["Wv"], inp["Wo"],
+                                out, lse, wsf[nm], inp.get("q_gamma"), inp.get("k_gamma"))
+
+        fns = {nm: fwd_of(nm) for nm in wsb}
+        for fn in fns.values():
+            fn()
+        if u.last_error() != 0:
+            raise RuntimeError("device error in the fused forward comparison")
+        k = max(2, int(2.0 / timed(fns["fused"], 1)))
+        rates = {nm: [] for nm in fns}
+        for order in (("separate", "fused"), ("fused", "separate")):
+            for nm in order:
+                rates[nm].append(fwd_flops * k / timed(fns[nm], k) / 1e12)
+        launch_ms = {}
+        for nm, kid in (("separate", 0), ("fused", 5)):
+            kt = u.KernelTimer(kid, nchunks)
+            with kt:
+                fns[nm]()
+            launch_ms[nm] = round(sum(kt.durations_ms()), 3)
+        res["fused"] = {
+            "chunk_heads": ch, "steps": k,
+            "forward_tflops": {nm: round(sum(r) / len(r), 2) for nm, r in rates.items()},
+            "forward_tflops_passes": {nm: [round(x, 2) for x in r] for nm, r in rates.items()},
+            "workspace_gb": {nm: round(b / 1e9, 4) for nm, b in wsb.items()},
+            "attention_kernel_ms_per_forward": launch_ms,
+            "note": "upipe_attn_fwd_fused: the attention kernel adds o_h Wo_h^T into out (fp32 "
+                    "TMA reduce-adds at the end of each CTA), no O buffer; 'separate' is "
+                    "upipe_attn_fwd (Wo-slice GEMM per chunk, overlapped on a side stream). "
+                    "The fused kernel's time includes the Wo work"}
+        del wsf
+
     # ---- the saved-O backward: the forward keeps every head's attention
     # output and the backward reuses it instead of recomputing the attention
     if mode and full:
@@ -678,6 +726,8 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-fused", action="store_true",
+                    help="skip the fused Wo-slice forward comparison")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the end-to-end and HBM-kernel measurements (profiling runs)")
     ap.add_argument("--seq-len", type=int, default=None,
@@ -716,18 +766,19 @@ def main():
     dev = torch.device("cuda", local)
     mode = 1 if args.pass_ == "fwdbwd" else 0
     r = measure(u, w, ch, mode, args.steps, args.warmup, dist, world, rank, dev,
-                full=not args.no_e2e, sweep_on=not args.no_sweep, cpu_on=not args.no_cpu)
+                full=not args.no_e2e, sweep_on=not args.no_sweep, cpu_on=not args.no_cpu,
+                fused_on=not args.no_fused)
     secondary = None
     if not args.no_secondary and args.workload != SECONDARY_WORKLOAD:
         w2 = WORKLOADS[SECONDARY_WORKLOAD]
         r2 = measure(u, w2, w2.chunk_heads[0], 0, args.steps, 3, dist, world, rank, dev,
-                     full=False)
+                     full=False, fused_on=not args.no_fused)
         secondary = {"config": config_of(w2, w2.chunk_heads[0], "fwd"),
                      "value": round(r2["value"], 2), "unit": "TFLOP/s",
                      "ms_per_step": round(1e3 * r2["t"] / args.steps, 3),
                      "steps": args.steps, "roofline_attn_fwd": r2["roof_fwd"],
                      "chunk_sweep": r2["sweep"], "paired_accumulate": r2.get("paired"),
-                     "clocks": r2["clocks"]}
+                     "fused_wo_forward": r2.get("fused"), "clocks": r2["clocks"]}
 
     if rank != 0:
         if dist is not None:
@@ -755,6 +806,7 @@ def main():
         "chunk_sweep": r["sweep"],
         "saved_o_backward": r.get("saved_o"),
         "paired_accumulate": r.get("paired"),
+        "fused_wo_forward": r.get("fused"),
         "roofline": r["roof_bwd"] if r["roof_bwd"] else r["roof_fwd"],
         "roofline_attn_fwd": r["roof_fwd"],
         "roofline_attn_bwd": r["roof_bwd"],

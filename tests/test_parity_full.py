@@ -2,7 +2,9 @@
 configurations the benchmark times, against the plain float64 oracle.
 
 A million-token layer is beyond the oracle, so the forward is checked on a
-seeded sample of 256 query rows per head (the same rows for every head).  The
+seeded sample of 256 query rows per head (the same rows for every head), and
+so is the forward with the fused Wo-slice accumulate in the benchmark's chunk
+size (its lse bit-identical to the separate forward's).  The
 backward is checked on complete dx rows: with the upstream gradient set to
 zero after row T, causality makes dx of the rows up to T depend only on the
 prefix [0, T] of the sequence, which the oracle's tail backward covers (the
@@ -42,6 +44,18 @@ def _gpu_fwd(u, w, ch, t):
     return out, lse, o
 
 
+def _gpu_fwd_fused(u, w, ch, t):
+    sh = u.Shape.of(w, ch)
+    out = torch.empty(w.S, w.hidden, device="cuda")
+    lse = torch.empty(w.Hq, w.S, device="cuda")
+    ws = torch.empty(u.workspace_bytes(sh, 3), dtype=torch.uint8, device="cuda")
+    u.attn_fwd_fused(sh, t["x"], t["Wq"], t["Wk"], t["Wv"], t["Wo"], out, lse, ws,
+                     t.get("q_gamma"), t.get("k_gamma"))
+    torch.cuda.synchronize()
+    assert u.last_error() == 0
+    return out, lse
+
+
 @pytest.mark.parametrize("name", ["llama3.2-3b-s65536", "llama3-8b-rank-s1m",
                                   "llama3-8b-rank-s5m", "qwen3-32b-rank-s1m"])
 def test_forward_sampled_rows_at_full_size(name):
@@ -56,6 +70,13 @@ def test_forward_sampled_rows_at_full_size(name):
                    f64(o[rows]).reshape(len(rows), w.Hq, w.d).transpose(1, 0, 2))
         del out, lse, o
         torch.cuda.empty_cache()
+    # the fused forward (Wo-slice accumulate inside the attention kernel) in
+    # the benchmark's chunk size
+    ch0 = w.chunk_heads[0]
+    out, lse = _gpu_fwd_fused(u, w, ch0, t)
+    fused = (f64(out[rows]), f64(lse[:, rows]))
+    del out, lse
+    torch.cuda.empty_cache()
     xg = t["x"]
     a = {k: f64(v) for k, v in t.items() if k != "x"}
     ref = O.layer_forward(w, lambda lo, hi: f64(xg[lo:hi]), a["Wq"], a["Wk"], a["Wv"],
@@ -65,6 +86,8 @@ def test_forward_sampled_rows_at_full_size(name):
         assert_close(o, ref["o"], f"{name} attention output ch={ch}")
         dl = np.abs(lse - ref["lse"]).max()
         assert dl <= LSE_ABS, f"{name} lse ch={ch}: {dl:.2e}"
+    assert_close(fused[0], ref["out"], f"{name} fused out ch={ch0}")
+    assert np.array_equal(fused[1], got[ch0][1]), f"{name} fused lse ch={ch0}"
     # the per-head attention output does not depend on the chunk size
     first = got[w.chunk_heads[0]][2]
     for ch in w.chunk_heads[1:]:
