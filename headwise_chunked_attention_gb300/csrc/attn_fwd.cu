@@ -47,9 +47,9 @@
 // rows live in a per-SM slot (one CTA per SM), so the scratch is bounded.
 //
 // Fused Wo-slice accumulate (FUSE): instead of storing o, the CTA adds its
-// rows' partial result out[rows] += o_h Wo[:, h*d:(h+1)*d]^T itself (the
-// chunk's "store the partial result", memeeeeeex.com "Untied Ulysses (UPipe)",
-// without an O buffer).  After the attention loop the softmax warps write o
+// rows' partial result out[rows] += o_h Wo[:, h*d:(h+1)*d]^T itself (each
+// chunk keeps its heads' contribution to the layer output, memeeeeeex.com
+// "Untied Ulysses (UPipe)", here without an attention-output buffer).  After the attention loop the softmax warps write o
 // (bf16) over their Q tile in shared memory, the K/V ring is reused for two
 // 128-row tiles of the head's Wo slice and for fp32 staging, and for each
 // 128-column block n of out the MMA warp computes the two 128 x 128 products
