@@ -39,6 +39,9 @@
 // The diagonal KV tile of each query tile is the only one masked; KV tiles
 // beyond it are never loaded (causal skipping).
 // Grid: heaviest query blocks first, all heads of a block together.
+// Known LSE (the backward's recompute): with the forward's LSE of each row the
+// kernel takes p = 2^(s * scale_log2 - lse_2 + kPShift) directly, p <= 2^8, so
+// it skips the row sum and the max test and O needs no division by l.
 // Long rows: the tensor core's fp32 accumulation of O drifts over hundreds of
 // thousands of MMA steps (measured: the error grows linearly with position
 // past ~1M keys), so every kFlushTiles KV tiles each softmax thread folds its
@@ -80,6 +83,13 @@ constexpr float kSumLimit = 128.0f * 256.0f;
 constexpr int kStgBufs = 2;                    // fp32 staging buffers per softmax warp (FUSE)
 constexpr uint32_t kStgBytes = 32 * 32 * 4;    // [32 rows][32 cols] fp32, 128-byte swizzled
 
+// Kernel modes: o stored to a.O (the forward, and the backward's recompute
+// without a known LSE); the fused Wo-slice accumulate; the backward's
+// recompute with the forward's LSE given.
+constexpr int kModeStore = 0;
+constexpr int kModeFused = 1;
+constexpr int kModeKnownLse = 2;
+
 template <int D, bool FUSE>
 struct FwdCfg {
   static constexpr uint32_t TILE_BYTES = 128 * D * 2;     // one Q, K or V tile
@@ -101,7 +111,7 @@ struct FwdCfg {
 
 }  // namespace
 
-template <int D, bool FUSE>
+template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
                     const __grid_constant__ CUtensorMap kmap,
@@ -109,6 +119,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap womap,
                     const __grid_constant__ CUtensorMap outmap, const AttnFwdArgs a,
                     int* __restrict__ err) {
+  constexpr bool FUSE = MODE == kModeFused;
+  constexpr bool KNOWN = MODE == kModeKnownLse;
   using Cfg = FwdCfg<D, FUSE>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -335,6 +347,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = a.scale_log2;
     float m_run = -INFINITY;
     float l_run = 0.f;
+    if constexpr (KNOWN) {
+      // the row's max is replaced by its log-sum-exp (base 2, scaled): every
+      // p is then final, p * 2^kPShift <= 2^kPShift, and no tile changes it
+      // (rows past S take 0: their values are never stored)
+      m_run = qpos < a.S ? a.lse_in[(long long)head * a.lse_stride + qpos] * 1.4426950408889634f
+                         : 0.f;
+    }
     float m_acc = -INFINITY;  // row max of the folded part of O (-inf: nothing folded)
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
@@ -381,6 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return (s01.x + s23.x) + (s01.y + s23.y);
       };
       float l_tile = p_tile(m_run);
+      if constexpr (!KNOWN) {
       // Every p <= 1 while m_run is the row's max, so a row sum above
       // kSumLimit (or inf / NaN: the first tile, m_run = -inf) means the
       // max has grown.  Only then is the row max taken; O and l are rescaled
@@ -421,6 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         l_tile = p_tile(m_run);
       }
       l_run += l_tile;
+      }
       if (folding && j > 0 && j % kFlushTiles == 0) {
         // O in TMEM holds PV(0 .. j-1) since the last fold, in units of m_run
         const bool have_acc = m_acc != -INFINITY;
@@ -455,7 +476,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[t], 0, err, abort_flag));
     if (ok) {
       tc_fence_after();
-      const float inv_l = 1.f / l_run;
+      // with the known LSE, sum_j p_j = 1: O carries just the 2^kPShift factor
+      const float inv_l = KNOWN ? 1.f / (float)(1 << (int)kPShift) : 1.f / l_run;
       const bool live = qpos < a.S;
       const bool have_acc = m_acc != -INFINITY;
       const float keep = have_acc ? ex2(m_acc - m_run) : 0.f;
@@ -590,21 +612,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool FUSE>
+template <int D, int MODE>
 static cudaError_t launch_fwd_t(const CUtensorMap& qmap, const CUtensorMap& kmap,
                                 const CUtensorMap& vmap, const CUtensorMap& womap,
                                 const CUtensorMap& outmap, const AttnFwdArgs& a, int* err,
                                 cudaStream_t stream) {
-  using Cfg = FwdCfg<D, FUSE>;
+  using Cfg = FwdCfg<D, MODE == kModeFused>;
   static std::atomic<unsigned long long> attr_done{0};
   const cudaError_t ea =
-      smem_attr_once(attn_fwd_kernel<D, FUSE>, (int)Cfg::SMEM_BYTES, attr_done);
+      smem_attr_once(attn_fwd_kernel<D, MODE>, (int)Cfg::SMEM_BYTES, attr_done);
   if (ea != cudaSuccess) return ea;
   const long long nqb = (a.S + 255) / 256;
   const long long grid = nqb * a.heads;
-  attn_fwd_kernel<D, FUSE><<<(unsigned)grid, kThreads, Cfg::SMEM_BYTES, stream>>>(
+  attn_fwd_kernel<D, MODE><<<(unsigned)grid, kThreads, Cfg::SMEM_BYTES, stream>>>(
       qmap, kmap, vmap, womap, outmap, a, err);
   return cudaGetLastError();
+}
+
+template <int MODE>
+static cudaError_t launch_fwd_d(int d, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                                const CUtensorMap& vmap, const CUtensorMap& womap,
+                                const CUtensorMap& outmap, const AttnFwdArgs& a, int* err,
+                                cudaStream_t stream) {
+  if (d == 128) return launch_fwd_t<128, MODE>(qmap, kmap, vmap, womap, outmap, a, err, stream);
+  if (d == 64) return launch_fwd_t<64, MODE>(qmap, kmap, vmap, womap, outmap, a, err, stream);
+  return cudaErrorNotSupported;
 }
 
 cudaError_t launch_attn_fwd(const CUtensorMap& qmap, const CUtensorMap& kmap,
@@ -613,17 +645,15 @@ cudaError_t launch_attn_fwd(const CUtensorMap& qmap, const CUtensorMap& kmap,
                             const CUtensorMap* outmap) {
   if (a.S <= 0 || a.heads <= 0) return cudaSuccess;
   const bool fuse = womap != nullptr;
-  if (fuse != (outmap != nullptr) || (fuse && (a.wo_tiles <= 0 || a.O || a.dO)))
+  if (fuse != (outmap != nullptr) || (fuse && (a.wo_tiles <= 0 || a.O || a.dO || a.lse_in)))
     return cudaErrorInvalidValue;
-  if (fuse) {
-    if (d == 128) return launch_fwd_t<128, true>(qmap, kmap, vmap, *womap, *outmap, a, err, stream);
-    if (d == 64) return launch_fwd_t<64, true>(qmap, kmap, vmap, *womap, *outmap, a, err, stream);
-  } else {
-    // the unused map parameters are passed as copies of the Q map
-    if (d == 128) return launch_fwd_t<128, false>(qmap, kmap, vmap, qmap, qmap, a, err, stream);
-    if (d == 64) return launch_fwd_t<64, false>(qmap, kmap, vmap, qmap, qmap, a, err, stream);
+  if (fuse) return launch_fwd_d<kModeFused>(d, qmap, kmap, vmap, *womap, *outmap, a, err, stream);
+  // the unused map parameters are passed as copies of the Q map
+  if (a.lse_in) {
+    if (a.lse) return cudaErrorInvalidValue;   // the LSE is an input here
+    return launch_fwd_d<kModeKnownLse>(d, qmap, kmap, vmap, qmap, qmap, a, err, stream);
   }
-  return cudaErrorNotSupported;
+  return launch_fwd_d<kModeStore>(d, qmap, kmap, vmap, qmap, qmap, a, err, stream);
 }
 
 }  // namespace upipe

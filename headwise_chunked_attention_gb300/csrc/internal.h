@@ -217,6 +217,10 @@ struct AttnFwdArgs {
   // fused Wo-slice accumulate (launch with womap / outmap; O and dO null):
   // the hidden / 128 column blocks of out each CTA adds its rows into
   int wo_tiles;
+  // nullptr, or the forward's LSE of these heads ([heads][lse_stride],
+  // natural log; then lse must be nullptr): the backward's recompute takes
+  // p = exp(s - lse) directly instead of the online softmax
+  const float* lse_in;
 };
 
 // The attention forward folds its TMEM O accumulator into an fp32 row in

@@ -408,7 +408,7 @@ int attention_chunk(const Geo& g, const DeviceState* ds, cudaStream_t st, const 
                     const __half* K, const __half* V, int h0, int kv0, bf16* O, int ldo,
                     float* lse, float* flush, const __half* dO = nullptr, int ld_do = 0,
                     float* D = nullptr, const CUtensorMap* womap = nullptr,
-                    const CUtensorMap* outmap = nullptr) {
+                    const CUtensorMap* outmap = nullptr, const float* lse_in = nullptr) {
   const int d = g.d;
   CUtensorMap qm, km, vm;
   UPIPE_MAP(&qm, Q, g.S, (uint64_t)g.ch * d, (uint64_t)g.ch * d, 128, 64);
@@ -430,6 +430,7 @@ int attention_chunk(const Geo& g, const DeviceState* ds, cudaStream_t st, const 
   a.ld_do = ld_do;
   a.D = D;
   a.wo_tiles = womap ? g.hidden / 128 : 0;
+  a.lse_in = lse_in;
   const int timer = womap ? 5 : 0;
   prof_begin(timer, st);
   const cudaError_t e = launch_attn_fwd(qm, km, vm, a, d, ds->err, st, womap, outmap);
@@ -904,10 +905,11 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
       UPIPE_CUDA(launch_gemm(d, false, true, EPI_DO, &dout_k, 1, &wom, 1, ga, ep, ds->err,
                              ds->num_sms, st));
     }
-    // 3. the recomputed attention output (and D')
+    // 3. the recomputed attention output (and D'), with the forward's LSE:
+    //    p = exp(s - lse) needs no online max or row sum
     if (!o_saved)
       UPIPE_TRY(attention_chunk(g, ds, st, Q, K, V, h0, kv0, Ows, g.ch * d, nullptr, flush, dO,
-                                g.ch * d, Dv));
+                                g.ch * d, Dv, nullptr, nullptr, lse + (size_t)h0 * g.S));
     // 4. dWo_c = dout^T O_c
     {
       CUtensorMap om;
