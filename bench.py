@@ -464,14 +464,18 @@ def measure(u, w, ch, mode, steps, warmup, dist, world, rank, dev, full=True, sw
             [{n: torch.empty_like(inp[n]) for n in in_names} for _ in range(nbuf - 1)]
         rbufs = [res0] + [torch.empty_like(res0) for _ in range(nbuf - 1)]
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        ev = {k: [torch.cuda.Event() for _ in range(nbuf)] for k in ("in", "done", "out")}
+        ev = {k: [torch.cuda.Event() for _ in range(nbuf)] for k in ("x", "in", "done", "out")}
 
         def step_io(b):
+            # the forward needs only x: dout's upload runs beside it
             db, rb = dbufs[b], rbufs[b]
             o_ = rb if not mode else out
+            main = torch.cuda.current_stream(dev)
+            main.wait_event(ev["x"][b])
             u.attn_fwd(shape, db["x"], inp["Wq"], inp["Wk"], inp["Wv"], inp["Wo"], o_, lse, ws,
                        inp.get("q_gamma"), inp.get("k_gamma"))
             if mode:
+                main.wait_event(ev["in"][b])
                 u.attn_bwd(shape, db["x"], inp["Wq"], inp["Wk"], inp["Wv"], inp["Wo"],
                            db["dout"], lse, rb, grads["dWq"], grads["dWk"], grads["dWv"],
                            grads["dWo"], ws, inp.get("q_gamma"), inp.get("k_gamma"),
@@ -487,8 +491,10 @@ def measure(u, w, ch, mode, steps, warmup, dist, world, rank, dev, full=True, sw
                 with torch.cuda.stream(s_in):
                     if i >= nbuf:
                         s_in.wait_event(ev["done"][b])   # step i - nbuf is done with it
-                    for n in in_names:
+                    for n in in_names:           # x first, then dout
                         dbufs[b][n].copy_(hosts[n], non_blocking=True)
+                        if n == "x":
+                            ev["x"][b].record(s_in)
                     ev["in"][b].record(s_in)
 
             upload(0)
@@ -496,7 +502,6 @@ def measure(u, w, ch, mode, steps, warmup, dist, world, rank, dev, full=True, sw
                 b = i % nbuf
                 if i + 1 < k:
                     upload(i + 1)
-                main.wait_event(ev["in"][b])
                 if i >= nbuf:
                     main.wait_event(ev["out"][b])        # its result has been downloaded
                 step_io(b)
