@@ -122,6 +122,19 @@ def test_fused_forward_many_heads_and_wide_out():
                      ORDER_MAX_REL, ORDER_MEAN_REL)
 
 
+def test_fused_forward_folds_long_rows():
+    # past 65536 keys the attention folds each long row's O out of TMEM into
+    # per-SM fp32 rows every 512 KV tiles; the fused tail then takes o from
+    # the folded rows plus TMEM, as the separate forward does (d = 64)
+    w = Workload("d64-s70000", S=70000, hidden=256, Hq=1, Hkv=1, d=64, chunk_heads=(1,),
+                 rope_theta=1e4)
+    t = {k: v.cuda() for k, v in make_inputs(w, seed=6).items()}
+    out, lse = run_fused(w, 1, t)
+    out_u, lse_u = run_unfused(w, 1, t)
+    assert torch.equal(lse, lse_u)
+    assert_close(f64(out), f64(out_u), "out vs upipe_attn_fwd", ORDER_MAX_REL, ORDER_MEAN_REL)
+
+
 def test_fused_forward_reports_projection_range_error():
     # a projected value beyond fp16's range is reported, as in upipe_attn_fwd
     w = Workload("range", S=300, hidden=256, Hq=2, Hkv=1, d=64, chunk_heads=(1,),
