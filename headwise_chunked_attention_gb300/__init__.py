@@ -7,5 +7,6 @@ fallback: without the built library every call raises.
 """
 from ._binding import (  # noqa: F401
     UpipeError, Shape, KernelTimer, attn_bwd, attn_fwd, attn_fwd_fused, last_error, lib, lib_path,
-    workspace_bytes, selftest_wait_timeout, ERR_NAMES, ERR_DEVICE_TIMEOUT, ERR_RANGE,
+    workspace_bytes, selftest_wait_timeout, selftest_bounds, debug_bounds, ERR_NAMES, ERR_DEVICE_TIMEOUT, ERR_RANGE, ERR_BOUNDS,
+    DEBUG_BOUNDS,
 )

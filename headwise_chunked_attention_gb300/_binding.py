@@ -8,14 +8,18 @@ from typing import Optional
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_LIB_PATH = os.path.join(_HERE, "_build", "libupipe.so")
+# UPIPE_DEBUG_BOUNDS=1 in the environment loads the debug build (device-side
+# bounds checks of every plain global access; build.build(debug=True))
+DEBUG_BOUNDS = os.environ.get("UPIPE_DEBUG_BOUNDS", "0") not in ("", "0")
+_LIB_PATH = os.path.join(_HERE, "_build_debug" if DEBUG_BOUNDS else "_build", "libupipe.so")
 _lib = None
 
 ERR_NAMES = {0: "UPIPE_OK", 1: "UPIPE_ERR_INVALID_ARG", 2: "UPIPE_ERR_UNSUPPORTED",
              3: "UPIPE_ERR_WORKSPACE_TOO_SMALL", 4: "UPIPE_ERR_CUDA",
-             5: "UPIPE_ERR_DEVICE_TIMEOUT", 6: "UPIPE_ERR_RANGE"}
+             5: "UPIPE_ERR_DEVICE_TIMEOUT", 6: "UPIPE_ERR_RANGE", 7: "UPIPE_ERR_BOUNDS"}
 ERR_DEVICE_TIMEOUT = 5
 ERR_RANGE = 6
+ERR_BOUNDS = 7
 
 
 class UpipeError(RuntimeError):
@@ -78,6 +82,10 @@ def lib():
         L.upipe_profile_count.restype = ctypes.c_int
         L.upipe_strerror.argtypes = [ctypes.c_int]
         L.upipe_strerror.restype = ctypes.c_char_p
+        L.upipe_debug_bounds.argtypes = []
+        L.upipe_debug_bounds.restype = ctypes.c_int
+        L.upipe_selftest_bounds.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
+        L.upipe_selftest_bounds.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -199,6 +207,21 @@ def selftest_wait_timeout(limit_us: int, stream=None) -> None:
     """Enqueue the bounded-wait self-test kernel (its waits expire)."""
     _check(lib().upipe_selftest_wait_timeout(int(limit_us), _stream(stream)),
            "upipe_selftest_wait_timeout")
+
+
+def debug_bounds() -> bool:
+    """True when the loaded library is the bounds-checked debug build."""
+    return bool(lib().upipe_debug_bounds())
+
+
+def selftest_bounds(stream=None) -> bool:
+    """Run the bounds-check self-test; True if its write past the declared
+    view happened (release build), False if a check refused it (debug build,
+    which then reports ERR_BOUNDS through last_error())."""
+    written = ctypes.c_int(-1)
+    _check(lib().upipe_selftest_bounds(_stream(stream), ctypes.byref(written)),
+           "upipe_selftest_bounds")
+    return written.value == 1
 
 
 def last_error() -> int:

@@ -315,8 +315,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
         const int q = min(qs0 + u * BQ + 32 * m + lane, S - 1);  // clamp: masked below
-        nl[m] = ld_nc_f32(lse_g + q);
-        nd[m] = ld_nc_f32(D_g + q);
+        const bool ok_l = dbg_in2(head, a.heads, q, q, a.lse_stride, err);
+        const bool ok_d = dbg_in2(head, a.heads, q, q, S, err);
+        nl[m] = ok_l ? ld_nc_f32(lse_g + q) : 0.f;
+        nd[m] = ok_d ? ld_nc_f32(D_g + q) : 0.f;
       }
     };
     if (wg < n_u) fetch(wg);
@@ -482,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(
         tmem_ld_wait(rv);
         tmem_ld32(tmem + lane_off + 384 + 32 * c, rk);
         tmem_ld_wait(rk);
-        if (key < S) {
+        if (key < S && dbg_in2(key, S, kvh * D + 32 * c, kvh * D + 32 * c + 31, a.ld_dkv, err)) {
           const long long off = (long long)key * a.ld_dkv + kvh * D + 32 * c;
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {

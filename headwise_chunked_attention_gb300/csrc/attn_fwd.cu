@@ -351,8 +351,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the row's max is replaced by its log-sum-exp (base 2, scaled): every
       // p is then final, p * 2^kPShift <= 2^kPShift, and no tile changes it
       // (rows past S take 0: their values are never stored)
-      m_run = qpos < a.S ? a.lse_in[(long long)head * a.lse_stride + qpos] * 1.4426950408889634f
-                         : 0.f;
+      const long long li = (long long)head * a.lse_stride + qpos;
+      m_run = (qpos < a.S && dbg_in(li, li, (long long)a.heads * a.lse_stride, err))
+                  ? a.lse_in[li] * 1.4426950408889634f
+                  : 0.f;
     }
     float m_acc = -INFINITY;  // row max of the folded part of O (-inf: nothing folded)
     bool ok = true;
@@ -446,12 +448,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // O in TMEM holds PV(0 .. j-1) since the last fold, in units of m_run
         const bool have_acc = m_acc != -INFINITY;
         const float keep = have_acc ? ex2(m_acc - m_run) : 0.f;
-        float* acc_row = a.flush + ((size_t)sm_id() * 256 + 128 * t + r) * D;
+        const long long row_off = ((long long)sm_id() * 256 + 128 * t + r) * D;
+        const bool row_ok = dbg_in(row_off, row_off + D - 1, (long long)kFlushSlots * 256 * D, err);
+        float* acc_row = a.flush + row_off;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t rr[32];
           tmem_ld32(o_tmem + 32 * c, rr);
           tmem_ld_wait(rr);
+          if (!row_ok) continue;
           float* ap = acc_row + 32 * c;
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
@@ -479,12 +484,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       // with the known LSE, sum_j p_j = 1: O carries just the 2^kPShift factor
       const float inv_l = KNOWN ? 1.f / (float)(1 << (int)kPShift) : 1.f / l_run;
       const bool live = qpos < a.S;
-      const bool have_acc = m_acc != -INFINITY;
+      const long long row_off = ((long long)sm_id() * 256 + 128 * t + r) * D;
+      const bool have_acc = m_acc != -INFINITY &&
+          dbg_in(row_off, row_off + D - 1, (long long)kFlushSlots * 256 * D, err);
       const float keep = have_acc ? ex2(m_acc - m_run) : 0.f;
-      const float* acc_row =
-          have_acc ? a.flush + ((size_t)sm_id() * 256 + 128 * t + r) * D : nullptr;
-      bf16* op = FUSE ? nullptr : a.O + (long long)qpos * a.ldo + head * D;
-      const __half* dop = a.dO ? a.dO + (long long)qpos * a.ld_do + head * D : nullptr;
+      const float* acc_row = have_acc ? a.flush + row_off : nullptr;
+      // o and dO' rows of this head: columns [head * D, head * D + D) of
+      // [S, ldo] and [S, ld_do]
+      const long long o_off = (long long)qpos * a.ldo + head * D;
+      const long long do_off = (long long)qpos * a.ld_do + head * D;
+      const bool o_ok = FUSE || !live || dbg_in2(qpos, a.S, head * D, head * D + D - 1, a.ldo, err);
+      const bool do_ok = !a.dO || !live ||
+          dbg_in2(qpos, a.S, head * D, head * D + D - 1, a.ld_do, err);
+      bf16* op = FUSE ? nullptr : a.O + o_off;
+      const __half* dop = (a.dO && do_ok) ? a.dO + do_off : nullptr;
       float dot = 0.f;  // D' = dO' . o over the fp32 o (the backward's recompute)
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
@@ -509,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (FUSE || live) {
+        if (FUSE || (live && o_ok)) {
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
             uint4 w;
@@ -532,10 +545,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (live && a.lse)
-        a.lse[(long long)head * a.lse_stride + qpos] =
-            (m_run - kPShift + __log2f(l_run)) * 0.69314718055994531f;
-      if (live && dop) a.D[(long long)head * a.S + qpos] = dot;
+      const long long l_off = (long long)head * a.lse_stride + qpos;
+      if (live && a.lse && dbg_in(l_off, l_off, (long long)a.heads * a.lse_stride, err))
+        a.lse[l_off] = (m_run - kPShift + __log2f(l_run)) * 0.69314718055994531f;
+      const long long d_off = (long long)head * a.S + qpos;
+      if (live && dop && dbg_in(d_off, d_off, (long long)a.heads * a.S, err)) a.D[d_off] = dot;
     }
     if constexpr (FUSE) {
       // o is in shared memory (for the async proxy) and every TMEM read of

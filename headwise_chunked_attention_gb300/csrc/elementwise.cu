@@ -24,7 +24,7 @@ namespace upipe {
 // lo_t[i][p], for consumers whose threads walk positions (one row each).
 __global__ void rope_table_kernel(float2* __restrict__ hi, float2* __restrict__ lo,
                                   float2* __restrict__ lo_t, long long nhi, int half,
-                                  double theta) {
+                                  double theta, int* __restrict__ err) {
   const long long total = (nhi + 1024) * half;
   for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
        t += (long long)gridDim.x * blockDim.x) {
@@ -33,27 +33,31 @@ __global__ void rope_table_kernel(float2* __restrict__ hi, float2* __restrict__ 
     const double w = pow(theta, -2.0 * i / (2.0 * half));
     double ang;
     float2* dst;
+    bool ok;
     if (row < nhi) {
       ang = (double)(row * 1024) * w;
       dst = hi + row * half + i;
+      ok = dbg_in2(row, nhi, i, i, half, err);
     } else {
       ang = (double)(row - nhi) * w;
       dst = lo + (row - nhi) * half + i;
+      ok = dbg_in2(row - nhi, 1024, i, i, half, err);
     }
     double s, c;
     sincos(ang, &s, &c);
-    *dst = make_float2((float)c, (float)s);
-    if (row >= nhi) lo_t[(long long)i * 1024 + (row - nhi)] = make_float2((float)c, (float)s);
+    if (ok) *dst = make_float2((float)c, (float)s);
+    if (row >= nhi && dbg_in2(i, half, row - nhi, row - nhi, 1024, err))
+      lo_t[(long long)i * 1024 + (row - nhi)] = make_float2((float)c, (float)s);
   }
 }
 
 cudaError_t launch_rope_table(float2* hi, float2* lo, float2* lo_t, long long S, int d,
-                              double theta, cudaStream_t stream) {
+                              double theta, cudaStream_t stream, int* err) {
   const long long nhi = (S >> 10) + 1;
   const long long total = (nhi + 1024) * (d / 2);
   const int threads = 256;
   const int blocks = (int)std::min<long long>((total + threads - 1) / threads, 4096);
-  rope_table_kernel<<<blocks, threads, 0, stream>>>(hi, lo, lo_t, nhi, d / 2, theta);
+  rope_table_kernel<<<blocks, threads, 0, stream>>>(hi, lo, lo_t, nhi, d / 2, theta, err);
   return cudaGetLastError();
 }
 
@@ -69,6 +73,7 @@ cudaError_t launch_rope_table(float2* hi, float2* lo, float2* lo_t, long long S,
 template <int D, bool NORM>
 __global__ void __launch_bounds__(256) qk_bwd_kernel(const QkBwdArgs a) {
   constexpr int H = D / 2;
+  int* err = a.err;
   constexpr int LPR = D / 8;      // lanes per item
   constexpr int IPW = 32 / LPR;   // items per warp pass
   __shared__ float sg[D];
@@ -99,8 +104,21 @@ __global__ void __launch_bounds__(256) qk_bwd_kernel(const QkBwdArgs a) {
     const long long it0 = base + sub;
     const bool live = it0 < items;
     const long long it = live ? it0 : items - 1;
-    const long long s = it / a.heads;
-    const int h = (int)(it - s * a.heads);
+    const long long s0 = it / a.heads;
+    const int h0 = (int)(it - s0 * a.heads);
+    // this lane's columns of row s: [h D + 4j, h D + 4j + 3] and the same + H
+    // in g, yhat and the outputs; entries [4j, 4j + 3] (float2) of rows
+    // s & 1023 and s >> 10 of the RoPE tables.
+    // A failed check (debug builds) reads item 0 instead and stores nothing;
+    // every lane still runs the body for the shuffles below.
+    const bool in_ok = dbg_in2(s0, a.S, h0 * D + 4 * j, h0 * D + H + 4 * j + 3, a.ld_g, err) &&
+                       dbg_in2(s0 & 1023, 1024, 4 * j, 4 * j + 3, H, err) &&
+                       dbg_in2(s0 >> 10, (a.S >> 10) + 1, 4 * j, 4 * j + 3, H, err) &&
+                       (!norm || (dbg_in2(s0, a.S, h0 * D + 4 * j, h0 * D + H + 4 * j + 3,
+                                          a.ld_yhat, err) &&
+                                  dbg_in2(h0, a.heads, s0, s0, a.S, err)));
+    const long long s = in_ok ? s0 : 0;
+    const int h = in_ok ? h0 : 0;
     const float* gp = a.g + s * a.ld_g + h * D + 4 * j;
     const float4 ga4 = *reinterpret_cast<const float4*>(gp);
     const float4 gb4 = *reinterpret_cast<const float4*>(gp + H);
@@ -137,7 +155,7 @@ __global__ void __launch_bounds__(256) qk_bwd_kernel(const QkBwdArgs a) {
 #pragma unroll
       for (int k = 0; k < 8; ++k) dy[k] = (dy[k] * gam[k] - yh[k] * mean) * rs;
     }
-    if (live) {
+    if (live && in_ok && dbg_in2(s, a.S, h * D + 4 * j, h * D + H + 4 * j + 3, a.ld_out, err)) {
       const long long o = s * a.ld_out + h * D + 4 * j;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
@@ -201,7 +219,7 @@ __device__ __forceinline__ void split_store(const float4 v, bf16* hi, bf16* lo) 
 
 __global__ void f32_to_bf16x2_kernel(const float* __restrict__ in, int ld_in,
                                      bf16* __restrict__ hi, bf16* __restrict__ lo, int ld_out,
-                                     long long S, int cols4) {
+                                     long long S, int cols4, int* __restrict__ err) {
   const long long total = S * cols4;
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
@@ -209,29 +227,33 @@ __global__ void f32_to_bf16x2_kernel(const float* __restrict__ in, int ld_in,
     const long long t2 = t + stride;
     const long long r = t / cols4;
     const int c = (int)(t - r * cols4) * 4;
-    const float4 v = *reinterpret_cast<const float4*>(in + r * ld_in + c);
+    const bool ok = dbg_in2(r, S, c, c + 3, ld_in, err) && dbg_in2(r, S, c, c + 3, ld_out, err);
+    const float4 v = ok ? *reinterpret_cast<const float4*>(in + r * ld_in + c)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
     long long r2 = 0;
     int c2 = 0;
     float4 v2 = make_float4(0.f, 0.f, 0.f, 0.f);
+    bool ok2 = false;
     if (t2 < total) {
       r2 = t2 / cols4;
       c2 = (int)(t2 - r2 * cols4) * 4;
-      v2 = *reinterpret_cast<const float4*>(in + r2 * ld_in + c2);
+      ok2 = dbg_in2(r2, S, c2, c2 + 3, ld_in, err) && dbg_in2(r2, S, c2, c2 + 3, ld_out, err);
+      if (ok2) v2 = *reinterpret_cast<const float4*>(in + r2 * ld_in + c2);
     }
-    split_store(v, hi + r * ld_out + c, lo + r * ld_out + c);
-    if (t2 < total) split_store(v2, hi + r2 * ld_out + c2, lo + r2 * ld_out + c2);
+    if (ok) split_store(v, hi + r * ld_out + c, lo + r * ld_out + c);
+    if (ok2) split_store(v2, hi + r2 * ld_out + c2, lo + r2 * ld_out + c2);
   }
 }
 
 cudaError_t launch_f32_to_bf16x2(const float* in, int ld_in, bf16* hi, bf16* lo, int ld_out,
-                                 long long S, int cols, cudaStream_t stream) {
+                                 long long S, int cols, cudaStream_t stream, int* err) {
   if (S <= 0 || cols <= 0) return cudaSuccess;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long total = S * (cols / 4);
   const int blocks = (int)std::min<long long>((total + 511) / 512, (long long)sms * 8);
-  f32_to_bf16x2_kernel<<<blocks, 256, 0, stream>>>(in, ld_in, hi, lo, ld_out, S, cols / 4);
+  f32_to_bf16x2_kernel<<<blocks, 256, 0, stream>>>(in, ld_in, hi, lo, ld_out, S, cols / 4, err);
   return cudaGetLastError();
 }
 
@@ -244,7 +266,7 @@ cudaError_t launch_f32_to_bf16x2(const float* in, int ld_in, bf16* hi, bf16* lo,
 __global__ void __launch_bounds__(256)
     grad_bound_kernel(const bf16* __restrict__ dout, long long S, int hidden,
                       const bf16* __restrict__ Wo, int ncols, int row_blocks,
-                      float* __restrict__ bound) {
+                      float* __restrict__ bound, int* __restrict__ err) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if ((int)blockIdx.x < row_blocks) {
     float mx = 0.f;
@@ -252,6 +274,7 @@ __global__ void __launch_bounds__(256)
       const bf16* row = dout + r * hidden;
       float ss = 0.f;
       for (int c = lane * 8; c < hidden; c += 256) {
+        if (!dbg_in2(r, S, c, c + 7, hidden, err)) continue;
         const uint4 v = *reinterpret_cast<const uint4*>(row + c);
         const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&v);
 #pragma unroll
@@ -272,6 +295,7 @@ __global__ void __launch_bounds__(256)
     float ss = 0.f;
     if (col < ncols)
       for (int r = warp; r < hidden; r += 8) {
+        if (!dbg_in2(r, hidden, col, col, ncols, err)) continue;
         const float v = __bfloat162float(Wo[(long long)r * ncols + col]);
         ss = fmaf(v, v, ss);
       }
@@ -289,7 +313,7 @@ __global__ void __launch_bounds__(256)
 }
 
 cudaError_t launch_grad_bound(const bf16* dout, long long S, int hidden, const bf16* Wo,
-                              int ncols, float* bound, cudaStream_t stream) {
+                              int ncols, float* bound, cudaStream_t stream, int* err) {
   if (S <= 0 || hidden <= 0 || ncols <= 0) return cudaSuccess;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
@@ -297,7 +321,7 @@ cudaError_t launch_grad_bound(const bf16* dout, long long S, int hidden, const b
   const int row_blocks = (int)std::min<long long>((S + 7) / 8, (long long)sms * 8);
   const int col_blocks = (ncols + 31) / 32;
   grad_bound_kernel<<<row_blocks + col_blocks, 256, 0, stream>>>(dout, S, hidden, Wo, ncols,
-                                                                 row_blocks, bound);
+                                                                 row_blocks, bound, err);
   return cudaGetLastError();
 }
 

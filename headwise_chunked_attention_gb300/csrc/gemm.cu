@@ -104,14 +104,14 @@ __device__ __forceinline__ void rope_cs(const float2* __restrict__ hi,
 
 template <int D>
 __device__ __forceinline__ void epi_proj_row(const EpiParams& ep, const ProjSeg& sg, long long m,
-                                             int n_local, float (&v)[D], int* err) {
+                                             long long M, int n_local, float (&v)[D], int* err) {
   constexpr int H = D / 2;
   if (sg.mode == PROJ_NORM_ROPE) {
     float ss = 0.f;
 #pragma unroll
     for (int i = 0; i < D; ++i) ss = fmaf(v[i], v[i], ss);
     const float rs = rsqrtf(ss * (1.0f / D) + ep.eps);
-    if (sg.yhat) {
+    if (sg.yhat && dbg_in2(m, M, n_local, n_local + D - 1, sg.ld_yhat, err)) {
       float* yp = sg.yhat + m * sg.ld_yhat + n_local;
 #pragma unroll
       for (int i = 0; i < D; i += 4)
@@ -145,6 +145,7 @@ __device__ __forceinline__ void epi_proj_row(const EpiParams& ep, const ProjSeg&
   }
   if (amax > 65504.f) atomicCAS(err, 0, kErrRange);
   if (sg.norm_max) atomic_max_nonneg(sg.norm_max, sqrtf(ss));
+  if (!dbg_in2(m, M, sg.col0 + n_local, sg.col0 + n_local + D - 1, sg.ld, err)) return;
   __half* op = sg.out + m * sg.ld + sg.col0 + n_local;
 #pragma unroll
   for (int i = 0; i < D; i += 8) {
@@ -368,25 +369,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           while (s + 1 < ep.nseg && n0 >= ep.seg[s].n_end) ++s;
           const ProjSeg& sg = ep.seg[s];
           const int n_local = n0 - sg.n_begin;
-          if (sg.mode == PROJ_NORM_ROPE && sg.rstd) {
+          if (sg.mode == PROJ_NORM_ROPE && sg.rstd &&
+              dbg_in2(n_local / D, (sg.n_end - sg.n_begin) / D, m, m, g.M, err)) {
             float ss = 0.f;
 #pragma unroll
             for (int i = 0; i < D; ++i) ss = fmaf(v[i], v[i], ss);
             sg.rstd[(long long)(n_local / D) * g.M + m] = rsqrtf(ss * (1.0f / D) + ep.eps);
           }
-          epi_proj_row<D>(ep, sg, m, n_local, v, err);
+          epi_proj_row<D>(ep, sg, m, g.M, n_local, v, err);
         }
       } else if constexpr (EPI == EPI_DO) {
         constexpr int D = BN;
         float dot = 0.f, ss = 0.f;
         const int head = n0 / D;
         const float sigma = grad_sigma(ep.bound);
+        // this row's D columns of dO' [M, ld_do] and O [M, ld_o]
+        const bool row_ok = live && dbg_in2(m, g.M, n0, n0 + D - 1, ep.ld_do, err) &&
+                            (!ep.O || dbg_in2(m, g.M, n0, n0 + D - 1, ep.ld_o, err));
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
           tmem_ld32(tbase + c * 32, r);
           tmem_ld_wait(r);
-          if (live) {
+          if (row_ok) {
             __half* dp = ep.dO + m * ep.ld_do + n0 + c * 32;
 #pragma unroll
             for (int i = 0; i < 32; i += 8) {
@@ -417,8 +422,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (live) {
-          if (ep.O) ep.D[(long long)head * g.M + m] = dot;
+        if (row_ok) {
+          if (ep.O && dbg_in2(head, g.N / D, m, m, g.M, err)) ep.D[(long long)head * g.M + m] = dot;
           atomic_max_nonneg(ep.do_max, sqrtf(ss));
         }
       } else if constexpr (EPI == EPI_F32) {
@@ -456,10 +461,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           int s = 0;
           while (s + 1 < g.nmseg && mtile >= g.mseg_t0[s + 1]) ++s;
           const long long ml = m - (long long)g.mseg_t0[s] * BM;
-          row_live = (tc.kb1 > tc.kb0) && ml < g.mseg_rows[s];
+          row_live = (tc.kb1 > tc.kb0) && ml < g.mseg_rows[s] &&
+                     dbg_in2(ml, g.mseg_rows[s], n0, n0 + BN - 1, g.N, err);
           crow = ep.mseg_c[s] + (row_live ? ml * ep.ldc : 0);
         } else {
-          row_live = live;
+          row_live = live && dbg_in2(m, g.M, n0, n0 + BN - 1, g.N, err);
           crow = ep.C + (row_live ? m * ep.ldc : 0);
         }
 #pragma unroll 1

@@ -99,7 +99,7 @@ __host__ __device__ inline float grad_lambda(float do_max, float vmax) {
 // max_i ||dout_i||_2 -> bound[0] and max_j ||Wo[:, j]||_2 -> bound[1]
 // (atomic maxima: bound must start at zero).
 cudaError_t launch_grad_bound(const bf16* dout, long long S, int hidden, const bf16* Wo,
-                              int ncols, float* bound, cudaStream_t stream);
+                              int ncols, float* bound, cudaStream_t stream, int* err);
 
 // ------------------------------------------------------------------ GEMM --
 
@@ -259,7 +259,7 @@ cudaError_t launch_attn_bwd(const AttnBwdArgs& a, int* err, cudaStream_t stream)
 
 // hi [(S >> 10) + 1][d/2], lo [1024][d/2] and lo_t [d/2][1024] (lo transposed)
 cudaError_t launch_rope_table(float2* hi, float2* lo, float2* lo_t, long long S, int d,
-                              double theta, cudaStream_t stream);
+                              double theta, cudaStream_t stream, int* err);
 
 // Backward of (RMSNorm ->) RoPE for one block of heads: g (fp32, gradient of
 // the rotated values) -> bf16 gradient of the projection output; optionally
@@ -276,13 +276,14 @@ struct QkBwdArgs {
   const float* gamma;                // [d] or nullptr
   float* dgamma;                     // [d] accumulated (norm mode)
   const float2* rope_hi; const float2* rope_lo;
+  int* err;                          // device error word (debug bounds checks)
 };
 cudaError_t launch_qk_bwd(const QkBwdArgs& a, cudaStream_t stream);
 
 // fp32 [S, ld_in] -> bf16 high part and bf16 low part (value - high),
 // [S, ld_out] each, for ``cols`` columns: hi + lo carries ~16 significant bits.
 cudaError_t launch_f32_to_bf16x2(const float* in, int ld_in, bf16* hi, bf16* lo, int ld_out,
-                                 long long S, int cols, cudaStream_t stream);
+                                 long long S, int cols, cudaStream_t stream, int* err);
 
 // upipe_attn_fwd with every launch on the caller's stream: no side stream,
 // no events (the static-scratch entry point, which must create nothing).
@@ -293,5 +294,10 @@ int attn_fwd_unforked(const upipe_shape_t* shape, const upipe_bf16* x, const upi
 
 // One-CTA kernel whose waits expire after limit_ns (failure-detection test).
 cudaError_t launch_selftest_wait(int* err, unsigned long long limit_ns, cudaStream_t stream);
+// One-thread kernel whose write lies one element past a declared view (inside
+// its array): debug builds refuse it (UPIPE_ERR_BOUNDS); *written after a
+// synchronisation tells whether the write happened.
+cudaError_t launch_selftest_bounds(int* err, cudaStream_t stream);
+cudaError_t selftest_bounds_probe_written(int* written);
 
 }  // namespace upipe

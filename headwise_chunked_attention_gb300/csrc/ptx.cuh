@@ -14,7 +14,37 @@ namespace upipe {
 
 constexpr int kErrDeviceTimeout = 5;                         // UPIPE_ERR_DEVICE_TIMEOUT
 constexpr int kErrRange = 6;                                 // UPIPE_ERR_RANGE
+constexpr int kErrBounds = 7;                                // UPIPE_ERR_BOUNDS
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s per wait
+
+// Debug builds (compiled with UPIPE_DEBUG_BOUNDS): a bounds check of one plain
+// (non-TMA) global access, elements [first, last] of a view of n elements as
+// the launch's arguments declare it.  A failed check records UPIPE_ERR_BOUNDS
+// in the error word and the caller skips the access; nothing traps.  Release
+// builds compile the check to true.
+__device__ __forceinline__ bool dbg_in(long long first, long long last, long long n, int* err) {
+#ifdef UPIPE_DEBUG_BOUNDS
+  if (first >= 0 && first <= last && last < n) return true;
+  atomicCAS(err, 0, kErrBounds);
+  return false;
+#else
+  (void)first; (void)last; (void)n; (void)err;
+  return true;
+#endif
+}
+
+// The same for columns [c0, c1] of row ``row`` of a row-major [rows, ld] view.
+__device__ __forceinline__ bool dbg_in2(long long row, long long rows, long long c0, long long c1,
+                                        long long ld, int* err) {
+#ifdef UPIPE_DEBUG_BOUNDS
+  if (row >= 0 && row < rows && c0 >= 0 && c0 <= c1 && c1 < ld) return true;
+  atomicCAS(err, 0, kErrBounds);
+  return false;
+#else
+  (void)row; (void)rows; (void)c0; (void)c1; (void)ld; (void)err;
+  return true;
+#endif
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -490,7 +490,7 @@ static int attn_fwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
   __half* V = at<__half>(workspace, L.v);
   bf16* Ows = at<bf16>(workspace, L.o);
   float* flush = L.flush == (size_t)-1 ? nullptr : at<float>(workspace, L.flush);
-  UPIPE_CUDA(launch_rope_table(rhi, rlo, rlo_t, g.S, g.d, shape->rope_theta, st));
+  UPIPE_CUDA(launch_rope_table(rhi, rlo, rlo_t, g.S, g.d, shape->rope_theta, st, ds->err));
 
   CUtensorMap xmap, outmap;
   UPIPE_MAP(&xmap, x, g.S, g.hidden, g.hidden, 128, 64);
@@ -671,7 +671,7 @@ extern "C" int upipe_attn_fwd_fused(const upipe_shape_t* shape, const upipe_bf16
   __half* K = at<__half>(workspace, L.k);
   __half* V = at<__half>(workspace, L.v);
   float* flush = L.flush == (size_t)-1 ? nullptr : at<float>(workspace, L.flush);
-  UPIPE_CUDA(launch_rope_table(rhi, rlo, rlo_t, g.S, g.d, shape->rope_theta, st));
+  UPIPE_CUDA(launch_rope_table(rhi, rlo, rlo_t, g.S, g.d, shape->rope_theta, st, ds->err));
 
   CUtensorMap xmap, outmap, womap;
   UPIPE_MAP(&xmap, x, g.S, g.hidden, g.hidden, 128, 64);
@@ -768,11 +768,11 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
   float* yk = g.norm ? at<float>(workspace, L.yk) : nullptr;
   float* rk = g.norm ? at<float>(workspace, L.rk) : nullptr;
 
-  UPIPE_CUDA(launch_rope_table(rhi, rlo, rlo_t, g.S, d, shape->rope_theta, st));
+  UPIPE_CUDA(launch_rope_table(rhi, rlo, rlo_t, g.S, d, shape->rope_theta, st, ds->err));
   // the fp16 gradient scales: norm maxima start at zero; the dO scale's
   // bound (max ||dout_i||, max ||Wo[:, j]||) is taken once per call
   UPIPE_CUDA(cudaMemsetAsync(sc, 0, sizeof(float) * (size_t)(2 + g.Hkv + g.nchunks), st));
-  UPIPE_CUDA(launch_grad_bound(dout, g.S, g.hidden, Wo, g.Hq * d, sc, st));
+  UPIPE_CUDA(launch_grad_bound(dout, g.S, g.hidden, Wo, g.Hq * d, sc, st, ds->err));
   // split-K weight gradients accumulate with reductions: start from zero
   UPIPE_CUDA(cudaMemsetAsync(dWq, 0, sizeof(float) * (size_t)g.Hq * d * g.hidden, st));
   UPIPE_CUDA(cudaMemsetAsync(dWk, 0, sizeof(float) * (size_t)g.Hkv * d * g.hidden, st));
@@ -964,6 +964,7 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
     //    dWq_c = dA_q^T x, each as a hi and a lo GEMM
     {
       QkBwdArgs q{};
+      q.err = ds->err;
       q.S = g.S;
       q.heads = g.ch;
       q.d = d;
@@ -993,6 +994,7 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
     //    dV -> hi over V and lo beside it
     if (last_of_group) {
       QkBwdArgs q{};
+      q.err = ds->err;
       q.S = g.S;
       q.heads = g.kvc;
       q.d = d;
@@ -1013,7 +1015,8 @@ static int attn_bwd_impl(const upipe_shape_t* shape, const upipe_bf16* x_,
       UPIPE_CUDA(launch_qk_bwd(q, st));
       prof_end(3, st);
       prof_begin(4, st);
-      UPIPE_CUDA(launch_f32_to_bf16x2(dV, g.kvc * d, V_hi, dVlo, g.kvc * d, g.S, g.kvc * d, st));
+      UPIPE_CUDA(launch_f32_to_bf16x2(dV, g.kvc * d, V_hi, dVlo, g.kvc * d, g.S, g.kvc * d, st,
+                                      ds->err));
       prof_end(4, st);
       const bf16* Wk_g = Wk + (size_t)kv0 * d * g.hidden;
       const bf16* Wv_g = Wv + (size_t)kv0 * d * g.hidden;
@@ -1079,6 +1082,25 @@ extern "C" int upipe_selftest_wait_timeout(int limit_us, void* stream) {
   return UPIPE_OK;
 }
 
+extern "C" int upipe_debug_bounds(void) {
+#ifdef UPIPE_DEBUG_BOUNDS
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+extern "C" int upipe_selftest_bounds(void* stream, int* written) {
+  if (!written) return UPIPE_ERR_INVALID_ARG;
+  DeviceState* ds = nullptr;
+  UPIPE_TRY(device_state(&ds));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  UPIPE_CUDA(launch_selftest_bounds(ds->err, st));
+  UPIPE_CUDA(cudaStreamSynchronize(st));
+  UPIPE_CUDA(selftest_bounds_probe_written(written));
+  return UPIPE_OK;
+}
+
 extern "C" int upipe_last_error(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return UPIPE_ERR_CUDA;
   int v = 0;
@@ -1098,6 +1120,7 @@ extern "C" const char* upipe_strerror(int code) {
     case UPIPE_ERR_CUDA: return "CUDA error";
     case UPIPE_ERR_DEVICE_TIMEOUT: return "device wait timed out";
     case UPIPE_ERR_RANGE: return "projected value outside the fp16 range";
+    case UPIPE_ERR_BOUNDS: return "device bounds check failed (debug build)";
     default: return "unknown error";
   }
 }

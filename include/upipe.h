@@ -88,8 +88,11 @@ enum {
   UPIPE_ERR_WORKSPACE_TOO_SMALL = 3,  /* ws_bytes < upipe_workspace_bytes()  */
   UPIPE_ERR_CUDA = 4,                 /* a CUDA runtime/driver call failed    */
   UPIPE_ERR_DEVICE_TIMEOUT = 5,       /* a kernel's bounded wait expired      */
-  UPIPE_ERR_RANGE = 6                 /* a projected q, k or v value exceeds
+  UPIPE_ERR_RANGE = 6,                /* a projected q, k or v value exceeds
                                          the fp16 range (|v| > 65504)        */
+  UPIPE_ERR_BOUNDS = 7                /* debug builds only: a device-side
+                                         bounds check of a global access
+                                         failed (the access was skipped)     */
 };
 
 /* Workspace bytes needed by upipe_attn_fwd (mode 0) or upipe_attn_bwd
@@ -244,10 +247,29 @@ int upipe_profile_count(void);
  * Returns UPIPE_OK once enqueued, UPIPE_ERR_INVALID_ARG for a bad limit. */
 int upipe_selftest_wait_timeout(int limit_us, void* stream);
 
+/* 1 if this library was built with device-side bounds checks (the debug
+ * build: UPIPE_DEBUG_BOUNDS), else 0.  In that build every plain (non-TMA)
+ * global load and store of the kernels is checked against the extent of its
+ * view as the launch declares it; a failed check skips the access and
+ * records UPIPE_ERR_BOUNDS for upipe_last_error().  It stands in for a
+ * memory checker (no such checker runs on the GPUs this library is tested
+ * on).  Host function. */
+int upipe_debug_bounds(void);
+
+/* Bounds-check self-test (no counterpart on the pages).  Runs a one-thread
+ * kernel that asks to write one element past a declared view (the element
+ * lies inside the underlying array, so the write is harmless either way) and
+ * waits for it on ``stream``.  *written receives 1 if the write happened.
+ * Debug build: the check refuses it (*written = 0) and the next
+ * upipe_last_error() returns UPIPE_ERR_BOUNDS.  Release build: the write
+ * happens (*written = 1) and nothing is reported.
+ * Returns UPIPE_OK, UPIPE_ERR_INVALID_ARG (written NULL) or UPIPE_ERR_CUDA. */
+int upipe_selftest_bounds(void* stream, int* written);
+
 /* Synchronises the current device, then returns and clears the device error
- * word (UPIPE_OK, UPIPE_ERR_DEVICE_TIMEOUT or UPIPE_ERR_RANGE: the first error
- * a kernel recorded since the last call), or UPIPE_ERR_CUDA if the device
- * reports a CUDA error. */
+ * word (UPIPE_OK, UPIPE_ERR_DEVICE_TIMEOUT, UPIPE_ERR_RANGE or, in the debug
+ * build, UPIPE_ERR_BOUNDS: the first error a kernel recorded since the last
+ * call), or UPIPE_ERR_CUDA if the device reports a CUDA error. */
 int upipe_last_error(void);
 
 /* Static description of an error code. */

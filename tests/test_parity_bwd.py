@@ -44,7 +44,8 @@ def run_fwd_bwd(w, ch, inp, saved_o=False, dout_scale=None):
                g["dx"], g["dWq"], g["dWk"], g["dWv"], g["dWo"], ws,
                t.get("q_gamma"), t.get("k_gamma"), dqg, dkg, attn_o=o)
     torch.cuda.synchronize()
-    assert u.last_error() == 0
+    rc = u.last_error()
+    assert rc == 0, f"device error word {rc}"
     for name, b in gb.items():
         b.check(name)
     g["dq_gamma"], g["dk_gamma"] = dqg, dkg

@@ -38,7 +38,8 @@ def run_fused(w, ch, t, expect_error=0):
     u.attn_fwd_fused(shape, t["x"], t["Wq"], t["Wk"], t["Wv"], t["Wo"], out, lse, ws,
                      t.get("q_gamma"), t.get("k_gamma"))
     torch.cuda.synchronize()
-    assert u.last_error() == expect_error
+    rc = u.last_error()
+    assert rc == expect_error, f"device error word {rc}, expected {expect_error}"
     for name, b in g.items():
         b.check(name)
     return out, lse
@@ -53,7 +54,8 @@ def run_unfused(w, ch, t):
     u.attn_fwd(shape, t["x"], t["Wq"], t["Wk"], t["Wv"], t["Wo"], out, lse, ws,
                t.get("q_gamma"), t.get("k_gamma"))
     torch.cuda.synchronize()
-    assert u.last_error() == 0
+    rc = u.last_error()
+    assert rc == 0, f"device error word {rc}"
     return out, lse
 
 

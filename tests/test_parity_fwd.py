@@ -34,7 +34,8 @@ def run_fwd(w, ch, inp, debug=True, expect_error=0):
     u.attn_fwd(shape, t["x"], t["Wq"], t["Wk"], t["Wv"], t["Wo"], out, lse, ws,
                t.get("q_gamma"), t.get("k_gamma"), o)
     torch.cuda.synchronize()
-    assert u.last_error() == expect_error
+    rc = u.last_error()
+    assert rc == expect_error, f"device error word {rc}, expected {expect_error}"
     for name, b in g.items():
         b.check(name)
     return out, lse, o
