@@ -89,10 +89,11 @@ NCU_TRAFFIC = {
     # bytes were taken at S = 262144 (same geometry and chunk size) and scaled
     # by the causal pairs to S = 1,048,576 (x16.0); from 65536 to 262144 the
     # traffic grew 3.7-4.0x per doubling of S, in step with the pairs
-    ("attn_fwd_kernel", "llama3-8b-rank-s1m", 1): (11269829632, "91bdcf6c4b8a9da0"),
-    ("attn_bwd_kernel", "llama3-8b-rank-s1m", 1): (53681712128, "74fa113cbcfbec9a"),
-    # the separate forward's launch at the secondary workload, captured in full
-    ("attn_fwd_kernel", "llama3.2-3b-s65536", 3): (88990208, "91bdcf6c4b8a9da0"),
+    ("attn_fwd_kernel", "llama3-8b-rank-s1m", 1): (11216113664, "ea34b7bf3592d3cf"),
+    ("attn_bwd_kernel", "llama3-8b-rank-s1m", 1): (53664954368, "952ce4de4e5f29cd"),
+    # the separate forward's launches at the secondary workload (a full
+    # capture: mean of one step's 8 chunk launches)
+    ("attn_fwd_kernel", "llama3.2-3b-s65536", 3): (88330144, "ea34b7bf3592d3cf"),
 }
 KERNEL_SOURCES = {"attn_fwd_kernel": "attn_fwd.cu", "attn_bwd_kernel": "attn_bwd.cu"}
 
