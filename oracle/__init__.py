@@ -1,4 +1,5 @@
-"""Float64 CPU oracle of the headwise-chunked causal GQA attention layer.
+"""Float64 CPU oracle of the headwise-chunked causal GQA attention layer and
+of the sequence-tiled MLP around it.
 
 TEST INFRASTRUCTURE: only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
 baseline of ``bench.py`` use it.  It shares no code with the CUDA path and is
@@ -9,4 +10,7 @@ from .attention_layer import (  # noqa: F401
     apply_rope, apply_rope_transpose, causal_attention,
     layer_backward, layer_backward_key_rows, layer_backward_tail, layer_forward, layer_loss, project_kv, rms_norm,
     rms_norm_backward, rope_cos_sin,
+)
+from .mlp import (  # noqa: F401
+    mlp_backward, mlp_forward, mlp_loss, sigmoid, silu, silu_grad,
 )
