@@ -45,6 +45,12 @@ class Shape(ctypes.Structure):
                    float(w.rope_theta), int(bool(w.qk_norm)), float(w.norm_eps))
 
 
+class MlpShape(ctypes.Structure):
+    """upipe_mlp_shape_t: the sequence-tiled MLP's geometry."""
+    _fields_ = [("S", ctypes.c_int64), ("hidden", ctypes.c_int32),
+                ("ffn", ctypes.c_int32), ("tile_rows", ctypes.c_int32)]
+
+
 def lib_path() -> str:
     return _LIB_PATH
 
@@ -82,6 +88,12 @@ def lib():
         L.upipe_profile_count.restype = ctypes.c_int
         L.upipe_strerror.argtypes = [ctypes.c_int]
         L.upipe_strerror.restype = ctypes.c_char_p
+        L.upipe_mlp_workspace_bytes.argtypes = [ctypes.POINTER(MlpShape), ctypes.c_int]
+        L.upipe_mlp_workspace_bytes.restype = ctypes.c_size_t
+        L.upipe_mlp_fwd.argtypes = [ctypes.POINTER(MlpShape)] + [P] * 6 + [ctypes.c_size_t, P]
+        L.upipe_mlp_fwd.restype = ctypes.c_int
+        L.upipe_mlp_bwd.argtypes = [ctypes.POINTER(MlpShape)] + [P] * 10 + [ctypes.c_size_t, P]
+        L.upipe_mlp_bwd.restype = ctypes.c_int
         L.upipe_debug_bounds.argtypes = []
         L.upipe_debug_bounds.restype = ctypes.c_int
         L.upipe_selftest_bounds.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
@@ -207,6 +219,31 @@ def selftest_wait_timeout(limit_us: int, stream=None) -> None:
     """Enqueue the bounded-wait self-test kernel (its waits expire)."""
     _check(lib().upipe_selftest_wait_timeout(int(limit_us), _stream(stream)),
            "upipe_selftest_wait_timeout")
+
+
+def mlp_workspace_bytes(shape: MlpShape, mode: int = 0) -> int:
+    return int(lib().upipe_mlp_workspace_bytes(ctypes.byref(shape), mode))
+
+
+def mlp_fwd(shape: MlpShape, x, Wg, Wu, Wd, y, workspace, stream=None):
+    """upipe_mlp_fwd: y [S, hidden] fp32 = the SwiGLU MLP of x, tile by tile."""
+    bf = torch.bfloat16
+    rc = lib().upipe_mlp_fwd(
+        ctypes.byref(shape), _ptr(x, bf, "x"), _ptr(Wg, bf, "Wg"), _ptr(Wu, bf, "Wu"),
+        _ptr(Wd, bf, "Wd"), _ptr(y, torch.float32, "y"), _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "upipe_mlp_fwd")
+
+
+def mlp_bwd(shape: MlpShape, x, Wg, Wu, Wd, dy, dx, dWg, dWu, dWd, workspace, stream=None):
+    """upipe_mlp_bwd: dx (fp32) and the fp32 weight gradients of sum(y * dy)."""
+    bf, f = torch.bfloat16, torch.float32
+    rc = lib().upipe_mlp_bwd(
+        ctypes.byref(shape), _ptr(x, bf, "x"), _ptr(Wg, bf, "Wg"), _ptr(Wu, bf, "Wu"),
+        _ptr(Wd, bf, "Wd"), _ptr(dy, bf, "dy"), _ptr(dx, f, "dx"), _ptr(dWg, f, "dWg"),
+        _ptr(dWu, f, "dWu"), _ptr(dWd, f, "dWd"), _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "upipe_mlp_bwd")
 
 
 def debug_bounds() -> bool:

@@ -31,7 +31,13 @@
 //                   read-modify-write runs in L2, the SM never reads out);
 //   EPI_DO          dO_c = dOut Wo_c, scaled and stored in fp16 (and, given
 //                   O, D = rowsum(dO * O) per head);
-//   EPI_F32_ATOMIC  split-K weight gradients, reduced with red.global.add.
+//   EPI_F32_ATOMIC  split-K weight gradients, reduced with red.global.add;
+//   EPI_SWIGLU      the sequence-tiled MLP's gate and up projections: each
+//                   256-wide output tile is 128 gate rows and the same 128 up
+//                   rows (two B maps, one 128-row TMA box each into one B
+//                   stage), and the epilogue stores a = silu(g) * u in bf16;
+//   EPI_SWIGLU_BWD  the same recomputed, with dA read for the tile and
+//                   dg = dA u silu'(g), du = dA silu(g) and a stored in bf16.
 #include <algorithm>
 
 #include "internal.h"
@@ -206,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&maps.b[1]);
       prefetch_tmap(&maps.b[2]);
     }
+    if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) prefetch_tmap(&maps.b[1]);
     for (int s = 1; s < g.nkseg; ++s) {
       prefetch_tmap(&maps.a[g.kseg_a[s]]);
       prefetch_tmap(&maps.b[g.kseg_b[s]]);
@@ -271,7 +278,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_2d(sam + 8192, am, &full[stage], arow + BM * mt + 64, k0);
             }
           }
-          if (!B_MN) {
+          if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) {
+            // gate rows, then the same up rows: one 256-row K-major B tile
+            tma_load_2d(sb, &maps.b[0], &full[stage], k0, brow / 2);
+            tma_load_2d(sb + (BN / 2) * BK * 2, &maps.b[1], &full[stage], k0, brow / 2);
+          } else if (!B_MN) {
             tma_load_2d(sb, bm, &full[stage], k0, brow);
           } else {
 #pragma unroll
@@ -426,6 +437,64 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ep.O && dbg_in2(head, g.N / D, m, m, g.M, err)) ep.D[(long long)head * g.M + m] = dot;
           atomic_max_nonneg(ep.do_max, sqrtf(ss));
         }
+      } else if constexpr (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) {
+        // accumulator columns [0, 128): g, [128, 256): u of output columns
+        // [c0, c0 + 128) of this row
+        constexpr int H = BN / 2;
+        const long long c0 = n0 / 2;
+        bool row_ok = live && dbg_in2(m, g.M, c0, c0 + H - 1, ep.ld_act, err);
+        if constexpr (EPI == EPI_SWIGLU_BWD)
+          row_ok = row_ok && dbg_in2(m, g.M, c0, c0 + H - 1, ep.ld_da, err) &&
+                   dbg_in2(m, g.M, c0, c0 + H - 1, ep.ld_dg, err);
+#pragma unroll 1
+        for (int c = 0; c < H / 32; ++c) {
+          uint32_t rg[32], ru[32];
+          tmem_ld32(tbase + 32 * c, rg);
+          tmem_ld_wait(rg);
+          tmem_ld32(tbase + H + 32 * c, ru);
+          tmem_ld_wait(ru);
+          if (!row_ok) continue;
+          const long long off_a = m * ep.ld_act + c0 + 32 * c;
+          if constexpr (EPI == EPI_SWIGLU) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+              uint4 w;
+              uint32_t* wp = &w.x;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const float g0 = __uint_as_float(rg[i + 2 * j]), g1 = __uint_as_float(rg[i + 2 * j + 1]);
+                const float u0 = __uint_as_float(ru[i + 2 * j]), u1 = __uint_as_float(ru[i + 2 * j + 1]);
+                // silu(v) = v / (1 + e^-v); e^-v = inf for v << 0 gives -0
+                wp[j] = pack_bf16(g0 / (1.f + __expf(-g0)) * u0, g1 / (1.f + __expf(-g1)) * u1);
+              }
+              *reinterpret_cast<uint4*>(ep.act + off_a + i) = w;
+            }
+          } else {
+            const float* dap = ep.dA + m * ep.ld_da + c0 + 32 * c;
+            const long long off_g = m * ep.ld_dg + c0 + 32 * c;
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              const float4 d4 = *reinterpret_cast<const float4*>(dap + i);
+              const float da[4] = {d4.x, d4.y, d4.z, d4.w};
+              float vg[4], vu[4], va[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const float gv = __uint_as_float(rg[i + j]), uv = __uint_as_float(ru[i + j]);
+                const float sg = 1.f / (1.f + __expf(-gv));   // sigmoid(g)
+                const float sl = gv * sg;                      // silu(g)
+                vg[j] = da[j] * uv * (sg * (1.f + gv * (1.f - sg)));
+                vu[j] = da[j] * sl;
+                va[j] = sl * uv;
+              }
+              *reinterpret_cast<uint2*>(ep.dG + off_g + i) =
+                  make_uint2(pack_bf16(vg[0], vg[1]), pack_bf16(vg[2], vg[3]));
+              *reinterpret_cast<uint2*>(ep.dU + off_g + i) =
+                  make_uint2(pack_bf16(vu[0], vu[1]), pack_bf16(vu[2], vu[3]));
+              *reinterpret_cast<uint2*>(ep.act + off_a + i) =
+                  make_uint2(pack_bf16(va[0], va[1]), pack_bf16(va[2], va[3]));
+            }
+          }
+        }
       } else if constexpr (EPI == EPI_F32) {
         // [32 rows x 32 cols] fp32 blocks of this warp's rows, 128-byte
         // swizzled in shared memory, then one TMA store / reduce-add each
@@ -574,6 +643,11 @@ cudaError_t launch_gemm(int bn, bool a_mn, bool b_mn, EpiKind epi, const CUtenso
   UPIPE_GEMM_CASE(256, true, true, EPI_F32_ATOMIC)
   UPIPE_GEMM_CASE(128, true, true, EPI_F32_ATOMIC)
   UPIPE_GEMM_CASE(64, true, true, EPI_F32_ATOMIC)
+  // the sequence-tiled MLP's gate/up projections (two B maps)
+  if ((epi == EPI_SWIGLU || epi == EPI_SWIGLU_BWD) && (bn != 256 || a_mn || b_mn || nb < 2))
+    return cudaErrorInvalidValue;
+  UPIPE_GEMM_CASE(256, false, false, EPI_SWIGLU)
+  UPIPE_GEMM_CASE(256, false, false, EPI_SWIGLU_BWD)
 #undef UPIPE_GEMM_CASE
   return cudaErrorNotSupported;
 }

@@ -108,6 +108,8 @@ enum EpiKind : int {
   EPI_F32 = 1,         // fp32 store (beta = 0) or read-modify-write add (beta = 1)
   EPI_DO = 2,          // scaled fp16 store of dO plus D = rowsum(dO * O) per head
   EPI_F32_ATOMIC = 3,  // fp32 reduction-add (split-K partial sums)
+  EPI_SWIGLU = 4,      // MLP gate/up: a = silu(g) * u, bf16 store
+  EPI_SWIGLU_BWD = 5,  // MLP gate/up recomputed: dg, du (from dA) and a, bf16 stores
 };
 
 enum ProjMode : int { PROJ_PLAIN = 0, PROJ_ROPE = 1, PROJ_NORM_ROPE = 2 };
@@ -156,6 +158,19 @@ struct EpiParams {
   float* D;  // [heads][M]
   const float* bound;   // [Mdout, Wcol] (backward fp16 scales, above)
   float* do_max;
+  // EPI_SWIGLU / EPI_SWIGLU_BWD: B map 0 holds the gate weights Wg, B map 1
+  // the up weights Wu ([ffn, K] each); output tile n of N = 2 ffn is gate rows
+  // and up rows [128 n, 128 n + 128), i.e. columns [128 n, 128 n + 128) of
+  // a = silu(g) * u [M, ffn] (bf16, row stride ld_act).  EPI_SWIGLU_BWD also
+  // reads dA [M, ffn] fp32 (row stride ld_da) and stores
+  //   dg = dA * u * silu'(g),  du = dA * silu(g)   (bf16, row stride ld_dg)
+  bf16* act;
+  long long ld_act;
+  const float* dA;
+  long long ld_da;
+  bf16* dG;
+  bf16* dU;
+  long long ld_dg;
 };
 
 constexpr int kMaxASegs = 6;  // A tensor maps of one GEMM
@@ -284,6 +299,22 @@ cudaError_t launch_qk_bwd(const QkBwdArgs& a, cudaStream_t stream);
 // [S, ld_out] each, for ``cols`` columns: hi + lo carries ~16 significant bits.
 cudaError_t launch_f32_to_bf16x2(const float* in, int ld_in, bf16* hi, bf16* lo, int ld_out,
                                  long long S, int cols, cudaStream_t stream, int* err);
+
+// The current device's error word and SM count (created on first use).
+int device_context(int** err, int* num_sms);
+
+// Split-K factor for a weight-gradient GEMM with K = S and an [M, N] output of
+// BN-wide tiles on ``sms`` SMs.
+int wgrad_splits(int64_t S, int M, int N, int bn, int sms);
+
+// NVTX range over the host-side enqueue of one entry point or one chunk
+// (header-only NVTX: without a tool attached each push/pop is a no-op call).
+struct NvtxRange {
+  explicit NvtxRange(const char* what, int chunk = -1);
+  ~NvtxRange();
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // upipe_attn_fwd with every launch on the caller's stream: no side stream,
 // no events (the static-scratch entry point, which must create nothing).

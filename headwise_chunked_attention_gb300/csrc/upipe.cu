@@ -29,23 +29,18 @@ namespace upipe {
 
 __device__ int g_device_error = 0;
 
-// NVTX range over the host-side enqueue of one entry point or one chunk, so
-// that a timeline tool shows the chunk loop (header-only NVTX: without a tool
-// attached each push/pop is a no-op call).
-struct NvtxRange {
-  explicit NvtxRange(const char* what, int chunk = -1) {
-    if (chunk < 0) {
-      nvtxRangePushA(what);
-    } else {
-      char name[64];
-      std::snprintf(name, sizeof name, "%s chunk %d", what, chunk);
-      nvtxRangePushA(name);
-    }
+// NVTX ranges (internal.h): one per entry point and per chunk, so that a
+// timeline tool shows the chunk loop.
+NvtxRange::NvtxRange(const char* what, int chunk) {
+  if (chunk < 0) {
+    nvtxRangePushA(what);
+  } else {
+    char name[64];
+    std::snprintf(name, sizeof name, "%s chunk %d", what, chunk);
+    nvtxRangePushA(name);
   }
-  ~NvtxRange() { nvtxRangePop(); }
-  NvtxRange(const NvtxRange&) = delete;
-  NvtxRange& operator=(const NvtxRange&) = delete;
-};
+}
+NvtxRange::~NvtxRange() { nvtxRangePop(); }
 
 namespace {
 
@@ -314,6 +309,8 @@ struct Events {
   }
 };
 
+}  // namespace
+
 // Split-K partitions of a weight-gradient GEMM (K = S tokens, M x N output in
 // 128 x bn tiles): about one partition per 8192 tokens (at most 64), moved
 // within a factor of two of that to the count whose tiles fill the last wave
@@ -337,6 +334,8 @@ int wgrad_splits(int64_t S, int M, int N, int bn, int sms) {
   }
   return best;
 }
+
+namespace {
 
 // Longest query walk (sub-tiles of 64 queries) of one attention-backward CTA,
 // whose dK / dV accumulate in TMEM over the walk: the whole walk up to 1M
@@ -1081,6 +1080,16 @@ extern "C" int upipe_selftest_wait_timeout(int limit_us, void* stream) {
                                   static_cast<cudaStream_t>(stream)));
   return UPIPE_OK;
 }
+
+namespace upipe {
+int device_context(int** err, int* num_sms) {
+  DeviceState* ds = nullptr;
+  UPIPE_TRY(device_state(&ds));
+  *err = ds->err;
+  *num_sms = ds->num_sms;
+  return UPIPE_OK;
+}
+}  // namespace upipe
 
 extern "C" int upipe_debug_bounds(void) {
 #ifdef UPIPE_DEBUG_BOUNDS

@@ -247,6 +247,53 @@ int upipe_profile_count(void);
  * Returns UPIPE_OK once enqueued, UPIPE_ERR_INVALID_ARG for a bad limit. */
 int upipe_selftest_wait_timeout(int limit_us, void* stream);
 
+/* ------------------------------------------------------------------------
+ * The sequence-tiled MLP of the decoder layer (no counterpart in the chunked
+ * attention itself).  The pages' memory stack tiles the element-wise parts of
+ * the layer, the MLPs and the loss, along the sequence so that no buffer as
+ * long as the sequence is created (memeeeeeex.com article, the stack section
+ * on Arctic sequence-length training; liquidgold.cc talk transcript).  The MLP
+ * is the bias-free SwiGLU MLP of the Llama / Qwen3 models:
+ *     y = (silu(x Wg^T) * (x Wu^T)) Wd^T,   silu(v) = v / (1 + e^-v)
+ * computed over tiles of tile_rows tokens; the [tile_rows, ffn]
+ * intermediates live in the workspace and are reused by every tile.  A
+ * token's output depends on that token alone, so tiling changes memory, not
+ * the result.
+ *   S          tokens, 1 <= S <= 2^31 - 256
+ *   hidden     model width, a multiple of 128
+ *   ffn        MLP width, a multiple of 128
+ *   tile_rows  tokens per tile, a multiple of 128 (S itself when shorter)
+ * Layouts (row-major, nn.Linear weights): x, dy [S, hidden] bf16;
+ * Wg, Wu [ffn, hidden] bf16; Wd [hidden, ffn] bf16; y, dx [S, hidden] fp32;
+ * dWg, dWu [ffn, hidden] fp32; dWd [hidden, ffn] fp32.  The per-tile
+ * intermediates a, dg, du are held in bf16, every contraction accumulates in
+ * fp32.  Device pointers, 16-byte aligned; the workspace 256-byte aligned.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  int64_t S;
+  int32_t hidden, ffn, tile_rows;
+} upipe_mlp_shape_t;
+
+/* Workspace bytes of upipe_mlp_fwd (mode 0: a, min(tile_rows, S) x ffn bf16)
+ * or upipe_mlp_bwd (mode 1: a, dg, du bf16 and dA fp32 of one tile), or 0 for
+ * an invalid shape or mode.  Pure host function. */
+size_t upipe_mlp_workspace_bytes(const upipe_mlp_shape_t* shape, int mode);
+
+/* y = MLP(x), tile by tile.  y is overwritten (every row is stored once).
+ * Returns UPIPE_OK or an error code (nothing launched on error). */
+int upipe_mlp_fwd(const upipe_mlp_shape_t* shape, const upipe_bf16* x, const upipe_bf16* Wg,
+                  const upipe_bf16* Wu, const upipe_bf16* Wd, float* y, void* workspace,
+                  size_t ws_bytes, void* stream);
+
+/* Gradients of L = sum(y * dy): dx (overwritten, row by row), dWg, dWu, dWd
+ * (zeroed, then accumulated over the tiles with fp32 reduce-adds in no fixed
+ * order).  Each tile recomputes its gate and up projections.
+ * Returns UPIPE_OK or an error code (nothing launched on error). */
+int upipe_mlp_bwd(const upipe_mlp_shape_t* shape, const upipe_bf16* x, const upipe_bf16* Wg,
+                  const upipe_bf16* Wu, const upipe_bf16* Wd, const upipe_bf16* dy, float* dx,
+                  float* dWg, float* dWu, float* dWd, void* workspace, size_t ws_bytes,
+                  void* stream);
+
 /* 1 if this library was built with device-side bounds checks (the debug
  * build: UPIPE_DEBUG_BOUNDS), else 0.  In that build every plain (non-TMA)
  * global load and store of the kernels is checked against the extent of its

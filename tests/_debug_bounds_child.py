@@ -1,7 +1,7 @@
 """Child process of test_debug_bounds: run with UPIPE_DEBUG_BOUNDS=1 (and
 UPIPE_BWD_WALK=4, so that the backward also runs its split query walks), it
-loads the bounds-checked build of the library and runs every entry point on
-small shapes against the float64 oracle.  Each call must leave the device
+loads the bounds-checked build of the library and runs every entry point
+(attention and MLP) on small shapes against the float64 oracle.  Each call must leave the device
 error word clear (a failed bounds check would report UPIPE_ERR_BOUNDS) and
 the guard margins untouched.  Exits non-zero on any failure."""
 import os
@@ -60,6 +60,19 @@ def main():
                     for name in ("dq_gamma", "dk_gamma"):
                         assert_close(f64(g[name]), ref[name], f"{w.name} {name} ch={ch}",
                                      GAIN_MAX_REL, GAIN_MEAN_REL)
+    # the sequence-tiled MLP, forward and backward
+    from tests import test_parity_mlp as PM
+    from workloads import make_mlp_inputs
+    import oracle as O
+    for w in PM.SMALL:
+        inp = make_mlp_inputs(w, seed=0, with_grad=True)
+        t = {k: v.cuda() for k, v in inp.items()}
+        a = {k: f64(v) for k, v in inp.items()}
+        ref = O.mlp_backward(a["x"], a["Wg"], a["Wu"], a["Wd"], a["dy"])
+        assert_close(f64(PM.run_fwd(w, t)), ref["y"], f"{w.name} y")
+        g = PM.run_bwd(w, t)
+        for name in ("dx", "dWg", "dWu", "dWd"):
+            assert_close(f64(g[name]), ref[name], f"{w.name} {name}")
     print("debug bounds ok")
 
 

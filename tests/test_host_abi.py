@@ -183,3 +183,37 @@ def test_fused_forward_validates_before_any_launch(u):
     q[7] += 16
     assert call(sh, q, need) == 1                           # workspace not 256-byte aligned
     assert call(sh, p, need - 1) == 3                       # workspace too small
+
+
+def test_mlp_workspace_and_validation(u):
+    # the MLP's workspace is one tile's intermediates: a (bf16) forward, plus
+    # dA (fp32), dg and du (bf16) backward, of min(tile_rows, S) rows
+    al = lambda b: (b + 255) // 256 * 256
+    for S, hidden, ffn, tile in [(300, 256, 384, 128), (77, 128, 128, 256),
+                                 (1 << 17, 4096, 14336, 8192)]:
+        sh = u.MlpShape(S, hidden, ffn, tile)
+        T = min(tile, S)
+        assert u.mlp_workspace_bytes(sh, 0) == al(T * ffn * 2)
+        assert u.mlp_workspace_bytes(sh, 1) == al(T * ffn * 2) + al(T * ffn * 4) + 2 * al(T * ffn * 2)
+    for bad in [u.MlpShape(0, 256, 256, 128), u.MlpShape(100, 200, 256, 128),
+                u.MlpShape(100, 256, 200, 128), u.MlpShape(100, 256, 256, 100),
+                u.MlpShape(100, 256, 256, 0)]:
+        assert u.mlp_workspace_bytes(bad, 0) == 0
+    assert u.mlp_workspace_bytes(u.MlpShape(100, 256, 256, 128), 2) == 0
+    L = u.lib()
+    sh = u.MlpShape(300, 256, 384, 128)
+    p = [0x100000 + 0x1000 * i for i in range(12)]
+    need0, need1 = u.mlp_workspace_bytes(sh, 0), u.mlp_workspace_bytes(sh, 1)
+    fwd = lambda shape, q, n: L.upipe_mlp_fwd(ctypes.byref(shape), *q[:5], q[5], n, None)
+    assert fwd(sh, p, need0 - 1) == 3                              # workspace too small
+    assert fwd(u.MlpShape(300, 200, 384, 128), p, need0) == 2       # hidden % 128
+    q = list(p); q[0] = 0
+    assert fwd(sh, q, need0) == 1                                   # NULL x
+    q = list(p); q[4] += 8
+    assert fwd(sh, q, need0) == 1                                   # misaligned y
+    q = list(p); q[5] += 16
+    assert fwd(sh, q, need0) == 1                                   # workspace not 256-aligned
+    bwd = lambda q, n: L.upipe_mlp_bwd(ctypes.byref(sh), *q[:9], q[9], n, None)
+    assert bwd(p, need1 - 1) == 3
+    q = list(p); q[8] = 0
+    assert bwd(q, need1) == 1                                       # NULL dWd

@@ -136,6 +136,50 @@ def make_inputs(w: Workload, seed: int = 0, device: str = "cpu",
     return out
 
 
+@dataclasses.dataclass(frozen=True)
+class MlpWorkload:
+    """The decoder layer's SwiGLU MLP over S tokens, computed in tiles of
+    tile_rows tokens (the sequence-tiled MLP of the pages' memory stack)."""
+    name: str
+    S: int
+    hidden: int
+    ffn: int
+    tile_rows: int
+
+    def with_(self, **kw) -> "MlpWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+MLP_WORKLOADS = {
+    w.name: w
+    for w in [
+        # Llama-3-8B's MLP (hidden 4096, ffn 14336) on one rank of an 8-way
+        # Ulysses split of 1M tokens: the MLP is sequence-sharded, so a rank
+        # holds S/8 = 131072 tokens; tiles of 8192 tokens
+        MlpWorkload("llama3-8b-mlp-rank-s1m", S=1 << 17, hidden=4096, ffn=14336,
+                    tile_rows=8192),
+    ]
+}
+
+
+def make_mlp_inputs(w: MlpWorkload, seed: int = 0, device: str = "cpu",
+                    with_grad: bool = False):
+    """Draw the MLP's inputs: x [S, hidden] ~ N(0, 1); Wg, Wu [ffn, hidden]
+    ~ N(0, 1/hidden); Wd [hidden, ffn] ~ N(0, 1/ffn); dy [S, hidden] ~ N(0, 1)
+    when ``with_grad``; all bf16, drawn in that order."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    out = {
+        "x": _randn((w.S, w.hidden), 1.0, gen, device),
+        "Wg": _randn((w.ffn, w.hidden), w.hidden ** -0.5, gen, device),
+        "Wu": _randn((w.ffn, w.hidden), w.hidden ** -0.5, gen, device),
+        "Wd": _randn((w.hidden, w.ffn), w.ffn ** -0.5, gen, device),
+    }
+    if with_grad:
+        out["dy"] = _randn((w.S, w.hidden), 1.0, gen, device)
+    return out
+
+
 def sample_rows(S: int, n: int = 256, seed: int = 0, tile: int = 128):
     """Seeded sorted query rows: always 0, 1, tile-1, tile, S/2, S-1 and tile
     edges, the rest uniform; the same rows serve every head."""
