@@ -26,6 +26,10 @@ GPU): ``value`` is the sum of all ranks' FLOPs over the max-over-ranks time.
 ``--impl reference`` times the float64 CPU oracle (the only reference this
 method has) on a bounded sample of the same workload.
 
+``tiled_mlp`` (``--no-mlp`` skips it) times the sequence-tiled SwiGLU MLP
+(upipe_mlp_fwd / upipe_mlp_bwd) at Llama-3-8B widths on one rank's 131072
+tokens.
+
 ``fused_wo_forward`` (main and secondary workload; ``--no-fused`` skips it)
 times the forward whose attention kernel adds the Wo-slice partial results
 into out itself (upipe_attn_fwd_fused, no attention-output buffer) against
@@ -721,6 +725,69 @@ def measure(u, w, ch, mode, steps, warmup, dist, world, rank, dev, full=True, sw
     return res
 
 
+def measure_mlp(u, dev, dist, steps):
+    """The sequence-tiled SwiGLU MLP at its benchmark workload (Llama-3-8B
+    widths, one rank's share of 1M tokens, tiles of 8192): forward and
+    backward TFLOP/s over ``steps`` device-resident calls each, and the
+    workspace against the untiled intermediates."""
+    import torch
+    from workloads import MLP_WORKLOADS, make_mlp_inputs
+    w = MLP_WORKLOADS["llama3-8b-mlp-rank-s1m"]
+    t = make_mlp_inputs(w, seed=0, device=str(dev), with_grad=True)
+    sh = u.MlpShape(w.S, w.hidden, w.ffn, w.tile_rows)
+    wsb = {m: u.mlp_workspace_bytes(sh, m) for m in (0, 1)}
+    ws = torch.empty(wsb[1], dtype=torch.uint8, device=dev)
+    y = torch.empty(w.S, w.hidden, device=dev)
+    g = {n: torch.empty(shp, device=dev) for n, shp in
+         [("dx", (w.S, w.hidden)), ("dWg", (w.ffn, w.hidden)), ("dWu", (w.ffn, w.hidden)),
+          ("dWd", (w.hidden, w.ffn))]}
+
+    def fwd():
+        u.mlp_fwd(sh, t["x"], t["Wg"], t["Wu"], t["Wd"], y, ws)
+
+    def bwd():
+        u.mlp_bwd(sh, t["x"], t["Wg"], t["Wu"], t["Wd"], t["dy"], g["dx"], g["dWg"], g["dWu"],
+                  g["dWd"], ws)
+
+    for _ in range(3):
+        fwd()
+        bwd()
+    if u.last_error() != 0:
+        raise RuntimeError("device error in the MLP measurement")
+
+    def timed(fn, k):
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record()
+        for _ in range(k):
+            fn()
+        e0.record()
+        torch.cuda.synchronize()
+        return max_over_ranks(s0.elapsed_time(e0) / 1e3, dist, dev) / k
+
+    k = max(3, min(steps, 20))
+    shf = float(w.S) * w.hidden * w.ffn
+    tf, tb = timed(fwd, k), timed(bwd, k)
+    untiled = w.S * w.ffn * (2 + 4 + 2 + 2)   # a, dA, dg, du over the whole sequence
+    res = {"config": {"workload": w.name, "S": w.S, "hidden": w.hidden, "ffn": w.ffn,
+                      "tile_rows": w.tile_rows},
+           "steps": k,
+           "fwd_ms": round(1e3 * tf, 3), "bwd_ms": round(1e3 * tb, 3),
+           "fwd_tflops": round(6.0 * shf / tf / 1e12, 2),
+           "bwd_tflops": round(12.0 * shf / tb / 1e12, 2),
+           # the backward also recomputes the gate and up projections
+           "bwd_hardware_tflops": round(16.0 * shf / tb / 1e12, 2),
+           "workspace_gb": {"fwd": round(wsb[0] / 1e9, 4), "bwd": round(wsb[1] / 1e9, 4),
+                            "untiled_bwd": round(untiled / 1e9, 3)},
+           "note": "upipe_mlp_fwd/bwd: y = (silu(x Wg^T) * (x Wu^T)) Wd^T in tiles of "
+                   "tile_rows tokens; model FLOPs 6 S hidden ffn forward, 12 backward"}
+    del t, ws, y, g
+    torch.cuda.empty_cache()
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -736,6 +803,8 @@ def main():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-fused", action="store_true",
                     help="skip the fused Wo-slice forward comparison")
+    ap.add_argument("--no-mlp", action="store_true",
+                    help="skip the sequence-tiled MLP measurement")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the end-to-end and HBM-kernel measurements (profiling runs)")
     ap.add_argument("--seq-len", type=int, default=None,
@@ -788,6 +857,8 @@ def main():
                      "chunk_sweep": r2["sweep"], "paired_accumulate": r2.get("paired"),
                      "fused_wo_forward": r2.get("fused"), "clocks": r2["clocks"]}
 
+    mlp = None if args.no_mlp else measure_mlp(u, dev, dist, args.steps)
+
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -823,6 +894,7 @@ def main():
         "gpu_launches": r["launches_per_step"] * args.steps,
         "clocks": r["clocks"],
         "secondary": secondary,
+        "tiled_mlp": mlp,
     }
     if "cpu_baseline" in r:
         line["cpu_baseline"] = r["cpu_baseline"]

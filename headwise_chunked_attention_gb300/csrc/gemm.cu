@@ -80,14 +80,23 @@ struct GemmMaps {
   CUtensorMap c;
 };
 
+// Tile order: column tiles fastest (consecutive tiles share an A row block;
+// the B operand cycles), or with m_fastest row blocks fastest (consecutive
+// tiles share a B column tile; A cycles and should be the operand that stays
+// in L2).
 __device__ __forceinline__ TileCoord tile_coord(int t, int num_m, int num_n, int kb_total,
-                                                int ksplit, int tile_rows) {
+                                                int ksplit, int tile_rows, int m_fastest) {
   const int per_split = num_m * num_n;
   const int ks = t / per_split;
   const int r = t - ks * per_split;
   TileCoord c;
-  c.m0 = (r / num_n) * tile_rows;
-  c.n0 = (r % num_n);
+  if (m_fastest) {
+    c.m0 = (r % num_m) * tile_rows;
+    c.n0 = r / num_m;
+  } else {
+    c.m0 = (r / num_n) * tile_rows;
+    c.n0 = (r % num_n);
+  }
   const int kb_per = (kb_total + ksplit - 1) / ksplit;
   c.kb0 = ks * kb_per;
   c.kb1 = min(kb_total, c.kb0 + kb_per);
@@ -106,6 +115,14 @@ __device__ __forceinline__ void rope_cs(const float2* __restrict__ hi,
   const float2 b = __ldg(lo_t + (long long)i * 1024 + (pos & 1023));
   c = a.x * b.x - a.y * b.y;
   s = a.y * b.x + a.x * b.y;
+}
+
+// sigmoid(v) = 1 / (1 + e^-v) with the fast exponential and reciprocal
+// division; the exponent is clamped at 80 so that the divisor stays below
+// 2^126, where the fast division is exact to its error bound (for v < -80,
+// sigmoid(v) < 2e-35 either way)
+__device__ __forceinline__ float sigmoid_fast(float v) {
+  return __fdividef(1.f, 1.f + __expf(fminf(-v, 80.f)));
 }
 
 template <int D>
@@ -236,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t issued = 0, issued_phase = 0;  // per-stage bit masks
       bool ok = true;
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        const TileCoord tc = tile_coord(t, num_m, num_n, kb_total, ksplit, BM * MT);
+        const TileCoord tc = tile_coord(t, num_m, num_n, kb_total, ksplit, BM * MT, g.m_fastest);
         const int n0 = tc.n0 * BN;
         const CUtensorMap* am = &maps.a[0];
         const CUtensorMap* bm = &maps.b[0];
@@ -309,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++it) {
-        const TileCoord tc = tile_coord(t, num_m, num_n, kb_total, ksplit, BM * MT);
+        const TileCoord tc = tile_coord(t, num_m, num_n, kb_total, ksplit, BM * MT, g.m_fastest);
         const int acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
         if (!mbar_wait_warp(&acc_empty[acc], acc_phase ^ 1, err, abort_flag)) break;
@@ -349,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = 0;
     uint32_t epi_round = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
-      const TileCoord tc = tile_coord(t, num_m, num_n, kb_total, ksplit, BM * MT);
+      const TileCoord tc = tile_coord(t, num_m, num_n, kb_total, ksplit, BM * MT, g.m_fastest);
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
       // warp-uniform: the tcgen05.ld below is warp-collective
@@ -464,23 +481,28 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int j = 0; j < 4; ++j) {
                 const float g0 = __uint_as_float(rg[i + 2 * j]), g1 = __uint_as_float(rg[i + 2 * j + 1]);
                 const float u0 = __uint_as_float(ru[i + 2 * j]), u1 = __uint_as_float(ru[i + 2 * j + 1]);
-                // silu(v) = v / (1 + e^-v); e^-v = inf for v << 0 gives -0
-                wp[j] = pack_bf16(g0 / (1.f + __expf(-g0)) * u0, g1 / (1.f + __expf(-g1)) * u1);
+                wp[j] = pack_bf16(g0 * sigmoid_fast(g0) * u0, g1 * sigmoid_fast(g1) * u1);
               }
               *reinterpret_cast<uint4*>(ep.act + off_a + i) = w;
             }
           } else {
-            const float* dap = ep.dA + m * ep.ld_da + c0 + 32 * c;
+            const float4* dap =
+                reinterpret_cast<const float4*>(ep.dA + m * ep.ld_da + c0 + 32 * c);
             const long long off_g = m * ep.ld_dg + c0 + 32 * c;
+            // all 32 dA values of the chunk in flight at once (dA is read-only
+            // here: written by the previous launch)
+            float4 d4v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) d4v[q] = __ldg(dap + q);
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
-              const float4 d4 = *reinterpret_cast<const float4*>(dap + i);
+              const float4 d4 = d4v[i / 4];
               const float da[4] = {d4.x, d4.y, d4.z, d4.w};
               float vg[4], vu[4], va[4];
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
                 const float gv = __uint_as_float(rg[i + j]), uv = __uint_as_float(ru[i + j]);
-                const float sg = 1.f / (1.f + __expf(-gv));   // sigmoid(g)
+                const float sg = sigmoid_fast(gv);
                 const float sl = gv * sg;                      // silu(g)
                 vg[j] = da[j] * uv * (sg * (1.f + gv * (1.f - sg)));
                 vu[j] = da[j] * sl;

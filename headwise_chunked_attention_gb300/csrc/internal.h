@@ -196,6 +196,10 @@ struct GemmArgs {
   int mseg_t0[kMaxASegs + 1];
   int mseg_rows[kMaxASegs];
   int mseg_a[kMaxASegs];
+  // tile order: 0 column tiles fastest (the default: A row blocks are
+  // reused, B cycles), 1 row blocks fastest (B column tiles are reused and A
+  // cycles: the order for an A much smaller than B, which then stays in L2)
+  int m_fastest;
 };
 
 // a_mn / b_mn: operand stored MN-major (A as [K, M] row-major, B as [K, N]).

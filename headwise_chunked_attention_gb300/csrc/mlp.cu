@@ -108,6 +108,9 @@ int gate_up(const upipe_mlp_shape_t* sh, const bf16* x_rows, int64_t rows, const
   ep.dU = dU;
   ep.ld_dg = sh->ffn;
   GemmArgs ga{(int)rows, 2 * sh->ffn, sh->hidden, 1, 128};
+  // the x tile (A) is far smaller than Wg and Wu together (B): row blocks
+  // fastest keeps it in L2 and reads each weight tile once
+  ga.m_fastest = 1;
   MLP_CUDA(launch_gemm(256, false, false, epi, &xm, 1, bm, 2, ga, ep, err, sms, st));
   return UPIPE_OK;
 }
@@ -221,6 +224,7 @@ extern "C" int upipe_mlp_bwd(const upipe_mlp_shape_t* shape, const upipe_bf16* x
       ep.C = dA;
       ep.ldc = F;
       GemmArgs ga{(int)rows, F, H, 1, 128};
+      ga.m_fastest = 1;   // the dy tile (A) stays in L2, Wd (B) is read once
       MLP_CUDA(launch_gemm(da_bn, false, true, EPI_F32, &dym, 1, &wd_mn, 1, ga, ep, err, sms, st,
                            &dam));
     }
@@ -255,6 +259,7 @@ extern "C" int upipe_mlp_bwd(const upipe_mlp_shape_t* shape, const upipe_bf16* x
       ep.ldc = F;
       const int bn = (F % 256 == 0) ? 256 : 128;
       GemmArgs ga{H, F, (int)rows, wgrad_splits(rows, H, F, bn, sms), 128};
+      ga.m_fastest = 1;   // dy^T (A) stays in L2, a^T (B) is read once
       MLP_CUDA(launch_gemm(bn, true, true, EPI_F32_ATOMIC, &dy_mn, 1, &a_mn, 1, ga, ep, err, sms,
                            st));
     }
