@@ -1,5 +1,5 @@
-"""Float64 CPU oracle of the headwise-chunked causal GQA attention layer and
-of the sequence-tiled MLP around it.
+"""Float64 CPU oracle of the headwise-chunked causal GQA attention layer, and
+of the sequence-tiled MLP and loss around it.
 
 TEST INFRASTRUCTURE: only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
 baseline of ``bench.py`` use it.  It shares no code with the CUDA path and is
@@ -13,4 +13,7 @@ from .attention_layer import (  # noqa: F401
 )
 from .mlp import (  # noqa: F401
     mlp_backward, mlp_forward, mlp_loss, sigmoid, silu, silu_grad,
+)
+from .loss import (  # noqa: F401
+    logsumexp_rows, loss_backward, loss_forward, loss_total,
 )
