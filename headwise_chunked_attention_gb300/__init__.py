@@ -6,7 +6,8 @@ PyTorch only provides device memory and the current stream.  There is no CPU
 fallback: without the built library every call raises.
 """
 from ._binding import (  # noqa: F401
-    UpipeError, Shape, MlpShape, KernelTimer, mlp_workspace_bytes, mlp_fwd, mlp_bwd, attn_bwd, attn_fwd, attn_fwd_fused, last_error, lib, lib_path,
+    UpipeError, Shape, MlpShape, LossShape, KernelTimer, mlp_workspace_bytes, mlp_fwd, mlp_bwd,
+    loss_workspace_bytes, loss_fwd, loss_bwd, attn_bwd, attn_fwd, attn_fwd_fused, last_error, lib, lib_path,
     workspace_bytes, selftest_wait_timeout, selftest_bounds, debug_bounds, ERR_NAMES, ERR_DEVICE_TIMEOUT, ERR_RANGE, ERR_BOUNDS,
-    DEBUG_BOUNDS,
+    ERR_TARGET, DEBUG_BOUNDS,
 )

@@ -16,10 +16,12 @@ _lib = None
 
 ERR_NAMES = {0: "UPIPE_OK", 1: "UPIPE_ERR_INVALID_ARG", 2: "UPIPE_ERR_UNSUPPORTED",
              3: "UPIPE_ERR_WORKSPACE_TOO_SMALL", 4: "UPIPE_ERR_CUDA",
-             5: "UPIPE_ERR_DEVICE_TIMEOUT", 6: "UPIPE_ERR_RANGE", 7: "UPIPE_ERR_BOUNDS"}
+             5: "UPIPE_ERR_DEVICE_TIMEOUT", 6: "UPIPE_ERR_RANGE", 7: "UPIPE_ERR_BOUNDS",
+             8: "UPIPE_ERR_TARGET"}
 ERR_DEVICE_TIMEOUT = 5
 ERR_RANGE = 6
 ERR_BOUNDS = 7
+ERR_TARGET = 8
 
 
 class UpipeError(RuntimeError):
@@ -49,6 +51,12 @@ class MlpShape(ctypes.Structure):
     """upipe_mlp_shape_t: the sequence-tiled MLP's geometry."""
     _fields_ = [("S", ctypes.c_int64), ("hidden", ctypes.c_int32),
                 ("ffn", ctypes.c_int32), ("tile_rows", ctypes.c_int32)]
+
+
+class LossShape(ctypes.Structure):
+    """upipe_loss_shape_t: the sequence-tiled loss's geometry."""
+    _fields_ = [("S", ctypes.c_int64), ("hidden", ctypes.c_int32),
+                ("vocab", ctypes.c_int32), ("tile_rows", ctypes.c_int32)]
 
 
 def lib_path() -> str:
@@ -94,6 +102,13 @@ def lib():
         L.upipe_mlp_fwd.restype = ctypes.c_int
         L.upipe_mlp_bwd.argtypes = [ctypes.POINTER(MlpShape)] + [P] * 10 + [ctypes.c_size_t, P]
         L.upipe_mlp_bwd.restype = ctypes.c_int
+        L.upipe_loss_workspace_bytes.argtypes = [ctypes.POINTER(LossShape), ctypes.c_int]
+        L.upipe_loss_workspace_bytes.restype = ctypes.c_size_t
+        L.upipe_loss_fwd.argtypes = [ctypes.POINTER(LossShape)] + [P] * 6 + [ctypes.c_size_t, P]
+        L.upipe_loss_fwd.restype = ctypes.c_int
+        L.upipe_loss_bwd.argtypes = ([ctypes.POINTER(LossShape)] + [P] * 4 + [ctypes.c_float] +
+                                     [P] * 3 + [ctypes.c_size_t, P])
+        L.upipe_loss_bwd.restype = ctypes.c_int
         L.upipe_debug_bounds.argtypes = []
         L.upipe_debug_bounds.restype = ctypes.c_int
         L.upipe_selftest_bounds.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
@@ -244,6 +259,31 @@ def mlp_bwd(shape: MlpShape, x, Wg, Wu, Wd, dy, dx, dWg, dWu, dWd, workspace, st
         _ptr(dWu, f, "dWu"), _ptr(dWd, f, "dWd"), _ptr(workspace, None, "workspace"),
         workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "upipe_mlp_bwd")
+
+
+def loss_workspace_bytes(shape: LossShape, mode: int = 0) -> int:
+    return int(lib().upipe_loss_workspace_bytes(ctypes.byref(shape), mode))
+
+
+def loss_fwd(shape: LossShape, h, W, targets, loss_rows, lse, workspace, stream=None):
+    """upipe_loss_fwd: per-token losses and log-sum-exps (fp32), tile by tile."""
+    bf, f = torch.bfloat16, torch.float32
+    rc = lib().upipe_loss_fwd(
+        ctypes.byref(shape), _ptr(h, bf, "h"), _ptr(W, bf, "W"), _ptr(targets, torch.int32, "targets"),
+        _ptr(loss_rows, f, "loss_rows"), _ptr(lse, f, "lse"), _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "upipe_loss_fwd")
+
+
+def loss_bwd(shape: LossShape, h, W, targets, lse, scale, dh, dW, workspace, stream=None):
+    """upipe_loss_bwd: dh and dW (fp32) of scale * sum of the token losses."""
+    bf, f = torch.bfloat16, torch.float32
+    rc = lib().upipe_loss_bwd(
+        ctypes.byref(shape), _ptr(h, bf, "h"), _ptr(W, bf, "W"), _ptr(targets, torch.int32, "targets"),
+        _ptr(lse, f, "lse"), float(scale), _ptr(dh, f, "dh"), _ptr(dW, f, "dW"),
+        _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+    _check(rc, "upipe_loss_bwd")
 
 
 def debug_bounds() -> bool:

@@ -325,4 +325,53 @@ cudaError_t launch_grad_bound(const bf16* dout, long long S, int hidden, const b
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------ tiled loss rows --
+// The sequence-tiled loss: each row's log-sum-exp over the vocabulary from
+// the (max, sum of exp) partials of its column tiles (base 2, written by the
+// logits GEMM's epilogue), and the row's loss lse - z[target].  One warp per
+// row; lane l combines tiles l, l + 32, ...; a target outside [0, vocab)
+// gives a NaN loss and UPIPE_ERR_TARGET.
+__global__ void __launch_bounds__(256)
+    loss_rows_kernel(const float2* __restrict__ part, int ntiles, const float* __restrict__ zt,
+                     const int* __restrict__ targets, int vocab, long long rows,
+                     float* __restrict__ lse, float* __restrict__ loss, int* __restrict__ err) {
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= rows) return;   // warp-uniform
+  float mx = -INFINITY;
+  for (int j = lane; j < ntiles; j += 32)
+    if (dbg_in2(row, rows, j, j, ntiles, err)) mx = fmaxf(mx, part[row * ntiles + j].x);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  float sm = 0.f;
+  for (int j = lane; j < ntiles; j += 32) {
+    if (!dbg_in2(row, rows, j, j, ntiles, err)) continue;
+    const float2 p = part[row * ntiles + j];
+    sm += p.y * exp2f(p.x - mx);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, off);
+  if (lane == 0) {
+    const float l = (mx + log2f(sm)) * 0.69314718055994531f;
+    const int t = targets[row];
+    lse[row] = l;
+    if (t < 0 || t >= vocab) {
+      loss[row] = __int_as_float(0x7fc00000);   // NaN
+      atomicCAS(err, 0, kErrTarget);
+    } else {
+      loss[row] = l - zt[row];
+    }
+  }
+}
+
+cudaError_t launch_loss_rows(const float2* part, int ntiles, const float* zt, const int* targets,
+                             int vocab, long long rows, float* lse, float* loss,
+                             cudaStream_t stream, int* err) {
+  if (rows <= 0) return cudaSuccess;
+  const long long blocks = (rows + 7) / 8;
+  loss_rows_kernel<<<(unsigned)blocks, 256, 0, stream>>>(part, ntiles, zt, targets, vocab, rows,
+                                                          lse, loss, err);
+  return cudaGetLastError();
+}
+
 }  // namespace upipe

@@ -37,7 +37,11 @@
 //                   rows (two B maps, one 128-row TMA box each into one B
 //                   stage), and the epilogue stores a = silu(g) * u in bf16;
 //   EPI_SWIGLU_BWD  the same recomputed, with dA read for the tile and
-//                   dg = dA u silu'(g), du = dA silu(g) and a stored in bf16.
+//                   dg = dA u silu'(g), du = dA silu(g) and a stored in bf16;
+//   EPI_LSE_PART    the sequence-tiled loss's logits z = h W^T: per row and
+//                   vocabulary tile the (max, sum of exp) partial of the
+//                   log-sum-exp, and the target's logit; z is never stored;
+//   EPI_DLOGITS     the same recomputed: dz = scale (softmax - onehot), bf16.
 #include <algorithm>
 
 #include "internal.h"
@@ -517,6 +521,66 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+      } else if constexpr (EPI == EPI_LSE_PART) {
+        // the row's max and sum of exponentials over this column tile, base 2
+        constexpr float kL2E = 1.4426950408889634f;
+        const int jt = n0 / BN;
+        const int tcol = live ? __ldg(ep.targets + m) - n0 : -1;   // target in this tile?
+        float mx = -INFINITY, sm = 0.f, zt = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tbase + 32 * c, r);
+          tmem_ld_wait(r);
+          float cmax = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) cmax = fmaxf(cmax, __uint_as_float(r[i]));
+          const float mnew = fmaxf(mx, cmax * kL2E);
+          float cs = 0.f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) cs += ex2(fmaf(__uint_as_float(r[i]), kL2E, -mnew));
+          sm = sm * ex2(mx - mnew) + cs;
+          mx = mnew;
+          if (tcol >= 32 * c && tcol < 32 * c + 32) {
+            // the target's logit, picked without indexing the register array
+            // by a run-time value (which would move it to local memory)
+            const int k = tcol - 32 * c;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) zt = fmaf(i == k ? 1.f : 0.f, __uint_as_float(r[i]), zt);
+          }
+        }
+        if (live && dbg_in2(m, g.M, jt, jt, ep.ld_part, err))
+          ep.part[m * ep.ld_part + jt] = make_float2(mx, sm);
+        if (live && tcol >= 0 && tcol < BN && dbg_in(m, m, g.M, err)) ep.zt[m] = zt;
+      } else if constexpr (EPI == EPI_DLOGITS) {
+        // dz = scale (softmax - onehot) over this column tile, bf16
+        constexpr float kL2E = 1.4426950408889634f;
+        const bool row_ok = live && dbg_in2(m, g.M, n0, n0 + BN - 1, ep.ld_dz, err);
+        const int tcol = row_ok ? __ldg(ep.targets + m) - n0 : -1;
+        const float lse2 = row_ok ? __ldg(ep.lse_rows + m) * kL2E : 0.f;
+        const float sc = ep.loss_scale;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tbase + 32 * c, r);
+          tmem_ld_wait(r);
+          if (!row_ok) continue;
+          bf16* dp = ep.dz + m * ep.ld_dz + n0 + 32 * c;
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 w;
+            uint32_t* wp = &w.x;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int col = 32 * c + i + 2 * j;
+              const float p0 = ex2(fmaf(__uint_as_float(r[i + 2 * j]), kL2E, -lse2));
+              const float p1 = ex2(fmaf(__uint_as_float(r[i + 2 * j + 1]), kL2E, -lse2));
+              wp[j] = pack_bf16(sc * (p0 - (col == tcol ? 1.f : 0.f)),
+                                sc * (p1 - (col + 1 == tcol ? 1.f : 0.f)));
+            }
+            *reinterpret_cast<uint4*>(dp + i) = w;
+          }
+        }
       } else if constexpr (EPI == EPI_F32) {
         // [32 rows x 32 cols] fp32 blocks of this warp's rows, 128-byte
         // swizzled in shared memory, then one TMA store / reduce-add each
@@ -670,6 +734,11 @@ cudaError_t launch_gemm(int bn, bool a_mn, bool b_mn, EpiKind epi, const CUtenso
     return cudaErrorInvalidValue;
   UPIPE_GEMM_CASE(256, false, false, EPI_SWIGLU)
   UPIPE_GEMM_CASE(256, false, false, EPI_SWIGLU_BWD)
+  // the sequence-tiled loss's logits (vocabulary tiles of 256 or 128)
+  UPIPE_GEMM_CASE(256, false, false, EPI_LSE_PART)
+  UPIPE_GEMM_CASE(128, false, false, EPI_LSE_PART)
+  UPIPE_GEMM_CASE(256, false, false, EPI_DLOGITS)
+  UPIPE_GEMM_CASE(128, false, false, EPI_DLOGITS)
 #undef UPIPE_GEMM_CASE
   return cudaErrorNotSupported;
 }

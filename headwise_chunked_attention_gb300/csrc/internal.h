@@ -110,6 +110,8 @@ enum EpiKind : int {
   EPI_F32_ATOMIC = 3,  // fp32 reduction-add (split-K partial sums)
   EPI_SWIGLU = 4,      // MLP gate/up: a = silu(g) * u, bf16 store
   EPI_SWIGLU_BWD = 5,  // MLP gate/up recomputed: dg, du (from dA) and a, bf16 stores
+  EPI_LSE_PART = 6,    // loss logits: per row and column tile, (max, sum of exp) partials
+  EPI_DLOGITS = 7,     // loss logits recomputed: dz = scale (softmax - onehot), bf16 store
 };
 
 enum ProjMode : int { PROJ_PLAIN = 0, PROJ_ROPE = 1, PROJ_NORM_ROPE = 2 };
@@ -171,6 +173,20 @@ struct EpiParams {
   bf16* dG;
   bf16* dU;
   long long ld_dg;
+  // EPI_LSE_PART / EPI_DLOGITS (the tiled loss; N = vocabulary, z = logits):
+  // targets [M] int32 of the tile's rows.  EPI_LSE_PART stores, for row m and
+  // column tile j, part[m * ld_part + j] = (max_v z*log2e, sum_v 2^(z*log2e - max))
+  // over the tile's columns, and zt[m] = z[m, targets[m]] from the tile that
+  // holds the target.  EPI_DLOGITS reads lse_rows [M] (natural log) and stores
+  // dz[m, v] = loss_scale * (exp(z - lse) - [v == target]) in bf16.
+  const int* targets;
+  float2* part;
+  int ld_part;
+  float* zt;
+  const float* lse_rows;
+  bf16* dz;
+  long long ld_dz;
+  float loss_scale;
 };
 
 constexpr int kMaxASegs = 6;  // A tensor maps of one GEMM
@@ -303,6 +319,12 @@ cudaError_t launch_qk_bwd(const QkBwdArgs& a, cudaStream_t stream);
 // [S, ld_out] each, for ``cols`` columns: hi + lo carries ~16 significant bits.
 cudaError_t launch_f32_to_bf16x2(const float* in, int ld_in, bf16* hi, bf16* lo, int ld_out,
                                  long long S, int cols, cudaStream_t stream, int* err);
+
+// The tiled loss's per-row log-sum-exp (natural log) and loss lse - z[target]
+// from the logits GEMM's per-tile partials [rows][ntiles] and target logits.
+cudaError_t launch_loss_rows(const float2* part, int ntiles, const float* zt, const int* targets,
+                             int vocab, long long rows, float* lse, float* loss,
+                             cudaStream_t stream, int* err);
 
 // The current device's error word and SM count (created on first use).
 int device_context(int** err, int* num_sms);

@@ -15,6 +15,7 @@ namespace upipe {
 constexpr int kErrDeviceTimeout = 5;                         // UPIPE_ERR_DEVICE_TIMEOUT
 constexpr int kErrRange = 6;                                 // UPIPE_ERR_RANGE
 constexpr int kErrBounds = 7;                                // UPIPE_ERR_BOUNDS
+constexpr int kErrTarget = 8;                                // UPIPE_ERR_TARGET
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s per wait
 
 // Debug builds (compiled with UPIPE_DEBUG_BOUNDS): a bounds check of one plain

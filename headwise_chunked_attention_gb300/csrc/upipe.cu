@@ -1130,6 +1130,7 @@ extern "C" const char* upipe_strerror(int code) {
     case UPIPE_ERR_DEVICE_TIMEOUT: return "device wait timed out";
     case UPIPE_ERR_RANGE: return "projected value outside the fp16 range";
     case UPIPE_ERR_BOUNDS: return "device bounds check failed (debug build)";
+    case UPIPE_ERR_TARGET: return "loss target outside the vocabulary";
     default: return "unknown error";
   }
 }

@@ -90,9 +90,11 @@ enum {
   UPIPE_ERR_DEVICE_TIMEOUT = 5,       /* a kernel's bounded wait expired      */
   UPIPE_ERR_RANGE = 6,                /* a projected q, k or v value exceeds
                                          the fp16 range (|v| > 65504)        */
-  UPIPE_ERR_BOUNDS = 7                /* debug builds only: a device-side
+  UPIPE_ERR_BOUNDS = 7,               /* debug builds only: a device-side
                                          bounds check of a global access
                                          failed (the access was skipped)     */
+  UPIPE_ERR_TARGET = 8                /* a loss target id outside
+                                         [0, vocab) (its row's loss is NaN)  */
 };
 
 /* Workspace bytes needed by upipe_attn_fwd (mode 0) or upipe_attn_bwd
@@ -294,6 +296,48 @@ int upipe_mlp_bwd(const upipe_mlp_shape_t* shape, const upipe_bf16* x, const upi
                   float* dWg, float* dWu, float* dWd, void* workspace, size_t ws_bytes,
                   void* stream);
 
+/* ------------------------------------------------------------------------
+ * The sequence-tiled cross-entropy loss of the model's last layer (the
+ * pages' stack tiles the loss along the sequence, as it does the MLPs:
+ * memeeeeeex.com article, the stack section on Arctic sequence-length
+ * training).  With logits z = h W^T over a vocabulary of V words,
+ *     lse_i = log sum_v exp(z_iv),   loss_i = lse_i - z_i[t_i]
+ * computed over tiles of tile_rows tokens: the [tile_rows, V] logits are
+ * never stored in the forward (the logits GEMM's epilogue reduces them to
+ * per-row partials); the backward recomputes them per tile.
+ *   S, hidden, tile_rows as for the MLP; vocab a multiple of 128
+ * Layouts: h [S, hidden] bf16; W [vocab, hidden] bf16 (nn.Linear);
+ * targets [S] int32 in [0, vocab); loss_rows, lse [S] fp32 (natural log);
+ * dh [S, hidden] fp32; dW [vocab, hidden] fp32.  dz is held in bf16 per
+ * tile; every contraction accumulates in fp32.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  int64_t S;
+  int32_t hidden, vocab, tile_rows;
+} upipe_loss_shape_t;
+
+/* Workspace bytes of upipe_loss_fwd (mode 0: one tile's per-row partials,
+ * tile x vocab/256 (or /128) float2, and target logits) or upipe_loss_bwd
+ * (mode 1: one tile's dz, tile x vocab bf16), or 0 for an invalid shape or
+ * mode.  Pure host function. */
+size_t upipe_loss_workspace_bytes(const upipe_loss_shape_t* shape, int mode);
+
+/* Per-token losses and log-sum-exps, tile by tile (both overwritten).  A
+ * target outside [0, vocab) gives its row a NaN loss and UPIPE_ERR_TARGET
+ * through upipe_last_error().
+ * Returns UPIPE_OK or an error code (nothing launched on error). */
+int upipe_loss_fwd(const upipe_loss_shape_t* shape, const upipe_bf16* h, const upipe_bf16* W,
+                   const int32_t* targets, float* loss_rows, float* lse, void* workspace,
+                   size_t ws_bytes, void* stream);
+
+/* Gradients of L = scale * sum_i loss_i (scale = 1/S for the mean) given the
+ * forward's lse: dh (overwritten, row by row) and dW (zeroed, then
+ * accumulated over the tiles with fp32 reduce-adds in no fixed order).
+ * Returns UPIPE_OK or an error code (nothing launched on error). */
+int upipe_loss_bwd(const upipe_loss_shape_t* shape, const upipe_bf16* h, const upipe_bf16* W,
+                   const int32_t* targets, const float* lse, float scale, float* dh, float* dW,
+                   void* workspace, size_t ws_bytes, void* stream);
+
 /* 1 if this library was built with device-side bounds checks (the debug
  * build: UPIPE_DEBUG_BOUNDS), else 0.  In that build every plain (non-TMA)
  * global load and store of the kernels is checked against the extent of its
@@ -314,9 +358,10 @@ int upipe_debug_bounds(void);
 int upipe_selftest_bounds(void* stream, int* written);
 
 /* Synchronises the current device, then returns and clears the device error
- * word (UPIPE_OK, UPIPE_ERR_DEVICE_TIMEOUT, UPIPE_ERR_RANGE or, in the debug
- * build, UPIPE_ERR_BOUNDS: the first error a kernel recorded since the last
- * call), or UPIPE_ERR_CUDA if the device reports a CUDA error. */
+ * word (UPIPE_OK, UPIPE_ERR_DEVICE_TIMEOUT, UPIPE_ERR_RANGE, UPIPE_ERR_TARGET
+ * or, in the debug build, UPIPE_ERR_BOUNDS: the first error a kernel recorded
+ * since the last call), or UPIPE_ERR_CUDA if the device reports a CUDA
+ * error. */
 int upipe_last_error(void);
 
 /* Static description of an error code. */

@@ -1,7 +1,7 @@
 """Child process of test_debug_bounds: run with UPIPE_DEBUG_BOUNDS=1 (and
 UPIPE_BWD_WALK=4, so that the backward also runs its split query walks), it
 loads the bounds-checked build of the library and runs every entry point
-(attention and MLP) on small shapes against the float64 oracle.  Each call must leave the device
+(attention, MLP and loss) on small shapes against the float64 oracle.  Each call must leave the device
 error word clear (a failed bounds check would report UPIPE_ERR_BOUNDS) and
 the guard margins untouched.  Exits non-zero on any failure."""
 import os
@@ -73,6 +73,10 @@ def main():
         g = PM.run_bwd(w, t)
         for name in ("dx", "dWg", "dWu", "dWd"):
             assert_close(f64(g[name]), ref[name], f"{w.name} {name}")
+    # the sequence-tiled loss, forward and backward
+    from tests import test_parity_loss as PL
+    for w in PL.SMALL:
+        PL.test_loss_matches_oracle(w)
     print("debug bounds ok")
 
 

@@ -217,3 +217,34 @@ def test_mlp_workspace_and_validation(u):
     assert bwd(p, need1 - 1) == 3
     q = list(p); q[8] = 0
     assert bwd(q, need1) == 1                                       # NULL dWd
+
+
+def test_loss_workspace_and_validation(u):
+    # forward: one tile's per-row partials (vocab / 256 or / 128 float2) and
+    # target logits; backward: one tile's dz in bf16
+    al = lambda b: (b + 255) // 256 * 256
+    for S, hidden, vocab, tile in [(300, 256, 1024, 128), (77, 128, 384, 256),
+                                   (1 << 17, 4096, 128256, 4096)]:
+        sh = u.LossShape(S, hidden, vocab, tile)
+        T = min(tile, S)
+        bn = 256 if vocab % 256 == 0 else 128
+        assert u.loss_workspace_bytes(sh, 0) == al(T * (vocab // bn) * 8) + al(T * 4)
+        assert u.loss_workspace_bytes(sh, 1) == al(T * vocab * 2)
+    for bad in [u.LossShape(0, 256, 256, 128), u.LossShape(100, 200, 256, 128),
+                u.LossShape(100, 256, 200, 128), u.LossShape(100, 256, 256, 64)]:
+        assert u.loss_workspace_bytes(bad, 0) == 0
+    L = u.lib()
+    sh = u.LossShape(300, 256, 1024, 128)
+    p = [0x100000 + 0x1000 * i for i in range(12)]
+    need0, need1 = u.loss_workspace_bytes(sh, 0), u.loss_workspace_bytes(sh, 1)
+    fwd = lambda q, n: L.upipe_loss_fwd(ctypes.byref(sh), *q[:5], q[5], n, None)
+    assert fwd(p, need0 - 1) == 3
+    q = list(p); q[2] = 0
+    assert fwd(q, need0) == 1                                       # NULL targets
+    q = list(p); q[3] += 4
+    assert fwd(q, need0) == 1                                       # misaligned loss_rows
+    bwd = lambda q, n: L.upipe_loss_bwd(ctypes.byref(sh), *q[:4], 1.0, q[4], q[5], q[6], n, None)
+    assert bwd(p, need1 - 1) == 3
+    q = list(p); q[5] = 0
+    assert bwd(q, need1) == 1                                       # NULL dW
+    assert L.upipe_strerror(8) == b"loss target outside the vocabulary"

@@ -92,7 +92,8 @@ def test_mlp_rows_do_not_depend_on_the_tile_size():
         g = run_bwd(w, t)
         assert torch.equal(g["dx"], g0["dx"]), tile
         for name in ("dWg", "dWu", "dWd"):
-            assert_close(f64(g[name]), f64(g0[name]), f"{name} tile={tile}", 1e-5, 1e-6)
+            # fp32 reduce-adds over a different number of tiles: summation order
+            assert_close(f64(g[name]), f64(g0[name]), f"{name} tile={tile}", 1e-4, 1e-5)
 
 
 def test_mlp_full_size_sampled_rows():

@@ -180,6 +180,46 @@ def make_mlp_inputs(w: MlpWorkload, seed: int = 0, device: str = "cpu",
     return out
 
 
+@dataclasses.dataclass(frozen=True)
+class LossWorkload:
+    """The last layer's cross-entropy loss over a vocabulary of ``vocab`` words
+    for S tokens, computed in tiles of tile_rows tokens."""
+    name: str
+    S: int
+    hidden: int
+    vocab: int
+    tile_rows: int
+
+    def with_(self, **kw) -> "LossWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+LOSS_WORKLOADS = {
+    w.name: w
+    for w in [
+        # Llama-3-8B's output projection (hidden 4096, vocabulary 128256) on
+        # one rank's 131072 tokens (1M over an 8-way split); tiles of 4096
+        LossWorkload("llama3-8b-loss-rank-s1m", S=1 << 17, hidden=4096, vocab=128256,
+                     tile_rows=4096),
+    ]
+}
+
+
+def make_loss_inputs(w: LossWorkload, seed: int = 0, device: str = "cpu"):
+    """Draw the loss's inputs: h [S, hidden] ~ N(0, 1), W [vocab, hidden]
+    ~ N(0, 1/hidden) (bf16), and targets [S] int32 uniform over the
+    vocabulary, in that order."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    out = {
+        "h": _randn((w.S, w.hidden), 1.0, gen, device),
+        "W": _randn((w.vocab, w.hidden), w.hidden ** -0.5, gen, device),
+    }
+    out["targets"] = torch.randint(0, w.vocab, (w.S,), generator=gen, device=device,
+                                   dtype=torch.int32)
+    return out
+
+
 def sample_rows(S: int, n: int = 256, seed: int = 0, tile: int = 128):
     """Seeded sorted query rows: always 0, 1, tile-1, tile, S/2, S-1 and tile
     edges, the rest uniform; the same rows serve every head."""
