@@ -26,9 +26,10 @@ GPU): ``value`` is the sum of all ranks' FLOPs over the max-over-ranks time.
 ``--impl reference`` times the float64 CPU oracle (the only reference this
 method has) on a bounded sample of the same workload.
 
-``tiled_mlp`` (``--no-mlp`` skips it) times the sequence-tiled SwiGLU MLP
-(upipe_mlp_fwd / upipe_mlp_bwd) at Llama-3-8B widths on one rank's 131072
-tokens.
+``tiled_mlp`` and ``tiled_loss`` (``--no-mlp`` skips both) time the
+sequence-tiled SwiGLU MLP (upipe_mlp_fwd / upipe_mlp_bwd) and cross-entropy
+loss (upipe_loss_fwd / upipe_loss_bwd) at Llama-3-8B widths on one rank's
+131072 tokens.
 
 ``fused_wo_forward`` (main and secondary workload; ``--no-fused`` skips it)
 times the forward whose attention kernel adds the Wo-slice partial results
@@ -788,6 +789,67 @@ def measure_mlp(u, dev, dist, steps):
     return res
 
 
+def measure_loss(u, dev, dist, steps):
+    """The sequence-tiled cross-entropy loss at its benchmark workload
+    (Llama-3-8B's vocabulary of 128256, one rank's 131072 tokens, tiles of
+    4096): forward and backward TFLOP/s over device-resident calls, and the
+    workspace against the untiled logits."""
+    import torch
+    from workloads import LOSS_WORKLOADS, make_loss_inputs
+    w = LOSS_WORKLOADS["llama3-8b-loss-rank-s1m"]
+    t = make_loss_inputs(w, seed=0, device=str(dev))
+    sh = u.LossShape(w.S, w.hidden, w.vocab, w.tile_rows)
+    wsb = {m: u.loss_workspace_bytes(sh, m) for m in (0, 1)}
+    ws = torch.empty(max(wsb.values()), dtype=torch.uint8, device=dev)
+    loss = torch.empty(w.S, device=dev)
+    lse = torch.empty(w.S, device=dev)
+    dh = torch.empty(w.S, w.hidden, device=dev)
+    dW = torch.empty(w.vocab, w.hidden, device=dev)
+
+    def fwd():
+        u.loss_fwd(sh, t["h"], t["W"], t["targets"], loss, lse, ws)
+
+    def bwd():
+        u.loss_bwd(sh, t["h"], t["W"], t["targets"], lse, 1.0 / w.S, dh, dW, ws)
+
+    for _ in range(3):
+        fwd()
+        bwd()
+    if u.last_error() != 0:
+        raise RuntimeError("device error in the loss measurement")
+
+    def timed(fn, k):
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record()
+        for _ in range(k):
+            fn()
+        e0.record()
+        torch.cuda.synchronize()
+        return max_over_ranks(s0.elapsed_time(e0) / 1e3, dist, dev) / k
+
+    k = max(3, min(steps, 10))
+    f = 2.0 * w.S * w.hidden * w.vocab
+    tf, tb = timed(fwd, k), timed(bwd, k)
+    res = {"config": {"workload": w.name, "S": w.S, "hidden": w.hidden, "vocab": w.vocab,
+                      "tile_rows": w.tile_rows},
+           "steps": k, "mean_loss": round(float(loss.mean()), 4),
+           "fwd_ms": round(1e3 * tf, 3), "bwd_ms": round(1e3 * tb, 3),
+           "fwd_tflops": round(f / tf / 1e12, 2),
+           "bwd_tflops": round(2.0 * f / tb / 1e12, 2),
+           # the backward also recomputes the logits
+           "bwd_hardware_tflops": round(3.0 * f / tb / 1e12, 2),
+           "workspace_gb": {"fwd": round(wsb[0] / 1e9, 4), "bwd": round(wsb[1] / 1e9, 4),
+                            "untiled_logits_fp32": round(w.S * w.vocab * 4 / 1e9, 2)},
+           "note": "upipe_loss_fwd/bwd: cross entropy over the vocabulary in tiles of tile_rows "
+                   "tokens; model FLOPs 2 S hidden vocab forward, 4 backward"}
+    del t, ws, loss, lse, dh, dW
+    torch.cuda.empty_cache()
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -804,7 +866,7 @@ def main():
     ap.add_argument("--no-fused", action="store_true",
                     help="skip the fused Wo-slice forward comparison")
     ap.add_argument("--no-mlp", action="store_true",
-                    help="skip the sequence-tiled MLP measurement")
+                    help="skip the sequence-tiled MLP and loss measurements")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the end-to-end and HBM-kernel measurements (profiling runs)")
     ap.add_argument("--seq-len", type=int, default=None,
@@ -858,6 +920,7 @@ def main():
                      "fused_wo_forward": r2.get("fused"), "clocks": r2["clocks"]}
 
     mlp = None if args.no_mlp else measure_mlp(u, dev, dist, args.steps)
+    loss_line = None if args.no_mlp else measure_loss(u, dev, dist, args.steps)
 
     if rank != 0:
         if dist is not None:
@@ -895,6 +958,7 @@ def main():
         "clocks": r["clocks"],
         "secondary": secondary,
         "tiled_mlp": mlp,
+        "tiled_loss": loss_line,
     }
     if "cpu_baseline" in r:
         line["cpu_baseline"] = r["cpu_baseline"]
