@@ -26,10 +26,11 @@ GPU): ``value`` is the sum of all ranks' FLOPs over the max-over-ranks time.
 ``--impl reference`` times the float64 CPU oracle (the only reference this
 method has) on a bounded sample of the same workload.
 
-``tiled_mlp`` and ``tiled_loss`` (``--no-mlp`` skips both) time the
-sequence-tiled SwiGLU MLP (upipe_mlp_fwd / upipe_mlp_bwd) and cross-entropy
-loss (upipe_loss_fwd / upipe_loss_bwd) at Llama-3-8B widths on one rank's
-131072 tokens.
+``tiled_mlp`` and ``tiled_loss`` (``--no-mlp`` skips them and ``offload``)
+time the sequence-tiled SwiGLU MLP (upipe_mlp_fwd / upipe_mlp_bwd) and
+cross-entropy loss (upipe_loss_fwd / upipe_loss_bwd) at Llama-3-8B widths on
+one rank's 131072 tokens; ``offload`` times the layer forward with its input
+offloaded to host memory and an input-sized buffer prefetched beside it.
 
 ``fused_wo_forward`` (main and secondary workload; ``--no-fused`` skips it)
 times the forward whose attention kernel adds the Wo-slice partial results
@@ -850,6 +851,70 @@ def measure_loss(u, dev, dist, steps):
     return res
 
 
+def measure_offload(u, w, ch, dev, dist):
+    """The offload of block inputs beside compute: the layer forward of ``w``
+    timed alone, and with an offload of its input x to page-locked host
+    memory and a prefetch of an x-sized buffer back running on the library's
+    copy stream during each forward (joined at the step's end); plus each
+    copy alone."""
+    import torch
+    from workloads import make_inputs
+    t = make_inputs(w, seed=0, device=str(dev))
+    sh = u.Shape.of(w, ch)
+    ws = torch.empty(u.workspace_bytes(sh, 0), dtype=torch.uint8, device=dev)
+    out = torch.empty(w.S, w.hidden, device=dev)
+    lse = torch.empty(w.Hq, w.S, device=dev)
+    host_out = torch.empty(t["x"].shape, dtype=torch.bfloat16).pin_memory()
+    host_in = torch.empty(t["x"].shape, dtype=torch.bfloat16).pin_memory()
+    back = torch.empty_like(t["x"])
+    nbytes = t["x"].numel() * t["x"].element_size()
+
+    def fwd():
+        u.attn_fwd(sh, t["x"], t["Wq"], t["Wk"], t["Wv"], t["Wo"], out, lse, ws,
+                   t.get("q_gamma"), t.get("k_gamma"))
+
+    def fwd_with_copies():
+        a = u.offload(t["x"], host_out)
+        b = u.prefetch(host_in, back)
+        fwd()
+        u.copy_join(a)
+        u.copy_join(b)
+
+    def timed(fn, k):
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record()
+        for _ in range(k):
+            fn()
+        e0.record()
+        torch.cuda.synchronize()
+        return max_over_ranks(s0.elapsed_time(e0) / 1e3, dist, dev) / k
+
+    for _ in range(2):
+        fwd_with_copies()
+    if u.last_error() != 0:
+        raise RuntimeError("device error in the offload measurement")
+    k = 3
+    t_alone = timed(fwd, k)
+    t_copies = timed(fwd_with_copies, k)
+    t_off = timed(lambda: u.copy_join(u.offload(t["x"], host_out)), 2)
+    t_pre = timed(lambda: u.copy_join(u.prefetch(host_in, back)), 2)
+    flops = layer_flops(w, "fwd")[0]
+    res = {"config": {"workload": w.name, "chunk_heads": ch, "pass": "fwd"},
+           "bytes_each_way": nbytes, "steps": k,
+           "layer_tflops_alone": round(flops / t_alone / 1e12, 2),
+           "layer_tflops_with_copies": round(flops / t_copies / 1e12, 2),
+           "offload_gbs_alone": round(nbytes / t_off / 1e9, 1),
+           "prefetch_gbs_alone": round(nbytes / t_pre / 1e9, 1),
+           "note": "upipe_offload / upipe_prefetch of a block input (x) beside the layer forward "
+                   "on the library's copy stream; the host link is shared with other jobs"}
+    del t, ws, out, lse, host_out, host_in, back
+    torch.cuda.empty_cache()
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -866,7 +931,7 @@ def main():
     ap.add_argument("--no-fused", action="store_true",
                     help="skip the fused Wo-slice forward comparison")
     ap.add_argument("--no-mlp", action="store_true",
-                    help="skip the sequence-tiled MLP and loss measurements")
+                    help="skip the sequence-tiled MLP, loss and offload measurements")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the end-to-end and HBM-kernel measurements (profiling runs)")
     ap.add_argument("--seq-len", type=int, default=None,
@@ -921,6 +986,7 @@ def main():
 
     mlp = None if args.no_mlp else measure_mlp(u, dev, dist, args.steps)
     loss_line = None if args.no_mlp else measure_loss(u, dev, dist, args.steps)
+    offload_line = None if args.no_mlp else measure_offload(u, w, ch, dev, dist)
 
     if rank != 0:
         if dist is not None:
@@ -959,6 +1025,7 @@ def main():
         "secondary": secondary,
         "tiled_mlp": mlp,
         "tiled_loss": loss_line,
+        "offload": offload_line,
     }
     if "cpu_baseline" in r:
         line["cpu_baseline"] = r["cpu_baseline"]

@@ -109,6 +109,12 @@ def lib():
         L.upipe_loss_bwd.argtypes = ([ctypes.POINTER(LossShape)] + [P] * 4 + [ctypes.c_float] +
                                      [P] * 3 + [ctypes.c_size_t, P])
         L.upipe_loss_bwd.restype = ctypes.c_int
+        for name in ("upipe_offload", "upipe_prefetch"):
+            fn = getattr(L, name)
+            fn.argtypes = [P, P, ctypes.c_size_t, P, ctypes.POINTER(ctypes.c_void_p)]
+            fn.restype = ctypes.c_int
+        L.upipe_copy_join.argtypes = [P, P]
+        L.upipe_copy_join.restype = ctypes.c_int
         L.upipe_debug_bounds.argtypes = []
         L.upipe_debug_bounds.restype = ctypes.c_int
         L.upipe_selftest_bounds.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
@@ -284,6 +290,39 @@ def loss_bwd(shape: LossShape, h, W, targets, lse, scale, dh, dW, workspace, str
         _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
         _stream(stream))
     _check(rc, "upipe_loss_bwd")
+
+
+def offload(dev_src, host_dst, stream=None):
+    """upipe_offload: copy a CUDA tensor into a page-locked CPU tensor of the
+    same size on the library's copy stream; returns the ticket to join."""
+    if not dev_src.is_cuda or host_dst.is_cuda or not host_dst.is_pinned():
+        raise ValueError("offload: a CUDA source and a pinned CPU destination")
+    n = dev_src.numel() * dev_src.element_size()
+    if host_dst.numel() * host_dst.element_size() != n:
+        raise ValueError("offload: sizes differ")
+    t = ctypes.c_void_p()
+    _check(lib().upipe_offload(dev_src.data_ptr(), host_dst.data_ptr(), n, _stream(stream),
+                               ctypes.byref(t)), "upipe_offload")
+    return t.value
+
+
+def prefetch(host_src, dev_dst, stream=None):
+    """upipe_prefetch: copy a page-locked CPU tensor into a CUDA tensor of the
+    same size on the library's copy stream; returns the ticket to join."""
+    if not dev_dst.is_cuda or host_src.is_cuda or not host_src.is_pinned():
+        raise ValueError("prefetch: a pinned CPU source and a CUDA destination")
+    n = dev_dst.numel() * dev_dst.element_size()
+    if host_src.numel() * host_src.element_size() != n:
+        raise ValueError("prefetch: sizes differ")
+    t = ctypes.c_void_p()
+    _check(lib().upipe_prefetch(host_src.data_ptr(), dev_dst.data_ptr(), n, _stream(stream),
+                                ctypes.byref(t)), "upipe_prefetch")
+    return t.value
+
+
+def copy_join(ticket, stream=None):
+    """upipe_copy_join: the stream (default: current) waits for the copy."""
+    _check(lib().upipe_copy_join(ticket, _stream(stream)), "upipe_copy_join")
 
 
 def debug_bounds() -> bool:

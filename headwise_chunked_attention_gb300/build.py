@@ -25,7 +25,7 @@ OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libupipe.so")
 OUT_DEBUG = os.path.join(PKG, "_build_debug")
 SOURCES = ["upipe.cu", "gemm.cu", "attn_fwd.cu", "attn_bwd.cu", "elementwise.cu", "noalloc.cu",
-           "selftest.cu", "mlp.cu", "loss.cu"]
+           "selftest.cu", "mlp.cu", "loss.cu", "offload.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

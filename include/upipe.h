@@ -338,6 +338,30 @@ int upipe_loss_bwd(const upipe_loss_shape_t* shape, const upipe_bf16* h, const u
                    const int32_t* targets, const float* lse, float scale, float* dh, float* dW,
                    void* workspace, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Offload of block inputs to host memory and their prefetch back (the pages'
+ * CPU-offload step: a transformer block's input leaves the GPU while it is
+ * not needed and is prefetched before the backward reaches that block, the
+ * copies running under compute; memeeeeeex.com article, the stack section on
+ * CPU offload).  Each call enqueues one asynchronous copy on a library-owned
+ * copy stream of the current device (created by the first call), ordered
+ * after everything enqueued on ``stream`` so far, and returns a ticket;
+ * upipe_copy_join(ticket, consumer_stream) makes the consumer's stream wait
+ * for the copy and releases the ticket (every ticket must be joined once).
+ *   dev_src / dev_dst   device memory of the current device
+ *   host_dst / host_src page-locked host memory (cudaHostAlloc or
+ *                       cudaHostRegister; pageable memory is refused: its
+ *                       copies would not run asynchronously)
+ *   bytes               > 0
+ * The caller must not touch the source or destination until the copy is
+ * joined.  Returns UPIPE_OK, UPIPE_ERR_INVALID_ARG (a NULL pointer, zero
+ * bytes, or memory of the wrong kind; nothing enqueued) or UPIPE_ERR_CUDA.
+ * ------------------------------------------------------------------------ */
+int upipe_offload(const void* dev_src, void* host_dst, size_t bytes, void* stream, void** ticket);
+int upipe_prefetch(const void* host_src, void* dev_dst, size_t bytes, void* stream,
+                   void** ticket);
+int upipe_copy_join(void* ticket, void* stream);
+
 /* 1 if this library was built with device-side bounds checks (the debug
  * build: UPIPE_DEBUG_BOUNDS), else 0.  In that build every plain (non-TMA)
  * global load and store of the kernels is checked against the extent of its

@@ -248,3 +248,14 @@ def test_loss_workspace_and_validation(u):
     q = list(p); q[5] = 0
     assert bwd(q, need1) == 1                                       # NULL dW
     assert L.upipe_strerror(8) == b"loss target outside the vocabulary"
+
+
+def test_offload_validates_before_enqueueing(u):
+    # NULL pointers, zero bytes and a missing ticket are refused on the host
+    L = u.lib()
+    t = ctypes.c_void_p(1)
+    assert L.upipe_offload(0x100000, 0x200000, 64, None, None) == 1
+    assert L.upipe_offload(None, 0x200000, 64, None, ctypes.byref(t)) == 1 and t.value is None
+    assert L.upipe_prefetch(0x100000, None, 64, None, ctypes.byref(t)) == 1
+    assert L.upipe_offload(0x100000, 0x200000, 0, None, ctypes.byref(t)) == 1
+    assert L.upipe_copy_join(None, None) == 1
