@@ -32,9 +32,10 @@
  *    one launch sequence on ``stream``.  Two calls in flight at once must not
  *    share a workspace.
  *  - Ownership: the caller owns every buffer.  The library allocates no device
- *    or host memory of its own (upipe_attn_fwd creates only the one stream per
- *    device named above and three events per call); all temporaries live in
- *    ``workspace``.
+ *    or host memory of its own: upipe_attn_fwd creates only the one stream per
+ *    device named above and three events per call, upipe_offload /
+ *    upipe_prefetch one copy stream per device and two events per copy (one
+ *    released by upipe_copy_join); all temporaries live in ``workspace``.
  *  - Errors: every argument is validated on the host before the first launch;
  *    a failed check returns a code and launches nothing.  A device-side wait
  *    that exceeds its time limit, or a projected value outside the fp16 range,
