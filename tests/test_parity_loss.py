@@ -134,3 +134,21 @@ def test_loss_full_size_sampled_rows():
     assert np.abs(f64(loss[idx]) - ref["loss_rows"]).max() <= LSE_ABS
     gref = O.loss_backward(h, W, tg, scale)
     assert_close(f64(dh[idx]), gref["dh"], "dh rows")
+
+
+def test_loss_weight_gradient_at_full_vocabulary():
+    # Llama-3's vocabulary (128256) and width (4096) on 1500 tokens in tiles
+    # of 512 (three tiles, the last one ragged): dW and dh in full against the
+    # whole float64 backward
+    w = LossWorkload("loss-vocab-s1500", S=1500, hidden=4096, vocab=128256, tile_rows=512)
+    inp = make_loss_inputs(w, seed=6)
+    t = {k: v.cuda() for k, v in inp.items()}
+    loss, lse = run_fwd(w, t)
+    scale = 1.0 / w.S
+    dh, dW = run_bwd(w, t, lse, scale)
+    h, W, tg = f64(inp["h"]), f64(inp["W"]), inp["targets"].numpy()
+    ref = O.loss_forward(h, W, tg)
+    assert np.abs(f64(loss) - ref["loss_rows"]).max() <= LSE_ABS
+    gref = O.loss_backward(h, W, tg, scale)
+    assert_close(f64(dh), gref["dh"], "dh at full vocabulary")
+    assert_close(f64(dW), gref["dW"], "dW at full vocabulary")

@@ -114,3 +114,17 @@ def test_mlp_full_size_sampled_rows():
     ref = O.mlp_backward(f64(t["x"][idx]), a["Wg"], a["Wu"], a["Wd"], f64(t["dy"][idx]))
     assert_close(y, ref["y"], "y rows")
     assert_close(dx, ref["dx"], "dx rows")
+
+
+def test_mlp_weight_gradients_at_full_widths():
+    # Llama-3-8B's MLP widths (hidden 4096, ffn 14336) on 3000 tokens in tiles
+    # of 1024 (three tiles, the last one ragged): every gradient in full,
+    # against the whole float64 backward
+    w = MlpWorkload("mlp-widths-s3000", S=3000, hidden=4096, ffn=14336, tile_rows=1024)
+    inp = make_mlp_inputs(w, seed=5, with_grad=True)
+    t = {k: v.cuda() for k, v in inp.items()}
+    g = run_bwd(w, t)
+    a = {k: f64(v) for k, v in inp.items()}
+    ref = O.mlp_backward(a["x"], a["Wg"], a["Wu"], a["Wd"], a["dy"])
+    for name in ("dx", "dWg", "dWu", "dWd"):
+        assert_close(f64(g[name]), ref[name], f"{name} at full widths")
