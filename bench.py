@@ -986,7 +986,9 @@ def main():
 
     mlp = None if args.no_mlp else measure_mlp(u, dev, dist, args.steps)
     loss_line = None if args.no_mlp else measure_loss(u, dev, dist, args.steps)
-    offload_line = None if args.no_mlp else measure_offload(u, w, ch, dev, dist)
+    # one process only: each copy pins an input-sized host buffer (8.6 GB at
+    # the default workload), which N ranks on one node would multiply
+    offload_line = None if (args.no_mlp or world > 1) else measure_offload(u, w, ch, dev, dist)
 
     if rank != 0:
         if dist is not None:
