@@ -487,17 +487,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float u0 = __uint_as_float(ru[i + 2 * j]), u1 = __uint_as_float(ru[i + 2 * j + 1]);
                 wp[j] = pack_bf16(g0 * sigmoid_fast(g0) * u0, g1 * sigmoid_fast(g1) * u1);
               }
-              *reinterpret_cast<uint4*>(ep.act + off_a + i) = w;
+              // streaming store: a is read once, by the next GEMM; it must not
+              // push the x tile (the A operand every tile re-reads) out of L2
+              __stcs(reinterpret_cast<uint4*>(ep.act + off_a + i), w);
             }
           } else {
             const float4* dap =
                 reinterpret_cast<const float4*>(ep.dA + m * ep.ld_da + c0 + 32 * c);
             const long long off_g = m * ep.ld_dg + c0 + 32 * c;
-            // all 32 dA values of the chunk in flight at once (dA is read-only
-            // here: written by the previous launch)
+            // all 32 dA values of the chunk in flight at once, read as a
+            // stream (each value once): with the three streaming stores below
+            // this keeps the x tile, which every tile of the launch re-reads,
+            // resident in L2
             float4 d4v[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) d4v[q] = __ldg(dap + q);
+            for (int q = 0; q < 8; ++q) d4v[q] = __ldcs(dap + q);
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
               const float4 d4 = d4v[i / 4];
@@ -512,12 +516,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 vu[j] = da[j] * sl;
                 va[j] = sl * uv;
               }
-              *reinterpret_cast<uint2*>(ep.dG + off_g + i) =
-                  make_uint2(pack_bf16(vg[0], vg[1]), pack_bf16(vg[2], vg[3]));
-              *reinterpret_cast<uint2*>(ep.dU + off_g + i) =
-                  make_uint2(pack_bf16(vu[0], vu[1]), pack_bf16(vu[2], vu[3]));
-              *reinterpret_cast<uint2*>(ep.act + off_a + i) =
-                  make_uint2(pack_bf16(va[0], va[1]), pack_bf16(va[2], va[3]));
+              __stcs(reinterpret_cast<uint2*>(ep.dG + off_g + i),
+                     make_uint2(pack_bf16(vg[0], vg[1]), pack_bf16(vg[2], vg[3])));
+              __stcs(reinterpret_cast<uint2*>(ep.dU + off_g + i),
+                     make_uint2(pack_bf16(vu[0], vu[1]), pack_bf16(vu[2], vu[3])));
+              __stcs(reinterpret_cast<uint2*>(ep.act + off_a + i),
+                     make_uint2(pack_bf16(va[0], va[1]), pack_bf16(va[2], va[3])));
             }
           }
         }
@@ -578,7 +582,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               wp[j] = pack_bf16(sc * (p0 - (col == tcol ? 1.f : 0.f)),
                                 sc * (p1 - (col + 1 == tcol ? 1.f : 0.f)));
             }
-            *reinterpret_cast<uint4*>(dp + i) = w;
+            // streaming store: dz (tile x vocabulary) would otherwise push the
+            // h tile out of L2
+            __stcs(reinterpret_cast<uint4*>(dp + i), w);
           }
         }
       } else if constexpr (EPI == EPI_F32) {
