@@ -85,16 +85,26 @@ struct GemmMaps {
 };
 
 // Tile order: column tiles fastest (consecutive tiles share an A row block;
-// the B operand cycles), or with m_fastest row blocks fastest (consecutive
-// tiles share a B column tile; A cycles and should be the operand that stays
-// in L2).
+// the B operand cycles), or with m_fastest = 1 row blocks fastest
+// (consecutive tiles share a B column tile; A cycles and should be the
+// operand that stays in L2), or with m_fastest = G > 1 the same within groups
+// of G row blocks, group after group (B is read once per group, and only a
+// group's A rows cycle).
 __device__ __forceinline__ TileCoord tile_coord(int t, int num_m, int num_n, int kb_total,
                                                 int ksplit, int tile_rows, int m_fastest) {
   const int per_split = num_m * num_n;
   const int ks = t / per_split;
   const int r = t - ks * per_split;
   TileCoord c;
-  if (m_fastest) {
+  if (m_fastest > 1) {
+    // groups of m_fastest row blocks: within a group row blocks fastest, then
+    // columns, then the next group (only a group's A rows need stay in L2)
+    const int group = r / (m_fastest * num_n);
+    const int rem = r - group * m_fastest * num_n;
+    const int gm = min(m_fastest, num_m - group * m_fastest);
+    c.m0 = (group * m_fastest + rem % gm) * tile_rows;
+    c.n0 = rem / gm;
+  } else if (m_fastest) {
     c.m0 = (r % num_m) * tile_rows;
     c.n0 = r / num_m;
   } else {

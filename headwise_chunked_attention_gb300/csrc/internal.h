@@ -214,7 +214,9 @@ struct GemmArgs {
   int mseg_a[kMaxASegs];
   // tile order: 0 column tiles fastest (the default: A row blocks are
   // reused, B cycles), 1 row blocks fastest (B column tiles are reused and A
-  // cycles: the order for an A much smaller than B, which then stays in L2)
+  // cycles: the order for an A much smaller than B, which then stays in L2),
+  // G > 1 row blocks fastest within groups of G row blocks (B read once per
+  // group; for an A too large to stay in L2 as a whole)
   int m_fastest;
 };
 

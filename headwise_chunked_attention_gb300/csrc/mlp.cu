@@ -109,8 +109,9 @@ int gate_up(const upipe_mlp_shape_t* sh, const bf16* x_rows, int64_t rows, const
   ep.ld_dg = sh->ffn;
   GemmArgs ga{(int)rows, 2 * sh->ffn, sh->hidden, 1, 128};
   // the x tile (A) is far smaller than Wg and Wu together (B): row blocks
-  // fastest keeps it in L2 and reads each weight tile once
-  ga.m_fastest = 1;
+  // fastest, in groups of 16 (2 MB of x per 128-row block at hidden 4096:
+  // a group stays in L2 while the columns are swept)
+  ga.m_fastest = 16;
   MLP_CUDA(launch_gemm(256, false, false, epi, &xm, 1, bm, 2, ga, ep, err, sms, st));
   return UPIPE_OK;
 }
@@ -224,7 +225,7 @@ extern "C" int upipe_mlp_bwd(const upipe_mlp_shape_t* shape, const upipe_bf16* x
       ep.C = dA;
       ep.ldc = F;
       GemmArgs ga{(int)rows, F, H, 1, 128};
-      ga.m_fastest = 1;   // the dy tile (A) stays in L2, Wd (B) is read once
+      ga.m_fastest = 16;  // groups of 16 dy row blocks stay in L2 while Wd (B) is swept
       MLP_CUDA(launch_gemm(da_bn, false, true, EPI_F32, &dym, 1, &wd_mn, 1, ga, ep, err, sms, st,
                            &dam));
     }
