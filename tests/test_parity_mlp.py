@@ -65,6 +65,10 @@ SMALL = [
     MlpWorkload("mlp-s77", S=77, hidden=128, ffn=128, tile_rows=256),
     # wider: 256-wide output tiles of y and dx, two split-K partitions
     MlpWorkload("mlp-s2500", S=2500, hidden=512, ffn=1024, tile_rows=1024),
+    # 18 row blocks in the first tile: the gate/up and dA GEMMs' grouped tile
+    # order runs a full group of 16 row blocks, then a partial group of 2;
+    # the second tile (296 rows) is ragged
+    MlpWorkload("mlp-s2600-groups", S=2600, hidden=256, ffn=384, tile_rows=2304),
 ]
 
 
