@@ -31,7 +31,9 @@
 //                   read-modify-write runs in L2, the SM never reads out);
 //   EPI_DO          dO_c = dOut Wo_c, scaled and stored in fp16 (and, given
 //                   O, D = rowsum(dO * O) per head);
-//   EPI_F32_ATOMIC  split-K weight gradients, reduced with red.global.add;
+//   EPI_F32_ATOMIC  split-K weight gradients, reduced with red.global.add
+//                   after a transpose through shared memory (whole
+//                   128-byte row segments per instruction);
 //   EPI_SWIGLU      the sequence-tiled MLP's gate and up projections: each
 //                   256-wide output tile is 128 gate rows and the same 128 up
 //                   rows (two B maps, one 128-row TMA box each into one B
@@ -625,31 +627,54 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        float* crow;
-        bool row_live;
-        if (g.nmseg > 0) {  // the segment holding this row, and the row within it
+        // [32 rows x 32 cols] fp32 blocks of this warp's rows go through its
+        // shared-memory buffer (128-byte swizzled) and are reduce-added back
+        // by rows: lanes 8j..8j+7 cover one row's 128 contiguous bytes, so an
+        // instruction adds 4 whole row segments instead of 16-byte pieces of
+        // 32 rows.  Lane l adds column chunk q = l & 7 of rows 4k + (l >> 3).
+        uint8_t* buf = smem + Cfg::EPI_OFF + quarter * kEpiBufs * EPI_BUF_BYTES;
+        const int q = lane & 7;
+        const int r_lane = lane >> 3;
+        // the rows of this warp's 32 start at warp_row0 (tile-local row index
+        // quarter * 32 within the 128-row part); with M segments the tile's
+        // segment holds them all, and rows are counted within it
+        const long long warp_row0 = (long long)m0t + quarter * 32;
+        float* cbase;
+        long long row0, row_end;   // first row of the warp, one past the last live row
+        if (g.nmseg > 0) {
           const int mtile = m0t / BM;
           int s = 0;
           while (s + 1 < g.nmseg && mtile >= g.mseg_t0[s + 1]) ++s;
-          const long long ml = m - (long long)g.mseg_t0[s] * BM;
-          row_live = (tc.kb1 > tc.kb0) && ml < g.mseg_rows[s] &&
-                     dbg_in2(ml, g.mseg_rows[s], n0, n0 + BN - 1, g.N, err);
-          crow = ep.mseg_c[s] + (row_live ? ml * ep.ldc : 0);
+          cbase = ep.mseg_c[s];
+          row0 = warp_row0 - (long long)g.mseg_t0[s] * BM;
+          row_end = g.mseg_rows[s];
         } else {
-          row_live = live && dbg_in2(m, g.M, n0, n0 + BN - 1, g.N, err);
-          crow = ep.C + (row_live ? m * ep.ldc : 0);
+          cbase = ep.C;
+          row0 = warp_row0;
+          row_end = g.M;
         }
+        const bool tile_live = (tc.kb1 > tc.kb0) && row0 < row_end;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t r[32];
           tmem_ld32(tbase + c * 32, r);
           tmem_ld_wait(r);
-          if (row_live) {
-            float* cp = crow + n0 + c * 32;
+          if (!tile_live) continue;   // warp-uniform
+          __syncwarp();               // the previous block's reads of buf are done
 #pragma unroll
-            for (int i = 0; i < 32; i += 4)
-              red_add_v4_f32(cp + i, __uint_as_float(r[i]), __uint_as_float(r[i + 1]),
-                             __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+          for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<uint4*>(buf + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+                make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int rr = 4 * k + r_lane;   // row within the warp's 32
+            const long long row = row0 + rr;
+            if (row < row_end && dbg_in2(row, row_end, n0, n0 + BN - 1, g.N, err)) {
+              const uint4 v = *reinterpret_cast<const uint4*>(buf + rr * 128 + ((q ^ (rr & 7)) << 4));
+              red_add_v4_f32(cbase + row * ep.ldc + n0 + 32 * c + 4 * q, __uint_as_float(v.x),
+                             __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
+            }
           }
         }
       }
