@@ -470,15 +470,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ep.O && dbg_in2(head, g.N / D, m, m, g.M, err)) ep.D[(long long)head * g.M + m] = dot;
           atomic_max_nonneg(ep.do_max, sqrtf(ss));
         }
-      } else if constexpr (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) {
+      } else if constexpr (EPI == EPI_SWIGLU) {
         // accumulator columns [0, 128): g, [128, 256): u of output columns
         // [c0, c0 + 128) of this row
         constexpr int H = BN / 2;
         const long long c0 = n0 / 2;
-        bool row_ok = live && dbg_in2(m, g.M, c0, c0 + H - 1, ep.ld_act, err);
-        if constexpr (EPI == EPI_SWIGLU_BWD)
-          row_ok = row_ok && dbg_in2(m, g.M, c0, c0 + H - 1, ep.ld_da, err) &&
-                   dbg_in2(m, g.M, c0, c0 + H - 1, ep.ld_dg, err);
+        const bool row_ok = live && dbg_in2(m, g.M, c0, c0 + H - 1, ep.ld_act, err);
 #pragma unroll 1
         for (int c = 0; c < H / 32; ++c) {
           uint32_t rg[32], ru[32];
@@ -488,52 +485,118 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait(ru);
           if (!row_ok) continue;
           const long long off_a = m * ep.ld_act + c0 + 32 * c;
-          if constexpr (EPI == EPI_SWIGLU) {
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-              uint4 w;
-              uint32_t* wp = &w.x;
+          for (int i = 0; i < 32; i += 8) {
+            uint4 w;
+            uint32_t* wp = &w.x;
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const float g0 = __uint_as_float(rg[i + 2 * j]), g1 = __uint_as_float(rg[i + 2 * j + 1]);
-                const float u0 = __uint_as_float(ru[i + 2 * j]), u1 = __uint_as_float(ru[i + 2 * j + 1]);
-                wp[j] = pack_bf16(g0 * sigmoid_fast(g0) * u0, g1 * sigmoid_fast(g1) * u1);
-              }
-              // streaming store: a is read once, by the next GEMM; it must not
-              // push the x tile (the A operand every tile re-reads) out of L2
-              __stcs(reinterpret_cast<uint4*>(ep.act + off_a + i), w);
+            for (int j = 0; j < 4; ++j) {
+              const float g0 = __uint_as_float(rg[i + 2 * j]), g1 = __uint_as_float(rg[i + 2 * j + 1]);
+              const float u0 = __uint_as_float(ru[i + 2 * j]), u1 = __uint_as_float(ru[i + 2 * j + 1]);
+              wp[j] = pack_bf16(g0 * sigmoid_fast(g0) * u0, g1 * sigmoid_fast(g1) * u1);
             }
-          } else {
-            const float4* dap =
-                reinterpret_cast<const float4*>(ep.dA + m * ep.ld_da + c0 + 32 * c);
-            const long long off_g = m * ep.ld_dg + c0 + 32 * c;
-            // all 32 dA values of the chunk in flight at once, read as a
-            // stream (each value once): with the three streaming stores below
-            // this keeps the x tile, which every tile of the launch re-reads,
-            // resident in L2
-            float4 d4v[8];
+            // streaming store: a is read once, by the next GEMM; it must not
+            // push the x tile (the A operand every tile re-reads) out of L2
+            __stcs(reinterpret_cast<uint4*>(ep.act + off_a + i), w);
+          }
+        }
+      } else if constexpr (EPI == EPI_SWIGLU_BWD) {
+        // The same accumulator layout.  dA comes in and dg, du and a go out
+        // through this warp's two shared-memory buffers, so that every global
+        // access is a whole row segment: the [32 rows x 32 cols] fp32 block of
+        // dA arrives 4 rows x 128 bytes per instruction (lane: row 4k + l/8,
+        // 16-byte chunk l%8) into buf0, 128-byte swizzled, and each thread
+        // takes its own row; the three [32 x 32] bf16 outputs (64 bytes a row,
+        // 16-byte chunks swizzled by row pair) leave 8 rows x 64 bytes per
+        // instruction (lane: row 8k + l/4, chunk l%4).  dg and du are staged
+        // in buf1, a in buf0 once dA has been read out of it.
+        constexpr int H = BN / 2;
+        const long long c0 = n0 / 2;
+        uint8_t* buf0 = smem + Cfg::EPI_OFF + quarter * kEpiBufs * EPI_BUF_BYTES;
+        uint8_t* buf1 = buf0 + EPI_BUF_BYTES;
+        const long long wrow0 = (long long)m0t + quarter * 32;   // first row of this warp
+        const bool warp_live = (tc.kb1 > tc.kb0) && wrow0 < g.M;
+        const int lq = lane & 7, lr = lane >> 3;   // dA loads
+        const int sq = lane & 3, sr = lane >> 2;   // output stores
+        const int pr = (lane >> 1) & 3;            // this thread's row-pair swizzle
+#pragma unroll 1
+        for (int c = 0; c < H / 32; ++c) {
+          uint32_t rg[32], ru[32];
+          tmem_ld32(tbase + 32 * c, rg);
+          tmem_ld_wait(rg);
+          tmem_ld32(tbase + H + 32 * c, ru);
+          tmem_ld_wait(ru);
+          if (!warp_live) continue;   // warp-uniform
+          const long long col = c0 + 32 * c;   // first output column of the block
+          __syncwarp();   // the previous block's reads of buf0 and buf1 are done
+          {
+            // all 8 loads in flight at once; dA is read once (streaming)
+            float4 v[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) d4v[q] = __ldcs(dap + q);
+            for (int k = 0; k < 8; ++k) {
+              const long long row = wrow0 + 4 * k + lr;
+              v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (row < g.M && dbg_in2(row, g.M, col, col + 31, ep.ld_da, err))
+                v[k] = __ldcs(reinterpret_cast<const float4*>(ep.dA + row * ep.ld_da + col) + lq);
+            }
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              const float4 d4 = d4v[i / 4];
-              const float da[4] = {d4.x, d4.y, d4.z, d4.w};
-              float vg[4], vu[4], va[4];
+            for (int k = 0; k < 8; ++k) {
+              const int rr = 4 * k + lr;
+              *reinterpret_cast<float4*>(buf0 + rr * 128 + ((lq ^ (rr & 7)) << 4)) = v[k];
+            }
+          }
+          __syncwarp();
+          float da[32];
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const float gv = __uint_as_float(rg[i + j]), uv = __uint_as_float(ru[i + j]);
+          for (int k = 0; k < 8; ++k) {
+            const float4 d4 =
+                *reinterpret_cast<const float4*>(buf0 + lane * 128 + ((k ^ (lane & 7)) << 4));
+            da[4 * k] = d4.x;
+            da[4 * k + 1] = d4.y;
+            da[4 * k + 2] = d4.z;
+            da[4 * k + 3] = d4.w;
+          }
+          __syncwarp();   // every row of dA is out of buf0 before a goes in
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {   // columns 8j..8j+7: one 16-byte chunk of each output
+            uint32_t wg[4], wu[4], wa[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float og[2], ou[2], oa[2];
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int i = 8 * j + 2 * e + h;
+                const float gv = __uint_as_float(rg[i]), uv = __uint_as_float(ru[i]);
                 const float sg = sigmoid_fast(gv);
                 const float sl = gv * sg;                      // silu(g)
-                vg[j] = da[j] * uv * (sg * (1.f + gv * (1.f - sg)));
-                vu[j] = da[j] * sl;
-                va[j] = sl * uv;
+                og[h] = da[i] * uv * (sg * (1.f + gv * (1.f - sg)));
+                ou[h] = da[i] * sl;
+                oa[h] = sl * uv;
               }
-              __stcs(reinterpret_cast<uint2*>(ep.dG + off_g + i),
-                     make_uint2(pack_bf16(vg[0], vg[1]), pack_bf16(vg[2], vg[3])));
-              __stcs(reinterpret_cast<uint2*>(ep.dU + off_g + i),
-                     make_uint2(pack_bf16(vu[0], vu[1]), pack_bf16(vu[2], vu[3])));
-              __stcs(reinterpret_cast<uint2*>(ep.act + off_a + i),
-                     make_uint2(pack_bf16(va[0], va[1]), pack_bf16(va[2], va[3])));
+              wg[e] = pack_bf16(og[0], og[1]);
+              wu[e] = pack_bf16(ou[0], ou[1]);
+              wa[e] = pack_bf16(oa[0], oa[1]);
+            }
+            const uint32_t off = lane * 64 + ((j ^ pr) << 4);
+            *reinterpret_cast<uint4*>(buf1 + off) = make_uint4(wg[0], wg[1], wg[2], wg[3]);
+            *reinterpret_cast<uint4*>(buf1 + 2048 + off) = make_uint4(wu[0], wu[1], wu[2], wu[3]);
+            *reinterpret_cast<uint4*>(buf0 + off) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+          }
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int rr = 8 * k + sr;
+            const long long row = wrow0 + rr;
+            if (row < g.M && dbg_in2(row, g.M, col, col + 31, ep.ld_dg, err) &&
+                dbg_in2(row, g.M, col, col + 31, ep.ld_act, err)) {
+              const uint32_t off = rr * 64 + ((sq ^ ((rr >> 1) & 3)) << 4);
+              const long long og = row * ep.ld_dg + col + 8 * sq;
+              // streaming stores: each output is read once, by a later GEMM
+              __stcs(reinterpret_cast<uint4*>(ep.dG + og), *reinterpret_cast<const uint4*>(buf1 + off));
+              __stcs(reinterpret_cast<uint4*>(ep.dU + og),
+                     *reinterpret_cast<const uint4*>(buf1 + 2048 + off));
+              __stcs(reinterpret_cast<uint4*>(ep.act + row * ep.ld_act + col + 8 * sq),
+                     *reinterpret_cast<const uint4*>(buf0 + off));
             }
           }
         }
