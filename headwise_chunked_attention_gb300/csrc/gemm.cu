@@ -141,6 +141,33 @@ __device__ __forceinline__ float sigmoid_fast(float v) {
   return __fdividef(1.f, 1.f + __expf(fminf(-v, 80.f)));
 }
 
+// Stores a warp's [32 rows x 32 cols] bf16 block, held one row per thread as
+// four 16-byte chunks w[0..3], through ``buf`` (2 KB of this warp's shared
+// memory): each instruction then writes 8 whole 64-byte row segments (lane:
+// row 8k + l/4, chunk l%4) instead of 16-byte pieces of 32 rows.  Chunks are
+// swizzled by row pair, which keeps both the row-per-thread writes and the
+// row-segment reads free of bank conflicts.  Rows at or past ``rows`` are not
+// stored.
+__device__ __forceinline__ void warp_store_rows_bf16(uint8_t* buf, int lane, const uint4 (&w)[4],
+                                                     bf16* dst, long long ld, long long row0,
+                                                     long long rows, long long col, int* err) {
+  __syncwarp();   // the previous block's reads of buf are done
+  const int pr = (lane >> 1) & 3;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(buf + lane * 64 + ((j ^ pr) << 4)) = w[j];
+  __syncwarp();
+  const int sq = lane & 3, sr = lane >> 2;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int rr = 8 * k + sr;
+    const long long row = row0 + rr;
+    // streaming store: the block is read once, by a later GEMM
+    if (row < rows && dbg_in2(row, rows, col, col + 31, ld, err))
+      __stcs(reinterpret_cast<uint4*>(dst + row * ld + col + 8 * sq),
+             *reinterpret_cast<const uint4*>(buf + rr * 64 + ((sq ^ ((rr >> 1) & 3)) << 4)));
+  }
+}
+
 template <int D>
 __device__ __forceinline__ void epi_proj_row(const EpiParams& ep, const ProjSeg& sg, long long m,
                                              long long M, int n_local, float (&v)[D], int* err) {
@@ -472,10 +499,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else if constexpr (EPI == EPI_SWIGLU) {
         // accumulator columns [0, 128): g, [128, 256): u of output columns
-        // [c0, c0 + 128) of this row
+        // [c0, c0 + 128) of this row; a = silu(g) u leaves through shared
+        // memory as whole row segments
         constexpr int H = BN / 2;
         const long long c0 = n0 / 2;
-        const bool row_ok = live && dbg_in2(m, g.M, c0, c0 + H - 1, ep.ld_act, err);
+        uint8_t* buf0 = smem + Cfg::EPI_OFF + quarter * kEpiBufs * EPI_BUF_BYTES;
+        const long long wrow0 = (long long)m0t + quarter * 32;   // first row of this warp
+        const bool warp_live = (tc.kb1 > tc.kb0) && wrow0 < g.M;
 #pragma unroll 1
         for (int c = 0; c < H / 32; ++c) {
           uint32_t rg[32], ru[32];
@@ -483,22 +513,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait(rg);
           tmem_ld32(tbase + H + 32 * c, ru);
           tmem_ld_wait(ru);
-          if (!row_ok) continue;
-          const long long off_a = m * ep.ld_act + c0 + 32 * c;
+          if (!warp_live) continue;   // warp-uniform
+          uint4 w[4];
 #pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            uint4 w;
-            uint32_t* wp = &w.x;
+          for (int q = 0; q < 4; ++q) {
+            uint32_t* wp = &w[q].x;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const float g0 = __uint_as_float(rg[i + 2 * j]), g1 = __uint_as_float(rg[i + 2 * j + 1]);
-              const float u0 = __uint_as_float(ru[i + 2 * j]), u1 = __uint_as_float(ru[i + 2 * j + 1]);
+              const int i = 8 * q + 2 * j;
+              const float g0 = __uint_as_float(rg[i]), g1 = __uint_as_float(rg[i + 1]);
+              const float u0 = __uint_as_float(ru[i]), u1 = __uint_as_float(ru[i + 1]);
               wp[j] = pack_bf16(g0 * sigmoid_fast(g0) * u0, g1 * sigmoid_fast(g1) * u1);
             }
-            // streaming store: a is read once, by the next GEMM; it must not
-            // push the x tile (the A operand every tile re-reads) out of L2
-            __stcs(reinterpret_cast<uint4*>(ep.act + off_a + i), w);
           }
+          warp_store_rows_bf16(buf0, lane, w, ep.act, ep.ld_act, wrow0, g.M, c0 + 32 * c, err);
         }
       } else if constexpr (EPI == EPI_SWIGLU_BWD) {
         // The same accumulator layout.  dA comes in and dg, du and a go out
@@ -632,35 +660,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           ep.part[m * ep.ld_part + jt] = make_float2(mx, sm);
         if (live && tcol >= 0 && tcol < BN && dbg_in(m, m, g.M, err)) ep.zt[m] = zt;
       } else if constexpr (EPI == EPI_DLOGITS) {
-        // dz = scale (softmax - onehot) over this column tile, bf16
+        // dz = scale (softmax - onehot) over this column tile, bf16, leaving
+        // through shared memory as whole row segments
         constexpr float kL2E = 1.4426950408889634f;
-        const bool row_ok = live && dbg_in2(m, g.M, n0, n0 + BN - 1, ep.ld_dz, err);
-        const int tcol = row_ok ? __ldg(ep.targets + m) - n0 : -1;
-        const float lse2 = row_ok ? __ldg(ep.lse_rows + m) * kL2E : 0.f;
+        uint8_t* buf0 = smem + Cfg::EPI_OFF + quarter * kEpiBufs * EPI_BUF_BYTES;
+        const long long wrow0 = (long long)m0t + quarter * 32;   // first row of this warp
+        const bool warp_live = (tc.kb1 > tc.kb0) && wrow0 < g.M;
+        const int tcol = live ? __ldg(ep.targets + m) - n0 : -1;
+        const float lse2 = live ? __ldg(ep.lse_rows + m) * kL2E : 0.f;
         const float sc = ep.loss_scale;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t r[32];
           tmem_ld32(tbase + 32 * c, r);
           tmem_ld_wait(r);
-          if (!row_ok) continue;
-          bf16* dp = ep.dz + m * ep.ld_dz + n0 + 32 * c;
+          if (!warp_live) continue;   // warp-uniform
+          uint4 w[4];
 #pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            uint4 w;
-            uint32_t* wp = &w.x;
+          for (int q = 0; q < 4; ++q) {
+            uint32_t* wp = &w[q].x;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const int col = 32 * c + i + 2 * j;
-              const float p0 = ex2(fmaf(__uint_as_float(r[i + 2 * j]), kL2E, -lse2));
-              const float p1 = ex2(fmaf(__uint_as_float(r[i + 2 * j + 1]), kL2E, -lse2));
+              const int i = 8 * q + 2 * j;
+              const int col = 32 * c + i;
+              const float p0 = ex2(fmaf(__uint_as_float(r[i]), kL2E, -lse2));
+              const float p1 = ex2(fmaf(__uint_as_float(r[i + 1]), kL2E, -lse2));
               wp[j] = pack_bf16(sc * (p0 - (col == tcol ? 1.f : 0.f)),
                                 sc * (p1 - (col + 1 == tcol ? 1.f : 0.f)));
             }
-            // streaming store: dz (tile x vocabulary) would otherwise push the
-            // h tile out of L2
-            __stcs(reinterpret_cast<uint4*>(dp + i), w);
           }
+          // dz (tile x vocabulary) is stored streaming, so that it does not
+          // push the h tile out of L2
+          warp_store_rows_bf16(buf0, lane, w, ep.dz, ep.ld_dz, wrow0, g.M, n0 + 32 * c, err);
         }
       } else if constexpr (EPI == EPI_F32) {
         // [32 rows x 32 cols] fp32 blocks of this warp's rows, 128-byte
