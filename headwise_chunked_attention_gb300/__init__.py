@@ -8,6 +8,6 @@ fallback: without the built library every call raises.
 from ._binding import (  # noqa: F401
     UpipeError, Shape, MlpShape, LossShape, KernelTimer, mlp_workspace_bytes, mlp_fwd, mlp_bwd,
     loss_workspace_bytes, loss_fwd, loss_bwd, offload, prefetch, copy_join, attn_bwd, attn_fwd, attn_fwd_fused, last_error, lib, lib_path,
-    workspace_bytes, selftest_wait_timeout, selftest_bounds, debug_bounds, ERR_NAMES, ERR_DEVICE_TIMEOUT, ERR_RANGE, ERR_BOUNDS,
+    workspace_bytes, selftest_wait_timeout, selftest_bounds, debug_bounds, gemm_tile_order, ERR_NAMES, ERR_DEVICE_TIMEOUT, ERR_RANGE, ERR_BOUNDS,
     ERR_TARGET, DEBUG_BOUNDS,
 )

@@ -119,6 +119,9 @@ def lib():
         L.upipe_debug_bounds.restype = ctypes.c_int
         L.upipe_selftest_bounds.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
         L.upipe_selftest_bounds.restype = ctypes.c_int
+        L.upipe_gemm_tile_order.argtypes = [ctypes.c_int] * 5 + [
+            ctypes.POINTER(ctypes.c_int32), ctypes.c_int64]
+        L.upipe_gemm_tile_order.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -338,6 +341,17 @@ def selftest_bounds(stream=None) -> bool:
     _check(lib().upipe_selftest_bounds(_stream(stream), ctypes.byref(written)),
            "upipe_selftest_bounds")
     return written.value == 1
+
+
+def gemm_tile_order(num_m: int, num_n: int, kb_total: int, ksplit: int = 1,
+                    m_fastest: int = 0) -> list:
+    """upipe_gemm_tile_order: the persistent GEMM's tile walk, one
+    (row block, column tile, first K block, end K block) tuple per tile index."""
+    n = num_m * num_n * ksplit
+    out = (ctypes.c_int32 * (4 * n))()
+    _check(lib().upipe_gemm_tile_order(num_m, num_n, kb_total, ksplit, m_fastest, out, 4 * n),
+           "upipe_gemm_tile_order")
+    return [tuple(out[4 * t:4 * t + 4]) for t in range(n)]
 
 
 def last_error() -> int:

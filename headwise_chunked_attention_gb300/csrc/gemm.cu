@@ -92,8 +92,9 @@ struct GemmMaps {
 // operand that stays in L2), or with m_fastest = G > 1 the same within groups
 // of G row blocks, group after group (B is read once per group, and only a
 // group's A rows cycle).
-__device__ __forceinline__ TileCoord tile_coord(int t, int num_m, int num_n, int kb_total,
-                                                int ksplit, int tile_rows, int m_fastest) {
+// (Host and device: the host copy backs upipe_gemm_tile_order.)
+__host__ __device__ __forceinline__ TileCoord tile_coord(int t, int num_m, int num_n, int kb_total,
+                                                         int ksplit, int tile_rows, int m_fastest) {
   const int per_split = num_m * num_n;
   const int ks = t / per_split;
   const int r = t - ks * per_split;
@@ -103,7 +104,8 @@ __device__ __forceinline__ TileCoord tile_coord(int t, int num_m, int num_n, int
     // columns, then the next group (only a group's A rows need stay in L2)
     const int group = r / (m_fastest * num_n);
     const int rem = r - group * m_fastest * num_n;
-    const int gm = min(m_fastest, num_m - group * m_fastest);
+    const int left = num_m - group * m_fastest;   // row blocks in this group
+    const int gm = left < m_fastest ? left : m_fastest;
     c.m0 = (group * m_fastest + rem % gm) * tile_rows;
     c.n0 = rem / gm;
   } else if (m_fastest) {
@@ -115,7 +117,7 @@ __device__ __forceinline__ TileCoord tile_coord(int t, int num_m, int num_n, int
   }
   const int kb_per = (kb_total + ksplit - 1) / ksplit;
   c.kb0 = ks * kb_per;
-  c.kb1 = min(kb_total, c.kb0 + kb_per);
+  c.kb1 = kb_total < c.kb0 + kb_per ? kb_total : c.kb0 + kb_per;
   return c;
 }
 
@@ -879,3 +881,19 @@ cudaError_t launch_gemm(int bn, bool a_mn, bool b_mn, EpiKind epi, const CUtenso
 }
 
 }  // namespace upipe
+
+extern "C" int upipe_gemm_tile_order(int num_m, int num_n, int kb_total, int ksplit,
+                                     int m_fastest, int32_t* out, int64_t out_len) {
+  if (num_m < 1 || num_n < 1 || kb_total < 1 || ksplit < 1 || m_fastest < 0 || !out)
+    return UPIPE_ERR_INVALID_ARG;
+  const long long tiles = (long long)num_m * num_n * ksplit;
+  if (tiles > INT32_MAX || out_len < 4 * tiles) return UPIPE_ERR_INVALID_ARG;
+  for (int t = 0; t < (int)tiles; ++t) {
+    const upipe::TileCoord c = upipe::tile_coord(t, num_m, num_n, kb_total, ksplit, 1, m_fastest);
+    out[4 * t] = c.m0;
+    out[4 * t + 1] = c.n0;
+    out[4 * t + 2] = c.kb0;
+    out[4 * t + 3] = c.kb1;
+  }
+  return UPIPE_OK;
+}

@@ -382,6 +382,23 @@ int upipe_debug_bounds(void);
  * Returns UPIPE_OK, UPIPE_ERR_INVALID_ARG (written NULL) or UPIPE_ERR_CUDA. */
 int upipe_selftest_bounds(void* stream, int* written);
 
+/* The output-tile walk of the library's persistent GEMM (no counterpart on
+ * the pages): the host copy of the device function by which every GEMM
+ * launch maps a tile index to its work.  A launch covers num_m 128-row
+ * blocks x num_n column tiles x ksplit partitions of the kb_total 64-wide K
+ * blocks; each CTA takes tile indices blockIdx.x, blockIdx.x + gridDim.x, ...
+ * For tile t the call writes out[4t .. 4t+3] = (row block, column tile,
+ * first K block, one past the last K block); the K range is empty when the
+ * partitions outnumber what kb_total fills.  m_fastest orders the tiles of a
+ * partition: 0 column tiles fastest, 1 row blocks fastest, G > 1 row blocks
+ * fastest within groups of G row blocks, group after group.  out holds
+ * out_len int32 elements (caller-owned host memory, at least
+ * 4 * num_m * num_n * ksplit).  Host function, no device work.
+ * Returns UPIPE_OK, or UPIPE_ERR_INVALID_ARG for a count below 1, a negative
+ * m_fastest, more than 2^31 - 1 tiles, or out NULL or short. */
+int upipe_gemm_tile_order(int num_m, int num_n, int kb_total, int ksplit, int m_fastest,
+                          int32_t* out, int64_t out_len);
+
 /* Synchronises the current device, then returns and clears the device error
  * word (UPIPE_OK, UPIPE_ERR_DEVICE_TIMEOUT, UPIPE_ERR_RANGE, UPIPE_ERR_TARGET
  * or, in the debug build, UPIPE_ERR_BOUNDS: the first error a kernel recorded
