@@ -887,7 +887,9 @@ extern "C" int upipe_gemm_tile_order(int num_m, int num_n, int kb_total, int ksp
   if (num_m < 1 || num_n < 1 || kb_total < 1 || ksplit < 1 || m_fastest < 0 || !out)
     return UPIPE_ERR_INVALID_ARG;
   const long long tiles = (long long)num_m * num_n * ksplit;
-  if (tiles > INT32_MAX || out_len < 4 * tiles) return UPIPE_ERR_INVALID_ARG;
+  // the walk forms m_fastest * num_n in int
+  if (tiles > INT32_MAX || (long long)m_fastest * num_n > INT32_MAX || out_len < 4 * tiles)
+    return UPIPE_ERR_INVALID_ARG;
   for (int t = 0; t < (int)tiles; ++t) {
     const upipe::TileCoord c = upipe::tile_coord(t, num_m, num_n, kb_total, ksplit, 1, m_fastest);
     out[4 * t] = c.m0;

@@ -395,7 +395,8 @@ int upipe_selftest_bounds(void* stream, int* written);
  * out_len int32 elements (caller-owned host memory, at least
  * 4 * num_m * num_n * ksplit).  Host function, no device work.
  * Returns UPIPE_OK, or UPIPE_ERR_INVALID_ARG for a count below 1, a negative
- * m_fastest, more than 2^31 - 1 tiles, or out NULL or short. */
+ * m_fastest, more than 2^31 - 1 tiles, m_fastest * num_n above 2^31 - 1, or
+ * out NULL or short. */
 int upipe_gemm_tile_order(int num_m, int num_n, int kb_total, int ksplit, int m_fastest,
                           int32_t* out, int64_t out_len);
 

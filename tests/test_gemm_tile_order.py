@@ -117,7 +117,7 @@ def test_invalid_arguments_are_rejected(u):
     buf = (ctypes.c_int32 * 64)()
     assert L.upipe_gemm_tile_order(2, 2, 4, 1, 0, buf, 64) == code["UPIPE_OK"]
     for args in [(0, 2, 4, 1, 0), (2, 0, 4, 1, 0), (2, 2, 0, 1, 0), (2, 2, 4, 0, 0),
-                 (2, 2, 4, 1, -1)]:
+                 (2, 2, 4, 1, -1), (2, 2, 4, 1, 2 ** 30)]:
         assert L.upipe_gemm_tile_order(*args, buf, 64) == invalid, args
     # short output buffer, NULL output
     assert L.upipe_gemm_tile_order(4, 4, 4, 1, 0, buf, 63) == invalid
